@@ -1,0 +1,141 @@
+"""CPU oracle for the token-sparse MLA forward (test infrastructure only).
+
+Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference leg
+may import this package.  The product path (token_sparse_mla_gb300) never loads
+it, and it never loads the product path: the two share no code.
+
+The arithmetic lives in sparse_mla_oracle.c (plain C, fp64, OpenMP over
+(token, head) pairs); this module compiles it with gcc and marshals arrays.
+See the C file's header for the definition it computes and the passages it
+follows.
+"""
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "sparse_mla_oracle.c"
+_LIB_PATH = _HERE / "liboracle_smla.so"
+_lib = None
+
+KV_FORMATS = {"bf16": 0, "fp8": 1}
+
+
+def build(force: bool = False) -> Path:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math)."""
+    if force or not _LIB_PATH.exists() or _LIB_PATH.stat().st_mtime < _SRC.stat().st_mtime:
+        tmp = _LIB_PATH.with_suffix(f".{os.getpid()}.tmp")
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+               "-o", str(tmp), str(_SRC), "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(str(build()))
+        lib.oracle_sparse_mla_fwd.restype = ctypes.c_int
+        lib.oracle_sparse_mla_fwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_e4m3_table.restype = None
+        lib.oracle_e4m3_table.argtypes = [ctypes.c_void_p]
+        lib.oracle_bf16_value.restype = ctypes.c_double
+        lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_row.restype = None
+        lib.oracle_decode_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_void_p]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def _as_np(x, dtype=None) -> np.ndarray:
+    """torch CPU tensor or numpy array -> C-contiguous numpy array (bf16 as uint16 bits)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                x = x.view(torch.int16)
+            x = x.numpy()
+    except ImportError:
+        pass
+    a = np.ascontiguousarray(x)
+    if dtype is not None:
+        a = a.view(dtype) if a.dtype.itemsize == np.dtype(dtype).itemsize else a.astype(dtype)
+    return a
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def sparse_mla_fwd(q, kv, indices, scale: float, kv_format: str = "bf16",
+                   tokens: Optional[Sequence[int]] = None,
+                   threads: Optional[int] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Exact sparse MLA forward in fp64.
+
+    q        [T, h, 576] bf16 (torch bf16 tensor, or uint16 bit patterns)
+    kv       bf16 [num_slots, 576], or uint8 [num_slots, 656] fp8 rows
+    indices  [T, topk] int32
+    tokens   optional token ids to evaluate (default: all)
+    returns  out [n, h, 512] float64 and lse [n, h] float64 (n = len(tokens) or T)
+    """
+    lib = _load()
+    qn = _as_np(q, np.uint16)
+    kvn = _as_np(kv, np.uint16 if kv_format == "bf16" else np.uint8)
+    idn = _as_np(indices, np.int32)
+    T, h, d = qn.shape
+    assert d == 576, qn.shape
+    topk = idn.shape[1]
+    assert idn.shape[0] == T
+    num_slots = kvn.shape[0]
+    if kv_format == "bf16":
+        assert kvn.shape[1] == 576
+    else:
+        assert kvn.shape[1] == 656
+    if tokens is None:
+        tok = None
+        n = T
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        n = tok.shape[0]
+    out = np.empty((n, h, 512), dtype=np.float64)
+    lse = np.empty((n, h), dtype=np.float64)
+    rc = lib.oracle_sparse_mla_fwd(
+        qn.ctypes.data, kvn.ctypes.data, KV_FORMATS[kv_format], idn.ctypes.data,
+        T, h, topk, num_slots, float(scale),
+        None if tok is None else tok.ctypes.data, n,
+        out.ctypes.data, lse.ctypes.data, int(threads or 0))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out, lse
+
+
+def e4m3_table() -> np.ndarray:
+    t = np.empty(256, dtype=np.float64)
+    _load().oracle_e4m3_table(t.ctypes.data)
+    return t
+
+
+def bf16_value(bits: int) -> float:
+    return float(_load().oracle_bf16_value(int(bits) & 0xFFFF))
+
+
+def decode_row(kv, kv_format: str, slot: int) -> np.ndarray:
+    kvn = _as_np(kv, np.uint16 if kv_format == "bf16" else np.uint8)
+    assert 0 <= slot < kvn.shape[0]
+    row = np.empty(576, dtype=np.float64)
+    _load().oracle_decode_row(kvn.ctypes.data, KV_FORMATS[kv_format], int(slot),
+                              row.ctypes.data)
+    return row

@@ -1,0 +1,202 @@
+/*
+ * Oracle for the token-sparse MLA attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this file:
+ * only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * leg load it.  It shares no code, header, table or constant with the CUDA
+ * library; both sides only read the same seeded inputs.
+ *
+ * What it computes (the plain definition, in fp64, two passes, no blocking):
+ * for every query token t and head h, with the per-token list idx[t, 0:topk]
+ * of int32 slots into a latent KV cache whose rows have 576 dims (512 latent +
+ * 64 rope, one KV head):
+ *
+ *   valid(j)  <=>  0 <= idx[t,j] < num_slots          (-1 marks an invalid entry)
+ *   s_j       =   scale * sum_{d<576} q[t,h,d] * kv[idx[t,j], d]
+ *   m         =   max_{valid j} s_j
+ *   l         =   sum_{valid j} exp(s_j - m)
+ *   O[t,h,d]  =   sum_{valid j} exp(s_j - m) * kv[idx[t,j], d] / l,  d < 512
+ *   LSE[t,h]  =   m + ln(l)          (natural log of the sum of exp of SCALED logits)
+ *   no valid j:   O = 0, LSE = -inf
+ *
+ * Each list entry is its own softmax term, so a slot listed k times weighs k.
+ *
+ * Sources (page title, section):
+ *  - vLLM PR #60220 "FlashMLA sparse: stage fp8 mixed-batch q/out in the
+ *    workspace", Claims: q is T x heads x 576 bf16 and the output is
+ *    T x heads x 512 bf16; Details: the kernel also returns lse (T x 64 x 4 B).
+ *  - PR #55738 report, 功能与动机 (motivation): prefill tokens go through a
+ *    "per-token top-k MQA kernel" -- one KV head shared by all query heads,
+ *    each token attending to its own top-k rows.
+ *  - PR #55738 report, `_is_masked_mha_available` geometry table:
+ *    kv_lora_rank 512 and qk_rope_head_dim 64, hence 576-dim keys whose first
+ *    512 dims are the values.
+ *  - vLLM PR #54951 "Shard long-context indexer prefill rows", Summary and
+ *    Additional checks: the index lists are fixed-width int32 and only the SET
+ *    of selected rows matters (top-k order is not deterministic).
+ *  - vLLM PR #60220, Overview: the sparse kernel also reads a quantised
+ *    latent cache (fp8_ds_mla).  The pages do not give its byte layout; this
+ *    oracle reads [512 x e4m3 | 4 x fp32 scale per 128 dims | 64 x bf16 rope]
+ *    (656 bytes) and computes latent[d] = e4m3(byte[d]) * scale[d / 128]
+ *    exactly in fp64.
+ *
+ * bf16 -> fp64 and e4m3 -> fp64 are exact; the e4m3 values come from the
+ * format's definition (OCP 8-bit floating point, E4M3: bias 7, 3 mantissa bits,
+ * exponent field 0 = subnormal, S.1111.111 = NaN, no infinities, max 448).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_DQK 576
+#define ORACLE_DV 512
+#define ORACLE_FP8_ROW 656
+
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_FP8 = 1 };
+
+static double bf16_bits_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* E4M3 value of one byte, from the format definition. */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7);      /* subnormal: m/8 * 2^(1-bias) */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7); /* normal: (1 + m/8) * 2^(e-bias) */
+    return sign ? -v : v;
+}
+
+void oracle_e4m3_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e4m3_value((uint8_t)c);
+}
+
+double oracle_bf16_value(uint16_t bits) { return bf16_bits_to_double(bits); }
+
+/* Decode one cache row to 576 fp64 values. */
+void oracle_decode_row(const void *kv, int kv_format, int64_t slot, double *row) {
+    if (kv_format == ORACLE_KV_BF16) {
+        const uint16_t *r = (const uint16_t *)kv + slot * (int64_t)ORACLE_DQK;
+        for (int d = 0; d < ORACLE_DQK; ++d) row[d] = bf16_bits_to_double(r[d]);
+    } else {
+        const uint8_t *r = (const uint8_t *)kv + slot * (int64_t)ORACLE_FP8_ROW;
+        float tile_scale[4];
+        memcpy(tile_scale, r + 512, sizeof tile_scale);
+        for (int d = 0; d < 512; ++d)
+            row[d] = oracle_e4m3_value(r[d]) * (double)tile_scale[d / 128];
+        for (int d = 0; d < 64; ++d) {
+            uint16_t b;
+            memcpy(&b, r + 528 + 2 * d, sizeof b);
+            row[512 + d] = bf16_bits_to_double(b);
+        }
+    }
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * q        [T, h, 576] bf16 bit patterns
+ * kv       [num_slots, 576] bf16, or [num_slots] rows of 656 bytes (fp8)
+ * idx      [T, topk] int32
+ * tokens   optional list of n_tokens token ids to evaluate (NULL: all T, n_tokens = T)
+ * out      [n_tokens, h, 512] fp64;  lse [n_tokens, h] fp64
+ * returns 0 on success, 1 on a bad argument, 2 if memory ran out
+ */
+int oracle_sparse_mla_fwd(const uint16_t *q, const void *kv, int kv_format,
+                          const int32_t *idx, int64_t T, int h, int topk,
+                          int64_t num_slots, double scale, const int64_t *tokens,
+                          int64_t n_tokens, double *out, double *lse, int nthreads) {
+    if (T < 0 || h <= 0 || topk <= 0 || num_slots <= 0 || n_tokens < 0) return 1;
+    if (kv_format != ORACLE_KV_BF16 && kv_format != ORACLE_KV_FP8) return 1;
+    if (n_tokens > 0 && (!q || !kv || !idx || !out || !lse)) return 1;
+    if (!tokens && n_tokens != T) return 1;
+    if (tokens)
+        for (int64_t i = 0; i < n_tokens; ++i)
+            if (tokens[i] < 0 || tokens[i] >= T) return 1;
+
+    int failed = 0;
+    int64_t pairs = n_tokens * (int64_t)h;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)topk);
+        double *row = (double *)malloc(sizeof(double) * ORACLE_DQK);
+        double qv[ORACLE_DQK], acc[ORACLE_DV];
+        if (!s || !row) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t p = 0; p < pairs; ++p) {
+            if (!s || !row) continue;
+            int64_t i = p / h;
+            int hh = (int)(p % h);
+            int64_t t = tokens ? tokens[i] : i;
+            const uint16_t *qr = q + (t * h + hh) * (int64_t)ORACLE_DQK;
+            const int32_t *list = idx + t * (int64_t)topk;
+            double *o = out + (i * h + hh) * (int64_t)ORACLE_DV;
+
+            for (int d = 0; d < ORACLE_DQK; ++d) qv[d] = bf16_bits_to_double(qr[d]);
+
+            /* pass 1: scaled logits of the valid entries and their maximum */
+            double m = -INFINITY;
+            int n_valid = 0;
+            for (int j = 0; j < topk; ++j) {
+                int64_t slot = list[j];
+                if (slot < 0 || slot >= num_slots) continue;
+                oracle_decode_row(kv, kv_format, slot, row);
+                double dot = 0.0;
+                for (int d = 0; d < ORACLE_DQK; ++d) dot += qv[d] * row[d];
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+                ++n_valid;
+            }
+            if (n_valid == 0) {
+                for (int d = 0; d < ORACLE_DV; ++d) o[d] = 0.0;
+                lse[i * h + hh] = -INFINITY;
+                continue;
+            }
+
+            /* pass 2: softmax weights and the weighted sum of the value rows */
+            double l = 0.0;
+            for (int d = 0; d < ORACLE_DV; ++d) acc[d] = 0.0;
+            for (int j = 0; j < topk; ++j) {
+                int64_t slot = list[j];
+                if (slot < 0 || slot >= num_slots) continue;
+                double w = exp(s[j] - m);
+                l += w;
+                oracle_decode_row(kv, kv_format, slot, row);
+                for (int d = 0; d < ORACLE_DV; ++d) acc[d] += w * row[d];
+            }
+            for (int d = 0; d < ORACLE_DV; ++d) o[d] = acc[d] / l;
+            lse[i * h + hh] = m + log(l);
+        }
+        free(s);
+        free(row);
+    }
+    return failed ? 2 : 0;
+}

@@ -1,0 +1,27 @@
+"""Seeded synthetic workloads for the token-sparse MLA forward.
+
+This package only draws random inputs (queries, a paged latent KV cache, block
+tables and per-token top-k slot lists) and packs them into the layouts the
+kernel and the oracle read.  It contains none of the attention arithmetic, so
+both sides of every parity check can take their inputs from here.
+"""
+
+from .configs import CONFIGS, WorkloadConfig, config_by_name
+from .generators import (
+    Workload,
+    gathered_bytes,
+    make_workload,
+    pad_heads,
+    quantize_fp8_rows,
+)
+
+__all__ = [
+    "CONFIGS",
+    "WorkloadConfig",
+    "config_by_name",
+    "Workload",
+    "gathered_bytes",
+    "make_workload",
+    "pad_heads",
+    "quantize_fp8_rows",
+]
