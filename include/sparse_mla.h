@@ -1,0 +1,150 @@
+/*
+ * sparse_mla.h -- C ABI of libsparse_mla.so, the token-sparse MLA attention
+ * forward for GB300 (sm_103a).
+ *
+ * What the library computes.  Each query token t has h heads of 576-dim bf16
+ * queries (512 latent + 64 rope dims) and its own list of `topk` int32 slot
+ * indices into a paged compact latent KV cache (one KV head, 576 dims per
+ * row).  For every head:
+ *     s_j    = scale * <q[t,h,:], kv[idx[t,j], :]>            (all 576 dims)
+ *     P      = softmax over the valid j (idx in [0, num_slots); -1 = invalid)
+ *     O[t,h] = sum_j P_j * kv[idx[t,j], 0:512]                (V = latent part)
+ *     LSE    = ln sum_j exp(s_j)                              (natural log, fp32)
+ * An index list with no valid entry gives O = 0 and LSE = -inf.  Each list
+ * entry is a separate softmax term (a slot listed twice counts twice).
+ *
+ * Sources (page title, section):
+ *   vLLM PR #60220 "FlashMLA sparse: stage fp8 mixed-batch q/out in the
+ *   workspace" -- Claims: q is T x heads x 576 bf16, out is T x heads x 512 bf16
+ *   and is passed in by the caller (out=); Details: the kernel returns lse and
+ *   should not allocate per call (o_accum, q padding).
+ *   vLLM PR #64510 "Enable existing native 8/16/32-head kernels in SM90 BF16
+ *   sparse FlashMLA" -- Overview/Details: 8, 16 and 32 heads per rank run
+ *   natively instead of being padded to 64; padding, when wanted, is the
+ *   caller's (zero heads whose outputs are discarded).
+ *   PR #55738 report, 功能与动机 (motivation): the "per-token top-k MQA kernel"
+ *   is bound by the HBM traffic of its KV gather.
+ *   vLLM PR #54951 "Shard long-context indexer prefill rows across TP" --
+ *   Summary: the index lists are fixed-width int32.
+ *
+ * Conventions for every entry point below:
+ *   - Device pointers belong to the caller; the library allocates no device or
+ *     host memory per call and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).
+ *   - A non-OK return means nothing was launched.  Device-side failures (a
+ *     bounded wait inside the kernel that ran out) are recorded in a device
+ *     error word and reported by sparse_mla_sync_status().
+ *   - sparse_mla_last_error() gives a message for the last non-OK return of
+ *     the calling host thread.
+ */
+#ifndef SPARSE_MLA_H_
+#define SPARSE_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMLA_D_QK 576          /* query/key dims: 512 latent + 64 rope */
+#define SMLA_D_V 512           /* value/output dims: the latent part */
+#define SMLA_BF16_ROW_BYTES 1152
+#define SMLA_FP8_ROW_BYTES 656 /* 512 x e4m3 | 4 x fp32 tile scales | 64 x bf16 rope */
+
+typedef enum smla_status {
+    SMLA_OK = 0,
+    SMLA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or scale */
+    SMLA_ERR_UNSUPPORTED = 2,  /* head count or KV format this build does not run */
+    SMLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    SMLA_ERR_TIMEOUT = 4       /* a bounded wait inside a kernel gave up */
+} smla_status;
+
+typedef enum smla_kv_format {
+    SMLA_KV_BF16 = 0,          /* rows of 576 bf16 (1152 bytes) */
+    SMLA_KV_FP8 = 1            /* rows of 656 bytes: 512 e4m3 latent values, then
+                                  4 fp32 scales (one per 128 latent values), then
+                                  64 bf16 rope values; latent[d] = e4m3[d] * scale[d/128] */
+} smla_kv_format;
+
+/*
+ * sparse_mla_fwd -- the forward pass.
+ *   q          device, [T, h, 576] bf16, contiguous, 16-byte aligned
+ *   kv_cache   device, [num_slots, 576] bf16 (SMLA_KV_BF16) or [num_slots] rows
+ *              of 656 bytes (SMLA_KV_FP8), contiguous, 16-byte aligned
+ *   indices    device, [T, topk] int32, contiguous, 4-byte aligned; entries
+ *              outside [0, num_slots) (-1 by convention) are masked out
+ *   T          query tokens (T = 0 is a no-op that returns SMLA_OK)
+ *   h          heads per token: 8, 16, 32 or 64, all run natively
+ *   topk       list length, >= 1
+ *   num_slots  rows in the cache, 1 .. 2^31-1
+ *   scale      softmax scale applied to the logits, finite
+ *   out        device, [T, h, 512] bf16, written (caller-owned)
+ *   lse        device, [T, h] fp32, written (caller-owned)
+ * Returns SMLA_OK once the kernel is queued.
+ */
+smla_status sparse_mla_fwd(const void* q, const void* kv_cache, const int32_t* indices,
+                           int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                           int32_t kv_format, float scale, void* out, float* lse,
+                           void* stream);
+
+/*
+ * sparse_mla_fwd_ex -- sparse_mla_fwd with an explicit split count.
+ * splits = 0 lets the library choose (what sparse_mla_fwd does).  splits in
+ * {1, 2, 4, 8} splits each token's list over that many CTAs of one thread-block
+ * cluster, merged on chip by log-sum-exp weights; other values are
+ * SMLA_ERR_INVALID_ARG.  Results agree with any other split count up to fp32
+ * rounding.
+ */
+smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t* indices,
+                              int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                              int32_t kv_format, float scale, void* out, float* lse,
+                              int32_t splits, void* stream);
+
+/*
+ * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the
+ * per-step inputs and outputs, for callers whose q/indices live in host memory.
+ * It queues on `stream`: copies of q_host and indices_host into `workspace`,
+ * the kernel, and copies of out/lse back into out_host/lse_host.  The KV cache
+ * stays a device pointer (it is state resident on the GPU).  Host buffers
+ * should be pinned for the copies to be asynchronous; the results are in
+ * out_host/lse_host once the stream has been synchronised.
+ *   workspace        device, at least sparse_mla_host_workspace_bytes(T,h,topk)
+ *                    bytes, 256-byte aligned, caller-owned
+ */
+size_t sparse_mla_host_workspace_bytes(int32_t T, int32_t h, int32_t topk);
+smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_cache,
+                                const int32_t* indices_host, int32_t T, int32_t h,
+                                int32_t topk, int64_t num_slots, int32_t kv_format,
+                                float scale, void* out_host, float* lse_host,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sparse_mla_sync_status -- synchronise `stream`, then read and clear the
+ * device error word of the current device.  Returns SMLA_ERR_TIMEOUT if a
+ * kernel gave up on a bounded wait since the last call, SMLA_ERR_CUDA if the
+ * synchronisation failed, SMLA_OK otherwise.  Not for the hot path.
+ */
+smla_status sparse_mla_sync_status(void* stream);
+
+/*
+ * sparse_mla_launch_info -- how sparse_mla_fwd would launch (T, h, topk):
+ * split count, CTAs in the grid, dynamic shared memory per CTA in bytes and
+ * kernel launches per call.  Any output pointer may be NULL.
+ */
+smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t kv_format,
+                                   int32_t* splits, int32_t* ctas, int32_t* smem_bytes,
+                                   int32_t* launches);
+
+/* Message for the calling thread's last non-OK return ("" if none). */
+const char* sparse_mla_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t sparse_mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H_ */

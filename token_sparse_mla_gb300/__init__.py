@@ -1,0 +1,39 @@
+"""token_sparse_mla_gb300: token-sparse MLA attention forward for GB300 (sm_103a).
+
+The work runs in the CUDA kernels of libsparse_mla.so; this module only
+marshals torch tensors into the library's C ABI (include/sparse_mla.h).  There
+is no fallback: if the library is missing or the tensors are not on a CUDA
+device, the calls raise.
+
+    out, lse = sparse_mla_fwd(q, kv_cache, indices, scale)
+
+q [T, h, 576] bf16, kv_cache [num_slots, 576] bf16 (or [num_slots, 656] uint8
+fp8 rows), indices [T, topk] int32 (-1 = invalid), h in {8, 16, 32, 64};
+returns out [T, h, 512] bf16 and lse [T, h] fp32.
+"""
+
+from ._binding import (  # noqa: F401
+    KV_FORMATS,
+    SparseMLAError,
+    host_workspace_bytes,
+    launch_info,
+    lib_path,
+    library,
+    sparse_mla_fwd,
+    sparse_mla_fwd_host,
+    sync_status,
+    version,
+)
+
+__all__ = [
+    "KV_FORMATS",
+    "SparseMLAError",
+    "host_workspace_bytes",
+    "launch_info",
+    "lib_path",
+    "library",
+    "sparse_mla_fwd",
+    "sparse_mla_fwd_host",
+    "sync_status",
+    "version",
+]

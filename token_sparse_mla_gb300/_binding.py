@@ -1,0 +1,167 @@
+"""ctypes binding of libsparse_mla.so (argument marshalling only)."""
+
+import ctypes
+from pathlib import Path
+from typing import Optional, Tuple
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "libsparse_mla.so"
+_lib = None
+
+KV_FORMATS = {"bf16": 0, "fp8": 1}
+D_QK, D_V, FP8_ROW_BYTES = 576, 512, 656
+
+_STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED",
+           3: "SMLA_ERR_CUDA", 4: "SMLA_ERR_TIMEOUT"}
+
+EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_ex", "sparse_mla_fwd_host",
+            "sparse_mla_host_workspace_bytes", "sparse_mla_sync_status",
+            "sparse_mla_launch_info", "sparse_mla_last_error", "sparse_mla_version")
+
+
+class SparseMLAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+
+
+def lib_path() -> Path:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load libsparse_mla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                          "`python -m token_sparse_mla_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+    lib.sparse_mla_fwd.restype = ctypes.c_int
+    lib.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp]
+    lib.sparse_mla_fwd_ex.restype = ctypes.c_int
+    lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_host_workspace_bytes.restype = sz
+    lib.sparse_mla_host_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.sparse_mla_fwd_host.restype = ctypes.c_int
+    lib.sparse_mla_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp, sz, vp]
+    lib.sparse_mla_sync_status.restype = ctypes.c_int
+    lib.sparse_mla_sync_status.argtypes = [vp]
+    lib.sparse_mla_launch_info.restype = ctypes.c_int
+    lib.sparse_mla_launch_info.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.sparse_mla_last_error.restype = ctypes.c_char_p
+    lib.sparse_mla_last_error.argtypes = []
+    lib.sparse_mla_version.restype = ctypes.c_int32
+    lib.sparse_mla_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = library().sparse_mla_last_error().decode(errors="replace")
+        raise SparseMLAError(status, msg)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def version() -> int:
+    return int(library().sparse_mla_version())
+
+
+def _dims(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor, kv_format: str):
+    if q.dim() != 3 or q.shape[2] != D_QK or q.dtype != torch.bfloat16:
+        raise ValueError(f"q must be [T, h, 576] bf16, got {tuple(q.shape)} {q.dtype}")
+    T, h = int(q.shape[0]), int(q.shape[1])
+    if indices.dim() != 2 or indices.shape[0] != T or indices.dtype != torch.int32:
+        raise ValueError(f"indices must be [T, topk] int32, got {tuple(indices.shape)} {indices.dtype}")
+    if kv_format not in KV_FORMATS:
+        raise ValueError(f"kv_format must be one of {sorted(KV_FORMATS)}")
+    if kv_format == "bf16":
+        if kv_cache.dim() != 2 or kv_cache.shape[1] != D_QK or kv_cache.dtype != torch.bfloat16:
+            raise ValueError(f"bf16 kv_cache must be [num_slots, 576] bf16, got "
+                             f"{tuple(kv_cache.shape)} {kv_cache.dtype}")
+    else:
+        if kv_cache.dim() != 2 or kv_cache.shape[1] != FP8_ROW_BYTES or kv_cache.dtype != torch.uint8:
+            raise ValueError(f"fp8 kv_cache must be [num_slots, 656] uint8, got "
+                             f"{tuple(kv_cache.shape)} {kv_cache.dtype}")
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    return T, h, int(indices.shape[1]), int(kv_cache.shape[0])
+
+
+def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                   scale: Optional[float] = None, *, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, kv_format: str = "bf16",
+                   splits: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Token-sparse MLA forward on the GPU (see include/sparse_mla.h).
+
+    scale defaults to 576 ** -0.5.  out / lse may be passed in (caller-owned
+    buffers, [T, h, 512] bf16 and [T, h] fp32); otherwise they are allocated
+    here.  splits = 0 lets the library choose how many CTAs share a token's
+    list.  Runs asynchronously on `stream` (default: torch's current stream).
+    """
+    T, h, topk, num_slots = _dims(q, kv_cache, indices, kv_format)
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if scale is None:
+        scale = D_QK ** -0.5
+    if out is None:
+        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, h), dtype=torch.float32, device=q.device)
+    if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
+    if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
+    st = library().sparse_mla_fwd_ex(
+        q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
+        KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
+        _stream_handle(stream))
+    _check(st)
+    return out, lse
+
+
+def host_workspace_bytes(T: int, h: int, topk: int) -> int:
+    return int(library().sparse_mla_host_workspace_bytes(T, h, topk))
+
+
+def sparse_mla_fwd_host(q_host: torch.Tensor, kv_cache: torch.Tensor, indices_host: torch.Tensor,
+                        scale: float, out_host: torch.Tensor, lse_host: torch.Tensor,
+                        workspace: torch.Tensor, *, kv_format: str = "bf16", stream=None) -> None:
+    """Forward pass with host-resident q/indices/out/lse (pinned for async copies);
+    the library queues H2D copies, the kernel and D2H copies on `stream`."""
+    T, h, topk, num_slots = _dims(q_host, kv_cache, indices_host, kv_format)
+    if q_host.is_cuda or indices_host.is_cuda or out_host.is_cuda or lse_host.is_cuda:
+        raise ValueError("q, indices, out and lse must be host tensors here")
+    if not kv_cache.is_cuda or not workspace.is_cuda:
+        raise ValueError("kv_cache and workspace must be CUDA tensors")
+    st = library().sparse_mla_fwd_host(
+        q_host.data_ptr(), kv_cache.data_ptr(), indices_host.data_ptr(), T, h, topk, num_slots,
+        KV_FORMATS[kv_format], float(scale), out_host.data_ptr(), lse_host.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st)
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a device-side error."""
+    _check(library().sparse_mla_sync_status(_stream_handle(stream)))
+
+
+def launch_info(T: int, h: int, topk: int, kv_format: str = "bf16") -> dict:
+    s, c, m, n = (ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32())
+    _check(library().sparse_mla_launch_info(T, h, topk, KV_FORMATS[kv_format], ctypes.byref(s),
+                                            ctypes.byref(c), ctypes.byref(m), ctypes.byref(n)))
+    return {"splits": s.value, "ctas": c.value, "smem_bytes": m.value, "launches": n.value}

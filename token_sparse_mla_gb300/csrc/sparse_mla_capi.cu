@@ -1,0 +1,336 @@
+// C ABI of libsparse_mla.so: argument validation, tensor-map encoding and launch.
+// The declarations, argument meanings and error behaviour are documented in
+// include/sparse_mla.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "sparse_mla.h"
+#include "sparse_mla_kernel.cuh"
+
+namespace {
+
+constexpr int32_t kVersion = 10000;  // 1.0.0
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_error[512] = "";
+
+smla_status fail(smla_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+smla_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(SMLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    int num_sms = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+template <int HP>
+cudaError_t set_kernel_attrs() {
+    auto k = smla::sparse_mla_fwd_bf16_kernel<HP>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smla::Layout<HP>::kBytes);
+    return e;
+}
+
+smla_status device_state(int* dev_out, DeviceState** st_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SMLA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, [&] {
+        cudaDeviceProp prop;
+        cudaError_t err = cudaGetDeviceProperties(&prop, dev);
+        if (err == cudaSuccess && prop.major < 10) err = cudaErrorInvalidDeviceFunction;
+        if (err == cudaSuccess) st.num_sms = prop.multiProcessorCount;
+        if (err == cudaSuccess) err = set_kernel_attrs<16>();
+        if (err == cudaSuccess) err = set_kernel_attrs<32>();
+        if (err == cudaSuccess) err = set_kernel_attrs<64>();
+        st.init_error = err;
+    });
+    if (st.init_error != cudaSuccess) return cuda_fail(st.init_error, "device set-up");
+    *dev_out = dev;
+    *st_out = &st;
+    return SMLA_OK;
+}
+
+smla_status encode_fn(EncodeTiledFn* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!g_encode) return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    *fn = g_encode;
+    return SMLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int pick_mma_n(int h) { return h <= 16 ? 16 : h; }
+
+// Split count: enough CTAs to cover the SMs once when there are few tokens.
+int auto_splits(int64_t T, int nblk, int num_sms) {
+    int s = 1;
+    const int cand[3] = {8, 4, 2};
+    for (int c : cand) {
+        if (c <= nblk && T * c <= num_sms) {
+            s = c;
+            break;
+        }
+    }
+    return s;
+}
+
+struct Plan {
+    int hp = 16;
+    int splits = 1;
+    int64_t ctas = 0;
+    int smem = 0;
+};
+
+smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
+                       int32_t topk, int64_t num_slots, int32_t kv_format, float scale,
+                       const void* out, const float* lse, int32_t splits) {
+    if (T < 0) return fail(SMLA_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
+    if (!(h == 8 || h == 16 || h == 32 || h == 64))
+        return fail(SMLA_ERR_UNSUPPORTED, "h must be 8, 16, 32 or 64 (got %d)", h);
+    if (topk < 1) return fail(SMLA_ERR_INVALID_ARG, "topk must be >= 1 (got %d)", topk);
+    if (num_slots < 1 || num_slots > 0x7fffffffLL)
+        return fail(SMLA_ERR_INVALID_ARG, "num_slots must be in [1, 2^31-1] (got %lld)",
+                    static_cast<long long>(num_slots));
+    if (kv_format != SMLA_KV_BF16 && kv_format != SMLA_KV_FP8)
+        return fail(SMLA_ERR_INVALID_ARG, "unknown kv_format %d", kv_format);
+    if (kv_format == SMLA_KV_FP8)
+        return fail(SMLA_ERR_UNSUPPORTED, "the fp8 KV format is not built in this library version");
+    if (!std::isfinite(scale)) return fail(SMLA_ERR_INVALID_ARG, "scale must be finite");
+    if (!(splits == 0 || splits == 1 || splits == 2 || splits == 4 || splits == 8))
+        return fail(SMLA_ERR_INVALID_ARG, "splits must be 0 (auto), 1, 2, 4 or 8 (got %d)", splits);
+    if (T == 0) return SMLA_OK;
+    if (!q || !kv || !idx || !out || !lse) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
+        return fail(SMLA_ERR_INVALID_ARG, "q, kv_cache and out must be 16-byte aligned");
+    if (!aligned(idx, 4) || !aligned(lse, 4))
+        return fail(SMLA_ERR_INVALID_ARG, "indices and lse must be 4-byte aligned");
+    if (static_cast<int64_t>(T) * 8 > 0x7fffffffLL)
+        return fail(SMLA_ERR_INVALID_ARG, "T too large for one launch (%d)", T);
+    return SMLA_OK;
+}
+
+Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms) {
+    Plan pl;
+    pl.hp = pick_mma_n(h);
+    const int nblk = (topk + smla::kRows - 1) / smla::kRows;
+    pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
+    pl.ctas = static_cast<int64_t>(T) * pl.splits;
+    pl.smem = pl.hp == 16 ? smla::Layout<16>::kBytes
+                          : (pl.hp == 32 ? smla::Layout<32>::kBytes : smla::Layout<64>::kBytes);
+    return pl;
+}
+
+smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
+                   int32_t topk, int64_t num_slots, int32_t kv_format, float scale, void* out,
+                   float* lse, int32_t splits, cudaStream_t stream) {
+    smla_status st = check_args(q, kv, idx, T, h, topk, num_slots, kv_format, scale, out, lse, splits);
+    if (st != SMLA_OK || T == 0) return st;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&dev, &ds)) != SMLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    if ((st = encode_fn(&enc)) != SMLA_OK) return st;
+    const Plan pl = make_plan(T, h, topk, splits, ds->num_sms);
+
+    alignas(64) CUtensorMap tm_kv, tm_q;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kDQK),
+                                    static_cast<cuuint64_t>(num_slots)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kDQK) * 2};
+        const cuuint32_t box[2] = {64, 1};
+        const cuuint32_t es[2] = {1, 1};
+        CUresult r = enc(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor map for kv_cache failed (%d)", (int)r);
+    }
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(smla::kDQK), static_cast<cuuint64_t>(h),
+                                    static_cast<cuuint64_t>(T)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(smla::kDQK) * 2,
+                                       static_cast<cuuint64_t>(smla::kDQK) * 2 * h};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(h), 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
+                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor map for q failed (%d)", (int)r);
+    }
+
+    smla::FwdParams prm;
+    prm.indices = idx;
+    prm.out = reinterpret_cast<__nv_bfloat16*>(out);
+    prm.lse = lse;
+    prm.num_slots = num_slots;
+    prm.T = T;
+    prm.h = h;
+    prm.topk = topk;
+    prm.splits = pl.splits;
+    prm.sm_scale_log2 = scale * 1.4426950408889634f;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+    cfg.blockDim = dim3(smla::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pl.splits > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(pl.splits);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e;
+    if (pl.hp == 16)
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<16>, tm_kv, tm_q, prm);
+    else if (pl.hp == 32)
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<32>, tm_kv, tm_q, prm);
+    else
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<64>, tm_kv, tm_q, prm);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return SMLA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+smla_status sparse_mla_fwd(const void* q, const void* kv_cache, const int32_t* indices, int32_t T,
+                           int32_t h, int32_t topk, int64_t num_slots, int32_t kv_format,
+                           float scale, void* out, float* lse, void* stream) {
+    return launch(q, kv_cache, indices, T, h, topk, num_slots, kv_format, scale, out, lse, 0,
+                  static_cast<cudaStream_t>(stream));
+}
+
+smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t* indices,
+                              int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                              int32_t kv_format, float scale, void* out, float* lse, int32_t splits,
+                              void* stream) {
+    return launch(q, kv_cache, indices, T, h, topk, num_slots, kv_format, scale, out, lse, splits,
+                  static_cast<cudaStream_t>(stream));
+}
+
+size_t sparse_mla_host_workspace_bytes(int32_t T, int32_t h, int32_t topk) {
+    if (T <= 0 || h <= 0 || topk <= 0) return 0;
+    const size_t t = static_cast<size_t>(T);
+    return align256(t * h * smla::kDQK * 2) + align256(t * topk * 4) + align256(t * h * smla::kDV * 2) +
+           align256(t * h * 4);
+}
+
+smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_cache, const int32_t* indices_host,
+                                int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                                int32_t kv_format, float scale, void* out_host, float* lse_host,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    if (T == 0) return check_args(q_host, kv_cache, indices_host, T, h, topk, num_slots, kv_format,
+                                  scale, out_host, lse_host, 0);
+    if (T < 0 || h <= 0 || topk <= 0)
+        return check_args(q_host, kv_cache, indices_host, T, h, topk, num_slots, kv_format, scale,
+                          out_host, lse_host, 0);
+    if (!q_host || !indices_host || !out_host || !lse_host || !workspace)
+        return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(workspace, 256)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = sparse_mla_host_workspace_bytes(T, h, topk);
+    if (workspace_bytes < need)
+        return fail(SMLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, need);
+    const size_t t = static_cast<size_t>(T);
+    const size_t q_bytes = t * h * smla::kDQK * 2, i_bytes = t * topk * 4;
+    const size_t o_bytes = t * h * smla::kDV * 2, l_bytes = t * h * 4;
+    char* w = static_cast<char*>(workspace);
+    void* q_dev = w;
+    int32_t* i_dev = reinterpret_cast<int32_t*>(w + align256(q_bytes));
+    void* o_dev = w + align256(q_bytes) + align256(i_bytes);
+    float* l_dev = reinterpret_cast<float*>(w + align256(q_bytes) + align256(i_bytes) + align256(o_bytes));
+    smla_status st = check_args(q_dev, kv_cache, i_dev, T, h, topk, num_slots, kv_format, scale, o_dev,
+                                l_dev, 0);
+    if (st != SMLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(i_dev, indices_host, i_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    st = launch(q_dev, kv_cache, i_dev, T, h, topk, num_slots, kv_format, scale, o_dev, l_dev, 0, s);
+    if (st != SMLA_OK) return st;
+    e = cudaMemcpyAsync(out_host, o_dev, o_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, l_dev, l_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return SMLA_OK;
+}
+
+smla_status sparse_mla_sync_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, smla::g_smla_error, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(smla::g_smla_error, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (word & smla::kErrTimeout)
+            return fail(SMLA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (error word 0x%x)", word);
+        return fail(SMLA_ERR_CUDA, "kernel reported an error (error word 0x%x)", word);
+    }
+    return SMLA_OK;
+}
+
+smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t kv_format,
+                                   int32_t* splits, int32_t* ctas, int32_t* smem_bytes,
+                                   int32_t* launches) {
+    if (T < 0 || topk < 1) return fail(SMLA_ERR_INVALID_ARG, "bad T or topk");
+    if (!(h == 8 || h == 16 || h == 32 || h == 64))
+        return fail(SMLA_ERR_UNSUPPORTED, "h must be 8, 16, 32 or 64 (got %d)", h);
+    if (kv_format != SMLA_KV_BF16) return fail(SMLA_ERR_UNSUPPORTED, "kv_format %d", kv_format);
+    int num_sms = 152;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&dev, &ds) == SMLA_OK) num_sms = ds->num_sms;
+    const Plan pl = make_plan(T, h, topk, 0, num_sms);
+    if (splits) *splits = pl.splits;
+    if (ctas) *ctas = static_cast<int32_t>(pl.ctas);
+    if (smem_bytes) *smem_bytes = pl.smem;
+    if (launches) *launches = T > 0 ? 1 : 0;
+    return SMLA_OK;
+}
+
+const char* sparse_mla_last_error(void) { return g_last_error; }
+
+int32_t sparse_mla_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,550 @@
+// Token-sparse MLA forward, bf16 latent cache, tcgen05/TMEM tensor cores (sm_103a).
+//
+// One CTA handles one (query token, split) pair: the token's top-k list is cut
+// into `splits` contiguous ranges of 64-row blocks, one per CTA of a thread-block
+// cluster, and the partial results are merged on chip through distributed shared
+// memory (no global workspace; vLLM PR #60220, Details/Limitations, describes the
+// per-call o_accum split-KV buffer this avoids).
+//
+// Roles (192 threads):
+//   warp 0      producer: reads 64 indices per block and gathers the 64 rows with
+//               TMA tile::gather4 (4 rows x 128 bytes per instruction) straight into
+//               the 128-byte-swizzled K-major operand layout, 9 panels of 64 dims.
+//               Invalid indices are out-of-range rows, which TMA fills with zeros.
+//   warp 1      MMA issuer (one thread) and TMEM owner.  Swap-AB form, so the head
+//               count only has to fill the MMA's N dimension (no padding to 64):
+//                 S^T[64 rows, HP heads]  = K_blk[64 x 576] . Q^T        (M=64)
+//                 O^T[512 dims, HP heads] += V_blk^T[512 x 64] . P^T     (4 x M=128)
+//               V^T is read from the SAME shared-memory tile as K, as an MN-major
+//               operand (the 128B-swizzled K-major K tile is the 128B-swizzled
+//               MN-major layout of V^T).
+//   warps 2-5   softmax warpgroup: reads S^T from TMEM (one KV row per thread,
+//               all heads), masks invalid entries, keeps a running max per head in
+//               log2 units and only rescales O when the max grows by more than
+//               2^8 (conditional rescaling), writes P^T (bf16) to shared memory,
+//               and runs the epilogue (O / l -> bf16, LSE = ln sum exp).
+//
+// HP is the MMA N size: the head count rounded up to 16 (h = 8 runs N = 16 with
+// the upper 8 query rows zero in shared memory; nothing is padded in HBM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "sm100_ptx.cuh"
+
+namespace smla {
+
+constexpr int kDQK = 576;
+constexpr int kDV = 512;
+constexpr int kRows = 64;                           // KV rows per pipeline stage
+constexpr int kPanels = kDQK / 64;                  // 9 panels of 64 bf16 = 128 bytes per row
+constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
+constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;    // draining in-flight work after an abort
+
+// device error word bits (read by sparse_mla_sync_status)
+constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrLayout = 2u;
+
+template <int HP>
+struct Layout {
+    static_assert(HP == 16 || HP == 32 || HP == 64, "MMA N must be 16, 32 or 64");
+    static constexpr int kQBytes = kPanels * HP * 128;
+    static constexpr int kPBytes = HP * 128;  // P^T: HP rows x 64 bf16
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQBytes;
+    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffIdx = kOffP + kPBytes;
+    static constexpr int kOffRed = kOffIdx + kStages * kRows * 4;  // [4 warps][HP]
+    static constexpr int kOffM = kOffRed + 4 * HP * 4;             // running max (log2 units)
+    static constexpr int kOffAlpha = kOffM + HP * 4;               // rescale factor / 1/L / merge weight
+    static constexpr int kOffML = kOffAlpha + HP * 4;              // final m[HP], L[HP]
+    static constexpr int kOffBar = kOffML + 2 * HP * 4;
+    static constexpr int kNumBars = 12;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kTmemCols = (6 * HP <= 128) ? 128 : ((6 * HP <= 256) ? 256 : 512);
+    static constexpr int kColS = 4 * HP;                     // S^T double buffer after O^T
+    static constexpr int kObufStride = HP + 1;               // merge buffer: fp32 per dim row
+    static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
+    static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
+    static_assert(kDV * kObufStride * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
+};
+
+struct FwdParams {
+    const int32_t* indices;  // [T, topk]
+    __nv_bfloat16* out;      // [T, h, 512]
+    float* lse;              // [T, h]
+    int64_t num_slots;
+    int32_t T, h, topk, splits;
+    float sm_scale_log2;     // scale * log2(e)
+};
+
+__device__ unsigned int g_smla_error;
+
+// barrier slots
+enum : int {
+    kBarQ = 0,
+    kBarKvFull = 1,   // +stage
+    kBarKvEmpty = 3,  // +stage
+    kBarSFull = 5,    // +buffer
+    kBarSEmpty = 7,   // +buffer
+    kBarPFull = 9,
+    kBarPvDone = 10,
+    kBarDrain = 11
+};
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+template <int HP>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                               const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+    using L = Layout<HP>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = ptx::smem_u32(smem);
+    if (sbase & 1023u) {  // uniform across the grid: every CTA leaves before any barrier
+        if (threadIdx.x == 0) atomicOr(&g_smla_error, kErrLayout);
+        return;
+    }
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t sQ = sbase + L::kOffQ;
+    const uint32_t sKV = sbase + L::kOffKV;
+    const uint32_t sP = sbase + L::kOffP;
+    int32_t* sIdx = reinterpret_cast<int32_t*>(smem + L::kOffIdx);
+    float* sRed = reinterpret_cast<float*>(smem + L::kOffRed);
+    float* sM = reinterpret_cast<float*>(smem + L::kOffM);
+    float* sAlpha = reinterpret_cast<float*>(smem + L::kOffAlpha);
+    float* sML = reinterpret_cast<float*>(smem + L::kOffML);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * static_cast<uint32_t>(i); };
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        return ptx::mbar_wait(bar(i), parity, sAbort, &g_smla_error, kErrTimeout, kWaitLimitNs);
+    };
+
+    // ---- work of this CTA
+    const int splits = p.splits;
+    const int t = blockIdx.x / splits;
+    const int rank = blockIdx.x % splits;  // == %cluster_ctarank when splits > 1
+    const int nblk_total = (p.topk + kRows - 1) / kRows;
+    const int per_split = (nblk_total + splits - 1) / splits;
+    const int b_begin = min(nblk_total, rank * per_split);
+    const int b_end = min(nblk_total, b_begin + per_split);
+    const int nb = b_end - b_begin;
+    const int j0 = b_begin * kRows;             // first list entry of this CTA
+    const int j1 = min(p.topk, b_end * kRows);  // one past the last
+
+    // ---- set-up
+    if (threadIdx.x == 0) {
+        *sAbort = 0;
+        ptx::mbar_init(bar(kBarQ), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar(kBarKvFull + s), 1);
+            ptx::mbar_init(bar(kBarKvEmpty + s), 1);
+            ptx::mbar_init(bar(kBarSFull + s), 1);
+            ptx::mbar_init(bar(kBarSEmpty + s), 4);
+        }
+        ptx::mbar_init(bar(kBarPFull), 4);
+        ptx::mbar_init(bar(kBarPvDone), 1);
+        ptx::mbar_init(bar(kBarDrain), 1);
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(sbase + L::kOffMisc, L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp >= 2) {
+        const int wtid = threadIdx.x - 64;
+        if (p.h < HP) {  // zero the query rows h..HP-1 of every panel (MMA N padding)
+            const int pad_rows = HP - p.h;
+            const int n16 = kPanels * pad_rows * 8;
+            for (int i = wtid; i < n16; i += 128) {
+                const int pn = i / (pad_rows * 8);
+                const int rem = i % (pad_rows * 8);
+                uint4* dst = reinterpret_cast<uint4*>(smem + L::kOffQ + pn * HP * 128 +
+                                                      (p.h + rem / 8) * 128 + (rem % 8) * 16);
+                *dst = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (wtid < HP) sM[wtid] = -CUDART_INF_F;
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *sTmem;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        int issued = 0;
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_kv);
+            ptx::prefetch_tmap(&tm_q);
+            ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
+            for (int pn = 0; pn < kPanels; ++pn)
+                ptx::tma_load_3d(sQ + pn * HP * 128, &tm_q, pn * 64, 0, t, bar(kBarQ));
+        }
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(t) * p.topk;
+        for (int b = 0; b < nb; ++b) {
+            const int s = b & 1;
+            if (b >= kStages) {
+                bool ok = false;
+                if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            }
+            const int j = j0 + b * kRows + 2 * lane;
+            const int i0 = (j < j1) ? ptx::ld_nc_s32(idx_row + j) : -1;
+            const int i1 = (j + 1 < j1) ? ptx::ld_nc_s32(idx_row + j + 1) : -1;
+            reinterpret_cast<int2*>(sIdx + s * kRows)[lane] = make_int2(i0, i1);
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t full = bar(kBarKvFull + s);
+                ptx::mbar_arrive_expect_tx(full, kStageBytes);
+                const uint32_t dst0 = sKV + s * kStageBytes;
+#pragma unroll 1
+                for (int g = 0; g < kRows / 4; ++g) {
+                    const int4 r4 = reinterpret_cast<const int4*>(sIdx + s * kRows)[g];
+#pragma unroll
+                    for (int pn = 0; pn < kPanels; ++pn)
+                        ptx::tma_gather4(dst0 + pn * kPanelBytes + g * 512, &tm_kv, pn * 64, r4.x,
+                                         r4.y, r4.z, r4.w, full);
+                }
+            }
+            __syncwarp();
+            issued = b + 1;
+        }
+        if (lane == 0 && *sAbort) {  // leave no copy in flight into this CTA's memory
+            ptx::mbar_wait(bar(kBarQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+            for (int b = max(0, issued - kStages); b < issued; ++b)
+                ptx::mbar_wait(bar(kBarKvFull + (b & 1)), (b >> 1) & 1, nullptr, &g_smla_error, 0u,
+                               kDrainLimitNs);
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(64, HP, 0, 0);
+            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
+            auto issue_s = [&](int b) {
+                const int s = b & 1;
+                const uint32_t kv = sKV + s * kStageBytes;
+                const uint32_t d = tmem + L::kColS + s * HP;
+#pragma unroll
+                for (int pn = 0; pn < kPanels; ++pn) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t a = ptx::smem_desc_sw128(kv + pn * kPanelBytes + k * 32, 16, 1024);
+                        const uint64_t bq = ptx::smem_desc_sw128(sQ + pn * HP * 128 + k * 32, 16, 1024);
+                        ptx::mma_bf16_ss(d, a, bq, kIdescS, (pn | k) != 0);
+                    }
+                }
+                ptx::mma_commit(bar(kBarSFull + s));
+            };
+            bool ok = wait(kBarQ, 0);
+            if (ok && nb > 0) {
+                ok = wait(kBarKvFull + 0, 0);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0);
+                }
+            }
+            for (int b = 0; ok && b < nb; ++b) {
+                if (b + 1 < nb) {
+                    const int s1 = (b + 1) & 1;
+                    ok = wait(kBarKvFull + s1, ((b + 1) >> 1) & 1);
+                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, (((b + 1) >> 1) - 1) & 1);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s(b + 1);
+                }
+                ok = wait(kBarPFull, b & 1);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const int s = b & 1;
+                const uint32_t kv = sKV + s * kStageBytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t a =
+                            ptx::smem_desc_sw128(kv + 2 * i * kPanelBytes + k * 2048, kPanelBytes, 1024);
+                        const uint64_t bp = ptx::smem_desc_sw128(sP + k * 32, 16, 1024);
+                        ptx::mma_bf16_ss(tmem + i * HP, a, bp, kIdescPV, (b > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+                ptx::mma_commit(bar(kBarKvEmpty + s));
+                ptx::mma_commit(bar(kBarPvDone));
+            }
+            ptx::mma_commit(bar(kBarDrain));
+            ptx::mbar_wait(bar(kBarDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax warpgroup
+        const int wtid = threadIdx.x - 64;
+        const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const int r = quad * 16 + lane;  // KV row within the block (M=64 layout: lanes 0-15)
+        const bool row_lane = lane < 16;
+        const float c = p.sm_scale_log2;
+        float l[HP];
+#pragma unroll
+        for (int h = 0; h < HP; ++h) l[h] = 0.f;
+        bool failed = false;
+
+        for (int b = 0; b < nb; ++b) {
+            if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
+                failed = true;
+                break;
+            }
+            const int s = b & 1;
+            bool ok = true;
+            if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1) && wait(kBarKvFull + s, (b >> 1) & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            uint32_t sv[HP];
+            bool need = false;
+            if (ok) {
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < HP / 16; ++cc)
+                    SMLA_TMEM_LD16(tmem + lane_base + L::kColS + s * HP + cc * 16, &sv[cc * 16]);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + s));
+                const int slot = sIdx[s * kRows + (row_lane ? r : 0)];
+                const int jj = j0 + b * kRows + r;
+                const bool valid = row_lane && jj < j1 && slot >= 0 &&
+                                   static_cast<int64_t>(slot) < p.num_slots;
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
+                    const float x = valid ? __uint_as_float(sv[h]) * c : -CUDART_INF_F;
+                    sv[h] = __float_as_uint(x);
+                    need |= x > sM[h] + kRescaleLog2;
+                }
+            } else {
+                failed = true;
+#pragma unroll
+                for (int h = 0; h < HP; ++h) sv[h] = __float_as_uint(-CUDART_INF_F);
+            }
+            bool pv_waited = false;
+            if (ptx::named_bar_red_or(1, 128, need)) {
+                // the running max of some head grew: new max, rescale l and O
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
+                    const float v = ptx::warp_max_f32(__uint_as_float(sv[h]));
+                    if (lane == 0) sRed[quad * HP + h] = v;
+                }
+                ptx::named_bar_sync(1, 128);
+                if (wtid < HP) {
+                    const float mo = sM[wtid];
+                    const float mb = fmaxf(fmaxf(sRed[wtid], sRed[HP + wtid]),
+                                           fmaxf(sRed[2 * HP + wtid], sRed[3 * HP + wtid]));
+                    const float mn = fmaxf(mo, mb);
+                    sAlpha[wtid] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(mo - mn);
+                    sM[wtid] = mn;
+                }
+                ptx::named_bar_sync(1, 128);
+#pragma unroll
+                for (int h = 0; h < HP; ++h) l[h] *= sAlpha[h];
+                if (b > 0) {
+                    bool okw = true;
+                    if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
+                    okw = __shfl_sync(0xffffffffu, okw, 0);
+                    pv_waited = true;
+                    if (okw) {
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                            for (int cc = 0; cc < HP / 16; ++cc) {
+                                uint32_t o[16];
+                                const uint32_t ta = tmem + lane_base + i * HP + cc * 16;
+                                SMLA_TMEM_LD16(ta, o);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * sAlpha[cc * 16 + e]);
+                                SMLA_TMEM_ST16(ta, o);
+                            }
+                        }
+                        ptx::tmem_wait_st();
+                    } else {
+                        failed = true;
+                    }
+                }
+            }
+            if (b > 0 && !pv_waited) {  // P^T has one buffer: the previous PV must be done
+                bool okw = true;
+                if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
+                if (!__shfl_sync(0xffffffffu, okw, 0)) failed = true;
+            }
+            // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout
+#pragma unroll
+            for (int h = 0; h < HP; ++h) {
+                const float x = __uint_as_float(sv[h]);
+                const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
+                l[h] += pr;
+                if (row_lane) {
+                    const uint32_t off = (h >> 3) * 1024 + (h & 7) * 128 +
+                                         ((((r >> 3) ^ (h & 7)) << 4) | ((r & 7) << 1));
+                    ptx::st_shared_u16(sP + off, bf16_bits(pr));
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));
+        }
+
+        // ---- per-head totals: L = sum of this CTA's probabilities
+        const bool aborted = ptx::named_bar_red_or(1, 128, failed || *sAbort);
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+            float v = l[h];
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            if (lane == 0) sRed[quad * HP + h] = v;
+        }
+        ptx::named_bar_sync(1, 128);
+        if (wtid < HP) {
+            const float tot = sRed[wtid] + sRed[HP + wtid] + sRed[2 * HP + wtid] + sRed[3 * HP + wtid];
+            sML[wtid] = sM[wtid];
+            sML[HP + wtid] = tot;
+            sAlpha[wtid] = tot > 0.f ? 1.0f / tot : 0.f;
+        }
+        ptx::named_bar_sync(1, 128);
+        // the last PV
+        if (nb > 0 && !aborted) {
+            bool okw = true;
+            if (lane == 0) okw = wait(kBarPvDone, (nb - 1) & 1);
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            if (okw) ptx::tc_fence_after();
+            failed = !okw;
+        } else {
+            failed = aborted;
+        }
+        const bool have_o = nb > 0 && !failed;
+
+        if (splits == 1 && !aborted) {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                uint32_t ov[HP];
+                if (have_o) {
+#pragma unroll
+                    for (int cc = 0; cc < HP / 16; ++cc)
+                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, &ov[cc * 16]);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) ov[h] = 0u;
+                }
+                const int d = i * 128 + quad * 32 + lane;
+                __nv_bfloat16* orow = p.out + static_cast<int64_t>(t) * p.h * kDV + d;
+#pragma unroll
+                for (int h = 0; h < HP; ++h)
+                    if (h < p.h) orow[h * kDV] = __float2bfloat16_rn(__uint_as_float(ov[h]) * sAlpha[h]);
+            }
+            if (wtid < p.h) {
+                const float tot = sML[HP + wtid];
+                p.lse[static_cast<int64_t>(t) * p.h + wtid] =
+                    tot > 0.f ? (sML[wtid] + log2f(tot)) * 0.69314718055994531f : -CUDART_INF_F;
+            }
+        }
+        ptx::tc_fence_before();
+        if (splits > 1) sAbort[0] = sAbort[0] | (failed ? 1 : 0);
+    }
+
+    __syncthreads();
+
+    if (splits > 1) {
+        // ================================================================ cluster merge
+        ptx::cluster_sync();  // every CTA's (m, L) is in its shared memory
+        if (warp >= 2) {
+            const int wtid = threadIdx.x - 64;
+            const int quad = warp & 3;
+            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+            const bool have_o = nb > 0 && *sAbort == 0;
+            if (wtid < HP) {
+                const uint32_t a_m = ptx::smem_u32(sML + wtid);
+                const uint32_t a_l = ptx::smem_u32(sML + HP + wtid);
+                float M = -CUDART_INF_F;
+                for (int k = 0; k < splits; ++k)
+                    M = fmaxf(M, ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k)));
+                float Lt = 0.f;
+                for (int k = 0; k < splits; ++k) {
+                    const float mk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k));
+                    const float lk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_l, k));
+                    if (mk != -CUDART_INF_F) Lt += lk * ptx::ex2_approx(mk - M);
+                }
+                const float mine = sML[wtid];
+                sAlpha[wtid] = (Lt > 0.f && mine != -CUDART_INF_F) ? ptx::ex2_approx(mine - M) / Lt : 0.f;
+                if (rank == 0 && wtid < p.h)
+                    p.lse[static_cast<int64_t>(t) * p.h + wtid] =
+                        Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
+            }
+            ptx::named_bar_sync(1, 128);
+            float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                uint32_t ov[HP];
+                if (have_o) {
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < HP / 16; ++cc)
+                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, &ov[cc * 16]);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) ov[h] = 0u;
+                }
+                const int d = i * 128 + quad * 32 + lane;
+#pragma unroll
+                for (int h = 0; h < HP; ++h)
+                    obuf[d * L::kObufStride + h] = __uint_as_float(ov[h]) * sAlpha[h];
+            }
+            ptx::tc_fence_before();
+        }
+        ptx::cluster_sync();  // every CTA's weighted partial O is in its shared memory
+        if (warp >= 2) {
+            const int wtid = threadIdx.x - 64;
+            const int ds = kDV / splits;
+            const uint32_t ob = sbase + L::kOffKV;
+            for (int it = wtid; it < p.h * ds; it += 128) {
+                const int hh = it / ds;
+                const int dd = rank * ds + it % ds;
+                const uint32_t a = ob + static_cast<uint32_t>((dd * L::kObufStride + hh) * 4);
+                float acc = 0.f;
+                for (int k = 0; k < splits; ++k)
+                    acc += ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a, k));
+                p.out[(static_cast<int64_t>(t) * p.h + hh) * kDV + dd] = __float2bfloat16_rn(acc);
+            }
+        }
+        ptx::cluster_sync();  // no CTA leaves while a peer still reads its shared memory
+    }
+
+    // ---- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace smla
