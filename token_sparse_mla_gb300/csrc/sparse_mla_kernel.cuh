@@ -203,7 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (b >= kStages) {
                 bool ok = false;
                 if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                __syncwarp();
+                if (!ok) break;
             }
             const int j = j0 + b * kRows + 2 * lane;
             const int i0 = (j < j1) ? ptx::ld_nc_s32(idx_row + j) : -1;
@@ -313,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1) && wait(kBarKvFull + s, (b >> 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
             uint32_t sv[HP];
             bool need = false;
             if (ok) {
@@ -363,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool okw = true;
                     if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
                     okw = __shfl_sync(0xffffffffu, okw, 0);
+                    __syncwarp();
                     pv_waited = true;
                     if (okw) {
                         ptx::tc_fence_after();
@@ -390,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool okw = true;
                 if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) failed = true;
+                __syncwarp();
             }
             // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout
 #pragma unroll
@@ -434,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool okw = true;
             if (lane == 0) okw = wait(kBarPvDone, (nb - 1) & 1);
             okw = __shfl_sync(0xffffffffu, okw, 0);
+            __syncwarp();
             if (okw) ptx::tc_fence_after();
             failed = !okw;
         } else {
