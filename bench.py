@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the token-sparse MLA forward (one JSON line on stdout).
+
+Default workload: the bf16 decode batch -- 32 sequences x 16384 cached tokens
+in a paged cache (block 64, random block table), one query token per sequence,
+h = 8 heads, top-k = 2048 distinct valid slots per token.  A step is one
+sparse_mla_fwd call over the whole batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+L2: each step uses the next of R independently drawn input sets (own cache,
+indices and queries); R is chosen so that R x gathered bytes >= 2 x L2, so a
+step never finds its rows in L2 from the previous steps.
+
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores on the
+same workload, a bounded number of tokens per step.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path shards by query token with no exchange), weak scaling.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+from workloads import config_by_name, gathered_bytes, make_workload, pad_heads  # noqa: E402
+
+METRIC = "query-tokens/s and gathered-KV HBM GB/s (fraction of roofline) at topk=2048"
+UNIT = "query-tokens/s"
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+KERNEL_SOURCES = ["token_sparse_mla_gb300/csrc/sparse_mla_kernel.cuh",
+                  "token_sparse_mla_gb300/csrc/sm100_ptx.cuh",
+                  "token_sparse_mla_gb300/csrc/sparse_mla_capi.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update((ROOT / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def ncu_traffic(workload: str, h: int, pad: bool):
+    """Per-launch DRAM bytes from the committed ncu summary, if it is for this kernel source."""
+    p = ROOT / "profiles" / "ncu_traffic.json"
+    if not p.exists():
+        return None
+    try:
+        d = json.loads(p.read_text())
+    except ValueError:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    key = f"{workload}/h{h}{'/pad64' if pad else ''}"
+    e = d.get("entries", {}).get(key)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (1 rank: itself)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_rate(w, budget_s: float, max_tokens_per_call: int = 32):
+    """Time the oracle on the host cores over tokens of workload w, for about budget_s seconds."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    toks = list(range(min(w.T, max_tokens_per_call)))
+    done, elapsed, calls = 0, 0.0, 0
+    while elapsed < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format=w.kv_format, tokens=toks)
+        elapsed += time.perf_counter() - t0
+        done += len(toks)
+        calls += 1
+    return done / elapsed, threads, done, elapsed
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    name = args.workload
+    w = make_workload(name, h=args.h)
+    if args.pad:
+        w.q = pad_heads(w.q, 64)
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    # calibrate one token, then size each step so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format=w.kv_format, tokens=[0])
+    t_tok = max(time.perf_counter() - t0, 1e-4)
+    per_step = max(1, min(w.T, int(120.0 / (args.steps + args.warmup) / t_tok)))
+    toks = [i % w.T for i in range(per_step)]
+    for _ in range(args.warmup):
+        oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format=w.kv_format, tokens=toks[:1])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format=w.kv_format, tokens=toks)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w, args, splits=None, rot=1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} query tokens of the workload per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args, splits, rot):
+    cfg = w.cfg
+    return {"workload": cfg.name, "T": w.T, "h": int(w.q.shape[1]), "h_real": w.h,
+            "padded_to_64": bool(args.pad), "topk": w.topk, "kv_format": cfg.kv_format,
+            "num_slots": w.num_slots, "block_size": 64, "splits": splits,
+            "l2": f"rotating {rot} independently drawn input sets (cache, indices, q); "
+                  f"{rot} x gathered bytes >= 2 x L2"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import token_sparse_mla_gb300 as smla
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    name = args.workload
+    cfg = config_by_name(name)
+    base = make_workload(name, h=args.h, seed=cfg.seed + 7919 * rank)
+    gb_step = gathered_bytes(base.indices, base.num_slots, cfg.row_bytes)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or L2_BYTES_DEFAULT
+    rot = args.rot or max(1, min(8, math.ceil(2 * l2 / max(gb_step, 1))))
+    sets = [base] + [make_workload(name, h=args.h, seed=cfg.seed + 100 * i + 7919 * rank)
+                     for i in range(1, rot)]
+    if args.pad:
+        for w in sets:
+            w.q = pad_heads(w.q, 64)
+    T, H, topk = sets[0].T, int(sets[0].q.shape[1]), sets[0].topk
+    qs = [w.q.to(dev) for w in sets]
+    kvs = [w.kv.to(dev) for w in sets]
+    ids = [w.indices.to(dev) for w in sets]
+    outs = [torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev) for _ in sets]
+    lses = [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in sets]
+    gbytes = [gathered_bytes(w.indices, w.num_slots, cfg.row_bytes) for w in sets]
+    stream = torch.cuda.current_stream(dev)
+    info = smla.launch_info(T, H, topk, cfg.kv_format)
+
+    def step(i):
+        k = i % rot
+        smla.sparse_mla_fwd(qs[k], kvs[k], ids[k], sets[k].scale, out=outs[k], lse=lses[k],
+                            kv_format=cfg.kv_format, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    smla.sync_status(stream)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    # keep the GPU busy for ~0.3 s before the timed region so the clock samples see load
+    t_pre = time.time()
+    i = 0
+    while time.time() - t_pre < 0.3:
+        step(i)
+        i += 1
+        if i % 256 == 0:
+            torch.cuda.synchronize(dev)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    barrier()
+    t_dev = ev0.elapsed_time(ev1) / 1e3
+    clocks.stop()
+    smla.sync_status(stream)
+    t_dev = max_over_ranks(t_dev, world, dev)
+    value = world * T * args.steps / t_dev
+    per_launch = t_dev / args.steps
+    avg_gb = sum(gbytes[i % rot] for i in range(args.steps)) / args.steps
+    peaks = measured_peaks()
+    achieved = avg_gb / per_launch / 1e9
+    traffic = ncu_traffic(name, base.h, args.pad)
+
+    # ---- end to end through the host-buffer entry point: H2D inputs, kernel, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        qh = [w.q.contiguous().pin_memory() for w in sets]
+        ih = [w.indices.contiguous().pin_memory() for w in sets]
+        oh = [torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory() for _ in sets]
+        lh = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in sets]
+        ws = torch.empty(smla.host_workspace_bytes(T, H, topk), dtype=torch.uint8, device=dev)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+        def estep(i):
+            k = i % rot
+            smla.sparse_mla_fwd_host(qh[k], kvs[k], ih[k], sets[k].scale, oh[k], lh[k], ws,
+                                     kv_format=cfg.kv_format, stream=stream)
+        for i in range(max(3, args.warmup // 10)):
+            estep(i)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            estep(i)
+        e1.record(stream)
+        barrier()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+        smla.sync_status(stream)
+        t_e2e = max_over_ranks(t_e2e, world, dev)
+        h2d = qh[0].numel() * 2 + ih[0].numel() * 4
+        d2h = oh[0].numel() * 2 + lh[0].numel() * 4
+        e2e = {"value": world * T * e2e_steps / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "path": "sparse_mla_fwd_host (pinned host q/indices in, out/lse back; cache resident)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, ntok, el = oracle_rate(base, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{ntok} query tokens (the workload's first {min(base.T, 32)} tokens, "
+                         f"repeated) in {el:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_launch * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(base, args, info["splits"], rot),
+        "gathered_gbps": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"],
+                     "per_launch_algorithmic_bytes": avg_gb,
+                     "kernel": "sparse_mla_fwd_bf16_kernel"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+        "gpu_launches": info["launches"] * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--h", type=int, default=None, help="head count (sweep workload)")
+    ap.add_argument("--pad", action="store_true", help="zero-pad the heads to 64")
+    ap.add_argument("--rot", type=int, default=0, help="input sets to rotate (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

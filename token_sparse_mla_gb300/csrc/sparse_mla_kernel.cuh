@@ -262,15 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_s(0);
                 }
             }
+            // PV(b) is issued before waiting for block b+1's rows, so the stage of block b
+            // is released (and refilled with block b+2) while block b+1 is still landing.
             for (int b = 0; ok && b < nb; ++b) {
-                if (b + 1 < nb) {
-                    const int s1 = (b + 1) & 1;
-                    ok = wait(kBarKvFull + s1, ((b + 1) >> 1) & 1);
-                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, (((b + 1) >> 1) - 1) & 1);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_s(b + 1);
-                }
                 ok = wait(kBarPFull, b & 1);
                 if (!ok) break;
                 ptx::tc_fence_after();
@@ -288,6 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
+                if (b + 1 < nb) {
+                    const int s1 = (b + 1) & 1;
+                    ok = wait(kBarKvFull + s1, ((b + 1) >> 1) & 1);
+                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, (((b + 1) >> 1) - 1) & 1);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_s(b + 1);
+                }
             }
             ptx::mma_commit(bar(kBarDrain));
             ptx::mbar_wait(bar(kBarDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
