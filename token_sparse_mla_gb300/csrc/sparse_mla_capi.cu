@@ -166,18 +166,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     if ((st = encode_fn(&enc)) != SMLA_OK) return st;
     const Plan pl = make_plan(T, h, topk, splits, ds->num_sms);
 
-    alignas(64) CUtensorMap tm_kv, tm_q;
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kDQK),
-                                    static_cast<cuuint64_t>(num_slots)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kDQK) * 2};
-        const cuuint32_t box[2] = {64, 1};
-        const cuuint32_t es[2] = {1, 1};
-        CUresult r = enc(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
-                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor map for kv_cache failed (%d)", (int)r);
-    }
+    alignas(64) CUtensorMap tm_q;
     {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(smla::kDQK), static_cast<cuuint64_t>(h),
                                     static_cast<cuuint64_t>(T)};
@@ -192,6 +181,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     }
 
     smla::FwdParams prm;
+    prm.kv = reinterpret_cast<const __nv_bfloat16*>(kv);
     prm.indices = idx;
     prm.out = reinterpret_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
@@ -218,11 +208,11 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     }
     cudaError_t e;
     if (pl.hp == 16)
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<16>, tm_kv, tm_q, prm);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<16>, tm_q, prm);
     else if (pl.hp == 32)
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<32>, tm_kv, tm_q, prm);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<32>, tm_q, prm);
     else
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<64>, tm_kv, tm_q, prm);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<64>, tm_q, prm);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return SMLA_OK;
 }

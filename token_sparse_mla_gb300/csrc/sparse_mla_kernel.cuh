@@ -6,23 +6,28 @@
 // memory (no global workspace; vLLM PR #60220, Details/Limitations, describes the
 // per-call o_accum split-KV buffer this avoids).
 //
-// Roles (192 threads):
-//   warp 0      producer: reads 64 indices per block and gathers the 64 rows with
-//               TMA tile::gather4 (4 rows x 128 bytes per instruction) straight into
-//               the 128-byte-swizzled K-major operand layout, 9 panels of 64 dims.
-//               Invalid indices are out-of-range rows, which TMA fills with zeros.
-//   warp 1      MMA issuer (one thread) and TMEM owner.  Swap-AB form, so the head
+// The pass is bound by the KV row gather (PR #55738 report, 功能与动机: the
+// per-token top-k MQA kernel is HBM-bound by its KV gather).  Rows are fetched
+// with 16-byte cp.async from seven producer warps, one warp per row at a time
+// (each warp instruction moves 512 contiguous bytes of a row), written straight
+// into the 128-byte-swizzled K-major operand layout; invalid entries are
+// zero-filled without a memory read.
+//
+// Roles (384 threads):
+//   warp 0      MMA issuer (one thread) and TMEM owner.  Swap-AB form, so the head
 //               count only has to fill the MMA's N dimension (no padding to 64):
-//                 S^T[64 rows, HP heads]  = K_blk[64 x 576] . Q^T        (M=64)
-//                 O^T[512 dims, HP heads] += V_blk^T[512 x 64] . P^T     (4 x M=128)
+//                 S^T[64 rows, HP]        = K_blk[64 x 576] . Q^T          (M=64)
+//                 O^T[512 dims, HP]      += V_blk^T[512 x 64] . P^T        (4 x M=128)
+//                 Lrep[128, HP]          += ONES[128 x 64] . P^T           (M=128)
 //               V^T is read from the SAME shared-memory tile as K, as an MN-major
-//               operand (the 128B-swizzled K-major K tile is the 128B-swizzled
-//               MN-major layout of V^T).
-//   warps 2-5   softmax warpgroup: reads S^T from TMEM (one KV row per thread,
-//               all heads), masks invalid entries, keeps a running max per head in
-//               log2 units and only rescales O when the max grows by more than
-//               2^8 (conditional rescaling), writes P^T (bf16) to shared memory,
-//               and runs the epilogue (O / l -> bf16, LSE = ln sum exp).
+//               operand.  ONES is an all-ones bf16 matrix kept in TMEM (the A
+//               operand of the last product), so every lane of Lrep holds the
+//               per-head sum of the bf16 probabilities that entered O.
+//   warps 1-7   producers: cp.async gather of 64 rows per stage, 2 stages.
+//   warps 8-11  softmax warpgroup: reads S^T from TMEM (one KV row per thread, all
+//               heads), masks invalid entries, keeps a running max per head in
+//               log2 units and only rescales O and L when that max grows by more
+//               than 2^8, writes P^T (bf16) to shared memory, runs the epilogue.
 //
 // HP is the MMA N size: the head count rounded up to 16 (h = 8 runs N = 16 with
 // the upper 8 query rows zero in shared memory; nothing is padded in HBM).
@@ -45,10 +50,13 @@ constexpr int kPanels = kDQK / 64;                  // 9 panels of 64 bf16 = 128
 constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
 constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kProducerWarps = 7;
+constexpr int kThreads = 32 * (1 + kProducerWarps + 4);  // 384
+constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
 constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;    // draining in-flight work after an abort
+constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;       // two bf16 1.0 values
 
 // device error word bits (read by sparse_mla_sync_status)
 constexpr unsigned int kErrTimeout = 1u;
@@ -62,8 +70,7 @@ struct Layout {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffIdx = kOffP + kPBytes;
-    static constexpr int kOffRed = kOffIdx + kStages * kRows * 4;  // [4 warps][HP]
+    static constexpr int kOffRed = kOffP + kPBytes;                // [4 warps][HP]
     static constexpr int kOffM = kOffRed + 4 * HP * 4;             // running max (log2 units)
     static constexpr int kOffAlpha = kOffM + HP * 4;               // rescale factor / 1/L / merge weight
     static constexpr int kOffML = kOffAlpha + HP * 4;              // final m[HP], L[HP]
@@ -71,21 +78,26 @@ struct Layout {
     static constexpr int kNumBars = 12;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kOffMisc + 16;
-    static constexpr int kTmemCols = (6 * HP <= 128) ? 128 : ((6 * HP <= 256) ? 256 : 512);
-    static constexpr int kColS = 4 * HP;                     // S^T double buffer after O^T
-    static constexpr int kObufStride = HP + 1;               // merge buffer: fp32 per dim row
+    // TMEM columns: O^T [0,4HP) | L [4HP,5HP) | S^T x2 [5HP,7HP) | ONES [7HP, 7HP+64)
+    static constexpr int kColL = 4 * HP;
+    static constexpr int kColS = 5 * HP;
+    static constexpr int kColOnes = 7 * HP;
+    static constexpr int kTmemCols = (7 * HP + 64 <= 256) ? 256 : 512;
+    static constexpr int kObufStride = HP + 1;  // merge buffer: fp32 per dim row
+    static_assert(7 * HP + 64 <= kTmemCols, "TMEM budget");
     static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kDV * kObufStride * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
 };
 
 struct FwdParams {
-    const int32_t* indices;  // [T, topk]
-    __nv_bfloat16* out;      // [T, h, 512]
-    float* lse;              // [T, h]
+    const __nv_bfloat16* kv;  // [num_slots, 576]
+    const int32_t* indices;   // [T, topk]
+    __nv_bfloat16* out;       // [T, h, 512]
+    float* lse;               // [T, h]
     int64_t num_slots;
     int32_t T, h, topk, splits;
-    float sm_scale_log2;     // scale * log2(e)
+    float sm_scale_log2;      // scale * log2(e)
 };
 
 __device__ unsigned int g_smla_error;
@@ -106,10 +118,16 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+// Slot of list entry j, or -1 when j is past this CTA's range or the index is invalid.
+__device__ __forceinline__ int entry_slot(const int32_t* idx_row, int j, int j1, int64_t num_slots) {
+    if (j >= j1) return -1;
+    const int s = ptx::ld_nc_s32(idx_row + j);
+    return (s >= 0 && static_cast<int64_t>(s) < num_slots) ? s : -1;
+}
+
 template <int HP>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
-                               const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+    sparse_mla_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
     using L = Layout<HP>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -123,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = sbase + L::kOffQ;
     const uint32_t sKV = sbase + L::kOffKV;
     const uint32_t sP = sbase + L::kOffP;
-    int32_t* sIdx = reinterpret_cast<int32_t*>(smem + L::kOffIdx);
     float* sRed = reinterpret_cast<float*>(smem + L::kOffRed);
     float* sM = reinterpret_cast<float*>(smem + L::kOffM);
     float* sAlpha = reinterpret_cast<float*>(smem + L::kOffAlpha);
@@ -146,13 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb = b_end - b_begin;
     const int j0 = b_begin * kRows;             // first list entry of this CTA
     const int j1 = min(p.topk, b_end * kRows);  // one past the last
+    const int32_t* idx_row = p.indices + static_cast<int64_t>(t) * p.topk;
 
     // ---- set-up
     if (threadIdx.x == 0) {
         *sAbort = 0;
         ptx::mbar_init(bar(kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar(kBarKvFull + s), 1);
+            ptx::mbar_init(bar(kBarKvFull + s), 32 * kProducerWarps);
             ptx::mbar_init(bar(kBarKvEmpty + s), 1);
             ptx::mbar_init(bar(kBarSFull + s), 1);
             ptx::mbar_init(bar(kBarSEmpty + s), 4);
@@ -162,88 +180,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarDrain), 1);
         ptx::fence_mbarrier_init();
     }
-    if (warp == 1) {
+    if (warp == 0) {
         ptx::tmem_alloc(sbase + L::kOffMisc, L::kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (warp >= 2) {
-        const int wtid = threadIdx.x - 64;
-        if (p.h < HP) {  // zero the query rows h..HP-1 of every panel (MMA N padding)
-            const int pad_rows = HP - p.h;
-            const int n16 = kPanels * pad_rows * 8;
-            for (int i = wtid; i < n16; i += 128) {
-                const int pn = i / (pad_rows * 8);
-                const int rem = i % (pad_rows * 8);
-                uint4* dst = reinterpret_cast<uint4*>(smem + L::kOffQ + pn * HP * 128 +
-                                                      (p.h + rem / 8) * 128 + (rem % 8) * 16);
-                *dst = make_uint4(0u, 0u, 0u, 0u);
-            }
+    if (warp >= 1 && warp <= kProducerWarps && p.h < HP) {
+        // zero the query rows h..HP-1 of every panel (the MMA N padding of h = 8)
+        const int pad_rows = HP - p.h;
+        const int n16 = kPanels * pad_rows * 8;
+        for (int i = threadIdx.x - 32; i < n16; i += 32 * kProducerWarps) {
+            const int pn = i / (pad_rows * 8);
+            const int rem = i % (pad_rows * 8);
+            *reinterpret_cast<uint4*>(smem + L::kOffQ + pn * HP * 128 + (p.h + rem / 8) * 128 +
+                                      (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
-        if (wtid < HP) sM[wtid] = -CUDART_INF_F;
         ptx::fence_proxy_async_smem();
+    }
+    if (warp > kProducerWarps) {
+        const int wtid = threadIdx.x - kSoftmaxThread0;
+        if (wtid < HP) sM[wtid] = -CUDART_INF_F;
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *sTmem;
+    if (warp > kProducerWarps) {
+        // all-ones A operand of the row-sum product, in every lane of this warp's quadrant
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        uint32_t ones[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ones[e] = kOnesBf16x2;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) SMLA_TMEM_ST16(tmem + lane_base + L::kColOnes + c, ones);
+        ptx::tmem_wait_st();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
 
     if (warp == 0) {
-        // ================================================================ producer
-        int issued = 0;
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tm_kv);
-            ptx::prefetch_tmap(&tm_q);
-            ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
-            for (int pn = 0; pn < kPanels; ++pn)
-                ptx::tma_load_3d(sQ + pn * HP * 128, &tm_q, pn * 64, 0, t, bar(kBarQ));
-        }
-        const int32_t* idx_row = p.indices + static_cast<int64_t>(t) * p.topk;
-        for (int b = 0; b < nb; ++b) {
-            const int s = b & 1;
-            if (b >= kStages) {
-                bool ok = false;
-                if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                __syncwarp();
-                if (!ok) break;
-            }
-            const int j = j0 + b * kRows + 2 * lane;
-            const int i0 = (j < j1) ? ptx::ld_nc_s32(idx_row + j) : -1;
-            const int i1 = (j + 1 < j1) ? ptx::ld_nc_s32(idx_row + j + 1) : -1;
-            reinterpret_cast<int2*>(sIdx + s * kRows)[lane] = make_int2(i0, i1);
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t full = bar(kBarKvFull + s);
-                ptx::mbar_arrive_expect_tx(full, kStageBytes);
-                const uint32_t dst0 = sKV + s * kStageBytes;
-#pragma unroll 1
-                for (int g = 0; g < kRows / 4; ++g) {
-                    const int4 r4 = reinterpret_cast<const int4*>(sIdx + s * kRows)[g];
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        ptx::tma_gather4(dst0 + pn * kPanelBytes + g * 512, &tm_kv, pn * 64, r4.x,
-                                         r4.y, r4.z, r4.w, full);
-                }
-            }
-            __syncwarp();
-            issued = b + 1;
-        }
-        if (lane == 0 && *sAbort) {  // leave no copy in flight into this CTA's memory
-            ptx::mbar_wait(bar(kBarQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
-            for (int b = max(0, issued - kStages); b < issued; ++b)
-                ptx::mbar_wait(bar(kBarKvFull + (b & 1)), (b >> 1) & 1, nullptr, &g_smla_error, 0u,
-                               kDrainLimitNs);
-        }
-    } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(64, HP, 0, 0);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
+            constexpr uint32_t kIdescL = ptx::idesc_bf16_f32(128, HP, 0, 0);
+            ptx::prefetch_tmap(&tm_q);
+            ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
+            for (int pn = 0; pn < kPanels; ++pn)
+                ptx::tma_load_3d(sQ + pn * HP * 128, &tm_q, pn * 64, 0, t, bar(kBarQ));
             auto issue_s = [&](int b) {
                 const int s = b & 1;
                 const uint32_t kv = sKV + s * kStageBytes;
                 const uint32_t d = tmem + L::kColS + s * HP;
-#pragma unroll
+#pragma unroll 1
                 for (int pn = 0; pn < kPanels; ++pn) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -270,15 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 const int s = b & 1;
                 const uint32_t kv = sKV + s * kStageBytes;
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t bp = ptx::smem_desc_sw128(sP + k * 32, 16, 1024);
+                    const uint32_t acc = (b > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int i = 0; i < 4; ++i) {
                         const uint64_t a =
                             ptx::smem_desc_sw128(kv + 2 * i * kPanelBytes + k * 2048, kPanelBytes, 1024);
-                        const uint64_t bp = ptx::smem_desc_sw128(sP + k * 32, 16, 1024);
-                        ptx::mma_bf16_ss(tmem + i * HP, a, bp, kIdescPV, (b > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_bf16_ss(tmem + i * HP, a, bp, kIdescPV, acc);
                     }
+                    ptx::mma_bf16_ts(tmem + L::kColL, tmem + L::kColOnes + k * 8, bp, kIdescL, acc);
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
@@ -293,20 +284,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::mma_commit(bar(kBarDrain));
             ptx::mbar_wait(bar(kBarDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+            if (*sAbort) ptx::mbar_wait(bar(kBarQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
         }
         __syncwarp();
+    } else if (warp <= kProducerWarps) {
+        // ================================================================ producers
+        // warp pw copies rows pw, pw + 7, pw + 14, ... of each 64-row block; lane i < 10
+        // holds the slot of the warp's i-th row.
+        const int pw = warp - 1;
+        const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
+        for (int b = 0; b < nb; ++b) {
+            const int s = b & 1;
+            if (b >= kStages) {
+                bool ok = true;
+                if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                __syncwarp();
+                if (!ok) break;
+            }
+            const int my_row = pw + kProducerWarps * lane;
+            const int my_slot = (lane < 10 && my_row < kRows)
+                                    ? entry_slot(idx_row, j0 + b * kRows + my_row, j1, p.num_slots)
+                                    : -1;
+            const uint32_t st = sKV + s * kStageBytes;
+#pragma unroll 1
+            for (int i = 0; i < 10; ++i) {
+                const int r = pw + kProducerWarps * i;
+                if (r >= kRows) break;
+                const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+                const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
+                const uint32_t nbytes = slot < 0 ? 0u : 16u;
+                const uint32_t dst_row = st + r * 128;
+                const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+                for (int cc = 0; cc < 3; ++cc) {
+                    const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+                    if (c < 72) {
+                        const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
+                        ptx::cp_async_16(dst, src + c * 16, nbytes);
+                    }
+                }
+            }
+            ptx::cp_async_arrive_noinc(bar(kBarKvFull + s));
+        }
+        ptx::cp_async_wait_all();  // no copy may still be in flight when the CTA leaves
     } else {
         // ================================================================ softmax warpgroup
-        const int wtid = threadIdx.x - 64;
+        const int wtid = threadIdx.x - kSoftmaxThread0;
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const int r = quad * 16 + lane;  // KV row within the block (M=64 layout: lanes 0-15)
         const bool row_lane = lane < 16;
         const float c = p.sm_scale_log2;
-        float l[HP];
-#pragma unroll
-        for (int h = 0; h < HP; ++h) l[h] = 0.f;
         bool failed = false;
+        int slot_next = row_lane && nb > 0 ? entry_slot(idx_row, j0 + r, j1, p.num_slots) : -1;
+        // P^T[h][r] sits at pbase[h & 7] + (h >> 3) * 1024 (128B-swizzled K-major rows of 64 bf16)
+        uint32_t pbase[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            pbase[k] = sP + k * 128 + ((((r >> 3) ^ k) << 4) | ((r & 7) << 1));
 
         for (int b = 0; b < nb; ++b) {
             if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
@@ -314,8 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int s = b & 1;
+            const bool valid = slot_next >= 0;
+            slot_next = (row_lane && b + 1 < nb)
+                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + r, j1, p.num_slots)
+                            : -1;
             bool ok = true;
-            if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1) && wait(kBarKvFull + s, (b >> 1) & 1);
+            if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();
             uint32_t sv[HP];
@@ -329,10 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + s));
-                const int slot = sIdx[s * kRows + (row_lane ? r : 0)];
-                const int jj = j0 + b * kRows + r;
-                const bool valid = row_lane && jj < j1 && slot >= 0 &&
-                                   static_cast<int64_t>(slot) < p.num_slots;
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
                     const float x = valid ? __uint_as_float(sv[h]) * c : -CUDART_INF_F;
@@ -346,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool pv_waited = false;
             if (ptx::named_bar_red_or(1, 128, need)) {
-                // the running max of some head grew: new max, rescale l and O
+                // the running max of some head grew: new max, rescale O and L
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
                     const float v = ptx::warp_max_f32(__uint_as_float(sv[h]));
@@ -362,8 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sM[wtid] = mn;
                 }
                 ptx::named_bar_sync(1, 128);
-#pragma unroll
-                for (int h = 0; h < HP; ++h) l[h] *= sAlpha[h];
                 if (b > 0) {
                     bool okw = true;
                     if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
@@ -372,17 +406,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pv_waited = true;
                     if (okw) {
                         ptx::tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < HP / 16; ++cc) {
+                            float a[16];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                            for (int cc = 0; cc < HP / 16; ++cc) {
+                            for (int e = 0; e < 16; ++e) a[e] = sAlpha[cc * 16 + e];
+#pragma unroll 1
+                            for (int i = 0; i < 5; ++i) {  // O^T blocks 0..3 and L (columns 4HP..5HP)
                                 uint32_t o[16];
                                 const uint32_t ta = tmem + lane_base + i * HP + cc * 16;
                                 SMLA_TMEM_LD16(ta, o);
                                 ptx::tmem_wait_ld();
 #pragma unroll
                                 for (int e = 0; e < 16; ++e)
-                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * sAlpha[cc * 16 + e]);
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * a[e]);
                                 SMLA_TMEM_ST16(ta, o);
                             }
                         }
@@ -399,15 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout
+            if (row_lane) {
 #pragma unroll
-            for (int h = 0; h < HP; ++h) {
-                const float x = __uint_as_float(sv[h]);
-                const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
-                l[h] += pr;
-                if (row_lane) {
-                    const uint32_t off = (h >> 3) * 1024 + (h & 7) * 128 +
-                                         ((((r >> 3) ^ (h & 7)) << 4) | ((r & 7) << 1));
-                    ptx::st_shared_u16(sP + off, bf16_bits(pr));
+                for (int h = 0; h < HP; ++h) {
+                    const float x = __uint_as_float(sv[h]);
+                    const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
+                    ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -416,27 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));
         }
 
-        // ---- per-head totals: L = sum of this CTA's probabilities
+        // ---- the last PV, then per-head totals L (any lane of the L columns)
         const bool aborted = ptx::named_bar_red_or(1, 128, failed || *sAbort);
-#pragma unroll
-        for (int h = 0; h < HP; ++h) {
-            float v = l[h];
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            if (lane == 0) sRed[quad * HP + h] = v;
-        }
-        ptx::named_bar_sync(1, 128);
-        if (wtid < HP) {
-            const float tot = sRed[wtid] + sRed[HP + wtid] + sRed[2 * HP + wtid] + sRed[3 * HP + wtid];
-            sML[wtid] = sM[wtid];
-            sML[HP + wtid] = tot;
-            sAlpha[wtid] = tot > 0.f ? 1.0f / tot : 0.f;
-        }
-        ptx::named_bar_sync(1, 128);
-        // the last PV
+        failed = aborted;
         if (nb > 0 && !aborted) {
             bool okw = true;
             if (lane == 0) okw = wait(kBarPvDone, (nb - 1) & 1);
@@ -444,29 +460,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (okw) ptx::tc_fence_after();
             failed = !okw;
-        } else {
-            failed = aborted;
         }
         const bool have_o = nb > 0 && !failed;
+        if (quad == 0) {
+#pragma unroll 1
+            for (int cc = 0; cc < HP / 16; ++cc) {
+                uint32_t lv[16];
+                if (have_o) {
+                    SMLA_TMEM_LD16(tmem + L::kColL + cc * 16, lv);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) lv[e] = 0u;
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int h = cc * 16 + e;
+                        const float tot = __uint_as_float(lv[e]);
+                        sML[h] = sM[h];
+                        sML[HP + h] = tot;
+                        sAlpha[h] = tot > 0.f ? 1.0f / tot : 0.f;
+                    }
+                }
+            }
+        }
+        ptx::named_bar_sync(1, 128);
 
         if (splits == 1 && !aborted) {
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
-                uint32_t ov[HP];
-                if (have_o) {
-#pragma unroll
-                    for (int cc = 0; cc < HP / 16; ++cc)
-                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, &ov[cc * 16]);
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int h = 0; h < HP; ++h) ov[h] = 0u;
-                }
                 const int d = i * 128 + quad * 32 + lane;
                 __nv_bfloat16* orow = p.out + static_cast<int64_t>(t) * p.h * kDV + d;
+#pragma unroll 1
+                for (int cc = 0; cc < HP / 16; ++cc) {
+                    uint32_t ov[16];
+                    if (have_o) {
+                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, ov);
+                        ptx::tmem_wait_ld();
+                    } else {
 #pragma unroll
-                for (int h = 0; h < HP; ++h)
-                    if (h < p.h) orow[h * kDV] = __float2bfloat16_rn(__uint_as_float(ov[h]) * sAlpha[h]);
+                        for (int e = 0; e < 16; ++e) ov[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int h = cc * 16 + e;
+                        if (h < p.h) orow[h * kDV] = __float2bfloat16_rn(__uint_as_float(ov[e]) * sAlpha[h]);
+                    }
+                }
             }
             if (wtid < p.h) {
                 const float tot = sML[HP + wtid];
@@ -475,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         ptx::tc_fence_before();
-        if (splits > 1) sAbort[0] = sAbort[0] | (failed ? 1 : 0);
+        if (splits > 1 && failed) sAbort[0] = 1;
     }
 
     __syncthreads();
@@ -483,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (splits > 1) {
         // ================================================================ cluster merge
         ptx::cluster_sync();  // every CTA's (m, L) is in its shared memory
-        if (warp >= 2) {
-            const int wtid = threadIdx.x - 64;
+        if (warp > kProducerWarps) {
+            const int wtid = threadIdx.x - kSoftmaxThread0;
             const int quad = warp & 3;
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
             const bool have_o = nb > 0 && *sAbort == 0;
@@ -498,39 +539,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < splits; ++k) {
                     const float mk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k));
                     const float lk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_l, k));
-                    if (mk != -CUDART_INF_F) Lt += lk * ptx::ex2_approx(mk - M);
+                    if (mk != -CUDART_INF_F && lk > 0.f) Lt += lk * ptx::ex2_approx(mk - M);
                 }
                 const float mine = sML[wtid];
-                sAlpha[wtid] = (Lt > 0.f && mine != -CUDART_INF_F) ? ptx::ex2_approx(mine - M) / Lt : 0.f;
+                sAlpha[wtid] = (Lt > 0.f && mine != -CUDART_INF_F && sML[HP + wtid] > 0.f)
+                                   ? ptx::ex2_approx(mine - M) / Lt
+                                   : 0.f;
                 if (rank == 0 && wtid < p.h)
                     p.lse[static_cast<int64_t>(t) * p.h + wtid] =
                         Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
             }
             ptx::named_bar_sync(1, 128);
             float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);
+            if (have_o) ptx::tc_fence_after();
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
-                uint32_t ov[HP];
-                if (have_o) {
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < HP / 16; ++cc)
-                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, &ov[cc * 16]);
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int h = 0; h < HP; ++h) ov[h] = 0u;
-                }
                 const int d = i * 128 + quad * 32 + lane;
+#pragma unroll 1
+                for (int cc = 0; cc < HP / 16; ++cc) {
+                    uint32_t ov[16];
+                    if (have_o) {
+                        SMLA_TMEM_LD16(tmem + lane_base + i * HP + cc * 16, ov);
+                        ptx::tmem_wait_ld();
+                    } else {
 #pragma unroll
-                for (int h = 0; h < HP; ++h)
-                    obuf[d * L::kObufStride + h] = __uint_as_float(ov[h]) * sAlpha[h];
+                        for (int e = 0; e < 16; ++e) ov[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        obuf[d * L::kObufStride + cc * 16 + e] = __uint_as_float(ov[e]) * sAlpha[cc * 16 + e];
+                }
             }
             ptx::tc_fence_before();
         }
         ptx::cluster_sync();  // every CTA's weighted partial O is in its shared memory
-        if (warp >= 2) {
-            const int wtid = threadIdx.x - 64;
+        if (warp > kProducerWarps) {
+            const int wtid = threadIdx.x - kSoftmaxThread0;
             const int ds = kDV / splits;
             const uint32_t ob = sbase + L::kOffKV;
             for (int it = wtid; it < p.h * ds; it += 128) {
@@ -549,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, L::kTmemCols);
     }
