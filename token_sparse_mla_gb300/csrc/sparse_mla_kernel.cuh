@@ -18,16 +18,15 @@
 //               count only has to fill the MMA's N dimension (no padding to 64):
 //                 S^T[64 rows, HP]        = K_blk[64 x 576] . Q^T          (M=64)
 //                 O^T[512 dims, HP]      += V_blk^T[512 x 64] . P^T        (4 x M=128)
-//                 Lrep[128, HP]          += ONES[128 x 64] . P^T           (M=128)
 //               V^T is read from the SAME shared-memory tile as K, as an MN-major
-//               operand.  ONES is an all-ones bf16 matrix kept in TMEM (the A
-//               operand of the last product), so every lane of Lrep holds the
-//               per-head sum of the bf16 probabilities that entered O.
+//               operand.
 //   warps 1-7   producers: cp.async gather of 64 rows per stage, 2 stages.
 //   warps 8-11  softmax warpgroup: reads S^T from TMEM (one KV row per thread, all
 //               heads), masks invalid entries, keeps a running max per head in
-//               log2 units and only rescales O and L when that max grows by more
-//               than 2^8, writes P^T (bf16) to shared memory, runs the epilogue.
+//               log2 units and only rescales O when that max grows by more than
+//               2^8, writes P^T (bf16) to shared memory, runs the epilogue.  Each
+//               row thread keeps its fp32 partial softmax sums (one per head) in
+//               its own TMEM lane, which keeps them out of the register file.
 //
 // HP is the MMA N size: the head count rounded up to 16 (h = 8 runs N = 16 with
 // the upper 8 query rows zero in shared memory; nothing is padded in HBM).
@@ -56,7 +55,6 @@ constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
 constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;    // draining in-flight work after an abort
-constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;       // two bf16 1.0 values
 
 // device error word bits (read by sparse_mla_sync_status)
 constexpr unsigned int kErrTimeout = 1u;
@@ -78,13 +76,12 @@ struct Layout {
     static constexpr int kNumBars = 12;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kOffMisc + 16;
-    // TMEM columns: O^T [0,4HP) | L [4HP,5HP) | S^T x2 [5HP,7HP) | ONES [7HP, 7HP+64)
+    // TMEM columns: O^T [0,4HP) | per-lane partial sums Lp [4HP,5HP) | S^T x2 [5HP,7HP)
     static constexpr int kColL = 4 * HP;
     static constexpr int kColS = 5 * HP;
-    static constexpr int kColOnes = 7 * HP;
-    static constexpr int kTmemCols = (7 * HP + 64 <= 256) ? 256 : 512;
+    static constexpr int kTmemCols = (7 * HP <= 128) ? 128 : ((7 * HP <= 256) ? 256 : 512);
     static constexpr int kObufStride = HP + 1;  // merge buffer: fp32 per dim row
-    static_assert(7 * HP + 64 <= kTmemCols, "TMEM budget");
+    static_assert(7 * HP <= kTmemCols, "TMEM budget");
     static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kDV * kObufStride * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
@@ -205,13 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *sTmem;
     if (warp > kProducerWarps) {
-        // all-ones A operand of the row-sum product, in every lane of this warp's quadrant
+        // partial softmax sums start at zero in every lane of this warp's quadrant
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        uint32_t ones[16];
+        uint32_t zeros[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ones[e] = kOnesBf16x2;
+        for (int e = 0; e < 16; ++e) zeros[e] = 0u;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) SMLA_TMEM_ST16(tmem + lane_base + L::kColOnes + c, ones);
+        for (int c = 0; c < HP; c += 16) SMLA_TMEM_ST16(tmem + lane_base + L::kColL + c, zeros);
         ptx::tmem_wait_st();
     }
     ptx::tc_fence_before();
@@ -223,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(64, HP, 0, 0);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
-            constexpr uint32_t kIdescL = ptx::idesc_bf16_f32(128, HP, 0, 0);
             ptx::prefetch_tmap(&tm_q);
             ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
             for (int pn = 0; pn < kPanels; ++pn)
@@ -269,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::smem_desc_sw128(kv + 2 * i * kPanelBytes + k * 2048, kPanelBytes, 1024);
                         ptx::mma_bf16_ss(tmem + i * HP, a, bp, kIdescPV, acc);
                     }
-                    ptx::mma_bf16_ts(tmem + L::kColL, tmem + L::kColOnes + k * 8, bp, kIdescL, acc);
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
@@ -382,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool pv_waited = false;
             if (ptx::named_bar_red_or(1, 128, need)) {
-                // the running max of some head grew: new max, rescale O and L
+                // the running max of some head grew: new max, rescale O and the partial sums
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
                     const float v = ptx::warp_max_f32(__uint_as_float(sv[h]));
@@ -412,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) a[e] = sAlpha[cc * 16 + e];
 #pragma unroll 1
-                            for (int i = 0; i < 5; ++i) {  // O^T blocks 0..3 and L (columns 4HP..5HP)
+                            for (int i = 0; i < 5; ++i) {  // O^T blocks 0..3 and Lp (columns 4HP..5HP)
                                 uint32_t o[16];
                                 const uint32_t ta = tmem + lane_base + i * HP + cc * 16;
                                 SMLA_TMEM_LD16(ta, o);
@@ -435,22 +430,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__shfl_sync(0xffffffffu, okw, 0)) failed = true;
                 __syncwarp();
             }
-            // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout
-            if (row_lane) {
+            // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout,
+            // and added in fp32 to this lane's partial sums in TMEM
 #pragma unroll
-                for (int h = 0; h < HP; ++h) {
+            for (int cc = 0; cc < HP / 16; ++cc) {
+                uint32_t lp[16];
+                const uint32_t ta = tmem + lane_base + L::kColL + cc * 16;
+                SMLA_TMEM_LD16(ta, lp);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int h = cc * 16 + e;
                     const float x = __uint_as_float(sv[h]);
                     const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
-                    ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
+                    lp[e] = __float_as_uint(__uint_as_float(lp[e]) + pr);
+                    if (row_lane) ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
                 }
+                SMLA_TMEM_ST16(ta, lp);
             }
+            ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));
         }
 
-        // ---- the last PV, then per-head totals L (any lane of the L columns)
+        // ---- the last PV, then per-head totals L = sum of the row lanes' partial sums
         const bool aborted = ptx::named_bar_red_or(1, 128, failed || *sAbort);
         failed = aborted;
         if (nb > 0 && !aborted) {
@@ -462,28 +467,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed = !okw;
         }
         const bool have_o = nb > 0 && !failed;
-        if (quad == 0) {
 #pragma unroll 1
-            for (int cc = 0; cc < HP / 16; ++cc) {
-                uint32_t lv[16];
-                if (have_o) {
-                    SMLA_TMEM_LD16(tmem + L::kColL + cc * 16, lv);
-                    ptx::tmem_wait_ld();
-                } else {
+        for (int cc = 0; cc < HP / 16; ++cc) {
+            uint32_t lv[16];
+            SMLA_TMEM_LD16(tmem + lane_base + L::kColL + cc * 16, lv);
+            ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) lv[e] = 0u;
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int h = cc * 16 + e;
-                        const float tot = __uint_as_float(lv[e]);
-                        sML[h] = sM[h];
-                        sML[HP + h] = tot;
-                        sAlpha[h] = tot > 0.f ? 1.0f / tot : 0.f;
-                    }
-                }
+            for (int e = 0; e < 16; ++e) {
+                float v = __uint_as_float(lv[e]);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                if (lane == 0) sRed[quad * HP + cc * 16 + e] = v;
             }
+        }
+        ptx::named_bar_sync(1, 128);
+        if (wtid < HP) {
+            const float tot =
+                have_o ? sRed[wtid] + sRed[HP + wtid] + sRed[2 * HP + wtid] + sRed[3 * HP + wtid] : 0.f;
+            sML[wtid] = sM[wtid];
+            sML[HP + wtid] = tot;
+            sAlpha[wtid] = tot > 0.f ? 1.0f / tot : 0.f;
         }
         ptx::named_bar_sync(1, 128);
 
