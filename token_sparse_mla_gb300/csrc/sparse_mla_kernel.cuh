@@ -224,17 +224,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
             for (int pn = 0; pn < kPanels; ++pn)
                 ptx::tma_load_3d(sQ + pn * HP * 128, &tm_q, pn * 64, 0, t, bar(kBarQ));
+            // Descriptors differ from a base only in the start-address field (address >> 4,
+            // low 14 bits), so each operand is its base descriptor plus a constant.
+            const uint64_t dq = ptx::smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dkv = ptx::smem_desc_sw128(sKV, 16, 1024);
+            const uint64_t dv = ptx::smem_desc_sw128(sKV, kPanelBytes, 1024);
+            const uint64_t dp = ptx::smem_desc_sw128(sP, 16, 1024);
             auto issue_s = [&](int b) {
                 const int s = b & 1;
-                const uint32_t kv = sKV + s * kStageBytes;
+                const uint64_t a0 = dkv + static_cast<uint64_t>((s * kStageBytes) >> 4);
                 const uint32_t d = tmem + L::kColS + s * HP;
-#pragma unroll 1
+#pragma unroll
                 for (int pn = 0; pn < kPanels; ++pn) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t a = ptx::smem_desc_sw128(kv + pn * kPanelBytes + k * 32, 16, 1024);
-                        const uint64_t bq = ptx::smem_desc_sw128(sQ + pn * HP * 128 + k * 32, 16, 1024);
-                        ptx::mma_bf16_ss(d, a, bq, kIdescS, (pn | k) != 0);
+                        ptx::mma_bf16_ss(d, a0 + ((pn * kPanelBytes + k * 32) >> 4),
+                                         dq + ((pn * HP * 128 + k * 32) >> 4), kIdescS, (pn | k) != 0);
                     }
                 }
                 ptx::mma_commit(bar(kBarSFull + s));
@@ -254,17 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
                 const int s = b & 1;
-                const uint32_t kv = sKV + s * kStageBytes;
-#pragma unroll 1
+                const uint64_t v0 = dv + static_cast<uint64_t>((s * kStageBytes) >> 4);
+#pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint64_t bp = ptx::smem_desc_sw128(sP + k * 32, 16, 1024);
                     const uint32_t acc = (b > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint64_t a =
-                            ptx::smem_desc_sw128(kv + 2 * i * kPanelBytes + k * 2048, kPanelBytes, 1024);
-                        ptx::mma_bf16_ss(tmem + i * HP, a, bp, kIdescPV, acc);
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        ptx::mma_bf16_ss(tmem + i * HP, v0 + ((2 * i * kPanelBytes + k * 2048) >> 4),
+                                         dp + ((k * 32) >> 4), kIdescPV, acc);
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
@@ -288,8 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // holds the slot of the warp's i-th row.
         const int pw = warp - 1;
         const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
+        const int my_row = pw + kProducerWarps * lane;
+        const bool row_owner = lane < 10 && my_row < kRows;
+        // slots of the next block are loaded one block ahead, off the refill's critical path
+        int next_slot = (row_owner && nb > 0) ? entry_slot(idx_row, j0 + my_row, j1, p.num_slots) : -1;
         for (int b = 0; b < nb; ++b) {
             const int s = b & 1;
+            const int my_slot = next_slot;
+            next_slot = (row_owner && b + 1 < nb)
+                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
+                            : -1;
             if (b >= kStages) {
                 bool ok = true;
                 if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
@@ -297,10 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!ok) break;
             }
-            const int my_row = pw + kProducerWarps * lane;
-            const int my_slot = (lane < 10 && my_row < kRows)
-                                    ? entry_slot(idx_row, j0 + b * kRows + my_row, j1, p.num_slots)
-                                    : -1;
             const uint32_t st = sKV + s * kStageBytes;
 #pragma unroll 1
             for (int i = 0; i < 10; ++i) {
