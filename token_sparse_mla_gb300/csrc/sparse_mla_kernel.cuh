@@ -49,6 +49,7 @@ constexpr int kPanels = kDQK / 64;                  // 9 panels of 64 bf16 = 128
 constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
 constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
 constexpr int kStages = 2;
+constexpr int kMaxSplits = 8;                       // CTAs per token (one portable cluster)
 constexpr int kProducerWarps = 7;
 constexpr int kThreads = 32 * (1 + kProducerWarps + 4);  // 384
 constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
@@ -80,11 +81,11 @@ struct Layout {
     static constexpr int kColL = 4 * HP;
     static constexpr int kColS = 5 * HP;
     static constexpr int kTmemCols = (7 * HP <= 128) ? 128 : ((7 * HP <= 256) ? 256 : 512);
-    static constexpr int kObufStride = HP + 1;  // merge buffer: fp32 per dim row
+    static constexpr bool kSumsInTmem = HP == 64;  // softmax partial sums: TMEM at 64 heads
     static_assert(7 * HP <= kTmemCols, "TMEM budget");
     static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
-    static_assert(kDV * kObufStride * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
+    static_assert(HP * kDV * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
 };
 
 struct FwdParams {
@@ -113,6 +114,10 @@ enum : int {
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return static_cast<uint32_t>(bf16_bits(lo)) | (static_cast<uint32_t>(bf16_bits(hi)) << 16);
 }
 
 // Slot of list entry j, or -1 when j is past this CTA's range or the index is invalid.
@@ -344,12 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             pbase[k] = sP + k * 128 + ((((r >> 3) ^ k) << 4) | ((r & 7) << 1));
+        // fp32 partial softmax sums of this row lane, per head: registers up to 32 heads,
+        // this lane's TMEM columns [4HP, 5HP) at 64 heads
+        float lreg[L::kSumsInTmem ? 1 : HP];
+#pragma unroll
+        for (int h = 0; h < (L::kSumsInTmem ? 1 : HP); ++h) lreg[h] = 0.f;
 
         for (int b = 0; b < nb; ++b) {
-            if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
-                failed = true;
-                break;
-            }
             const int s = b & 1;
             const bool valid = slot_next >= 0;
             slot_next = (row_lane && b + 1 < nb)
@@ -382,7 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < HP; ++h) sv[h] = __float_as_uint(-CUDART_INF_F);
             }
             bool pv_waited = false;
-            if (ptx::named_bar_red_or(1, 128, need)) {
+            // one warpgroup barrier per block in the common case (no new max, no abort)
+            if (ptx::named_bar_red_or(1, 128, need || failed || *sAbort)) {
+                if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
+                    failed = true;
+                    break;
+                }
                 // the running max of some head grew: new max, rescale O and the partial sums
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
@@ -399,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sM[wtid] = mn;
                 }
                 ptx::named_bar_sync(1, 128);
+                if constexpr (!L::kSumsInTmem) {
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) lreg[h] *= sAlpha[h];
+                }
                 if (b > 0) {
                     bool okw = true;
                     if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
@@ -407,13 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pv_waited = true;
                     if (okw) {
                         ptx::tc_fence_after();
+                        constexpr int kScaledBlocks = L::kSumsInTmem ? 5 : 4;  // O^T blocks (+ sums)
 #pragma unroll 1
                         for (int cc = 0; cc < HP / 16; ++cc) {
                             float a[16];
 #pragma unroll
                             for (int e = 0; e < 16; ++e) a[e] = sAlpha[cc * 16 + e];
 #pragma unroll 1
-                            for (int i = 0; i < 5; ++i) {  // O^T blocks 0..3 and Lp (columns 4HP..5HP)
+                            for (int i = 0; i < kScaledBlocks; ++i) {
                                 uint32_t o[16];
                                 const uint32_t ta = tmem + lane_base + i * HP + cc * 16;
                                 SMLA_TMEM_LD16(ta, o);
@@ -437,24 +453,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout,
-            // and added in fp32 to this lane's partial sums in TMEM
+            // and added in fp32 to this lane's partial sums
+            if constexpr (L::kSumsInTmem) {
 #pragma unroll
-            for (int cc = 0; cc < HP / 16; ++cc) {
-                uint32_t lp[16];
-                const uint32_t ta = tmem + lane_base + L::kColL + cc * 16;
-                SMLA_TMEM_LD16(ta, lp);
-                ptx::tmem_wait_ld();
+                for (int cc = 0; cc < HP / 16; ++cc) {
+                    uint32_t lp[16];
+                    const uint32_t ta = tmem + lane_base + L::kColL + cc * 16;
+                    SMLA_TMEM_LD16(ta, lp);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int h = cc * 16 + e;
+                    for (int e = 0; e < 16; ++e) {
+                        const int h = cc * 16 + e;
+                        const float x = __uint_as_float(sv[h]);
+                        const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
+                        lp[e] = __float_as_uint(__uint_as_float(lp[e]) + pr);
+                        if (row_lane) ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
+                    }
+                    SMLA_TMEM_ST16(ta, lp);
+                }
+                ptx::tmem_wait_st();
+            } else {
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
                     const float x = __uint_as_float(sv[h]);
                     const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
-                    lp[e] = __float_as_uint(__uint_as_float(lp[e]) + pr);
+                    lreg[h] += pr;
                     if (row_lane) ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
                 }
-                SMLA_TMEM_ST16(ta, lp);
             }
-            ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
@@ -473,11 +499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed = !okw;
         }
         const bool have_o = nb > 0 && !failed;
-#pragma unroll 1
+#pragma unroll
         for (int cc = 0; cc < HP / 16; ++cc) {
             uint32_t lv[16];
-            SMLA_TMEM_LD16(tmem + lane_base + L::kColL + cc * 16, lv);
-            ptx::tmem_wait_ld();
+            if constexpr (L::kSumsInTmem) {
+                SMLA_TMEM_LD16(tmem + lane_base + L::kColL + cc * 16, lv);
+                ptx::tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) lv[e] = __float_as_uint(lreg[cc * 16 + e]);
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 float v = __uint_as_float(lv[e]);
@@ -500,10 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::named_bar_sync(1, 128);
 
         if (splits == 1 && !aborted) {
+            // O = O^T / L as bf16, staged as out[t] ([h][512], contiguous) in the free stage memory,
+            // then written with 16-byte stores
+            uint16_t* so = reinterpret_cast<uint16_t*>(smem + L::kOffKV);
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
                 const int d = i * 128 + quad * 32 + lane;
-                __nv_bfloat16* orow = p.out + static_cast<int64_t>(t) * p.h * kDV + d;
 #pragma unroll 1
                 for (int cc = 0; cc < HP / 16; ++cc) {
                     uint32_t ov[16];
@@ -517,10 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int h = cc * 16 + e;
-                        if (h < p.h) orow[h * kDV] = __float2bfloat16_rn(__uint_as_float(ov[e]) * sAlpha[h]);
+                        if (h < p.h) so[h * kDV + d] = bf16_bits(__uint_as_float(ov[e]) * sAlpha[h]);
                     }
                 }
             }
+            ptx::named_bar_sync(1, 128);
+            const uint4* src = reinterpret_cast<const uint4*>(so);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * p.h * kDV);
+            for (int v = wtid; v < p.h * (kDV / 8); v += 128) dst[v] = src[v];
             if (wtid < p.h) {
                 const float tot = sML[HP + wtid];
                 p.lse[static_cast<int64_t>(t) * p.h + wtid] =
@@ -536,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (splits > 1) {
         // ================================================================ cluster merge
         ptx::cluster_sync();  // every CTA's (m, L) is in its shared memory
+        float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);  // [HP][512] fp32
         if (warp > kProducerWarps) {
             const int wtid = threadIdx.x - kSoftmaxThread0;
             const int quad = warp & 3;
@@ -544,15 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (wtid < HP) {
                 const uint32_t a_m = ptx::smem_u32(sML + wtid);
                 const uint32_t a_l = ptx::smem_u32(sML + HP + wtid);
-                float M = -CUDART_INF_F;
-                for (int k = 0; k < splits; ++k)
-                    M = fmaxf(M, ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k)));
-                float Lt = 0.f;
-                for (int k = 0; k < splits; ++k) {
-                    const float mk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k));
-                    const float lk = ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_l, k));
-                    if (mk != -CUDART_INF_F && lk > 0.f) Lt += lk * ptx::ex2_approx(mk - M);
+                float mk[kMaxSplits], lk[kMaxSplits];
+#pragma unroll
+                for (int k = 0; k < kMaxSplits; ++k) {
+                    mk[k] = k < splits ? ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k)) : -CUDART_INF_F;
+                    lk[k] = k < splits ? ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_l, k)) : 0.f;
                 }
+                float M = -CUDART_INF_F;
+#pragma unroll
+                for (int k = 0; k < kMaxSplits; ++k) M = fmaxf(M, mk[k]);
+                float Lt = 0.f;
+#pragma unroll
+                for (int k = 0; k < kMaxSplits; ++k)
+                    if (mk[k] != -CUDART_INF_F && lk[k] > 0.f) Lt += lk[k] * ptx::ex2_approx(mk[k] - M);
                 const float mine = sML[wtid];
                 sAlpha[wtid] = (Lt > 0.f && mine != -CUDART_INF_F && sML[HP + wtid] > 0.f)
                                    ? ptx::ex2_approx(mine - M) / Lt
@@ -562,7 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
             }
             ptx::named_bar_sync(1, 128);
-            float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);
             if (have_o) ptx::tc_fence_after();
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
@@ -579,24 +620,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        obuf[d * L::kObufStride + cc * 16 + e] = __uint_as_float(ov[e]) * sAlpha[cc * 16 + e];
+                        obuf[(cc * 16 + e) * kDV + d] = __uint_as_float(ov[e]) * sAlpha[cc * 16 + e];
                 }
             }
             ptx::tc_fence_before();
         }
         ptx::cluster_sync();  // every CTA's weighted partial O is in its shared memory
         if (warp > kProducerWarps) {
+            // this CTA sums dims [rank*ds, (rank+1)*ds) of every head over the cluster,
+            // eight dims per item, and stores them as one 16-byte vector
             const int wtid = threadIdx.x - kSoftmaxThread0;
             const int ds = kDV / splits;
-            const uint32_t ob = sbase + L::kOffKV;
-            for (int it = wtid; it < p.h * ds; it += 128) {
-                const int hh = it / ds;
-                const int dd = rank * ds + it % ds;
-                const uint32_t a = ob + static_cast<uint32_t>((dd * L::kObufStride + hh) * 4);
-                float acc = 0.f;
-                for (int k = 0; k < splits; ++k)
-                    acc += ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a, k));
-                p.out[(static_cast<int64_t>(t) * p.h + hh) * kDV + dd] = __float2bfloat16_rn(acc);
+            const int per_head = ds / 8;
+            const uint32_t ob = ptx::smem_u32(obuf);
+            for (int it = wtid; it < p.h * per_head; it += 128) {
+                const int hh = it / per_head;
+                const int d0 = rank * ds + (it % per_head) * 8;
+                const uint32_t a = ob + static_cast<uint32_t>((hh * kDV + d0) * 4);
+                float4 lo[kMaxSplits], hi[kMaxSplits];
+#pragma unroll
+                for (int k = 0; k < kMaxSplits; ++k) {
+                    if (k < splits) {
+                        const uint32_t ra = ptx::map_shared_rank(a, k);
+                        lo[k] = ptx::ld_shared_cluster_v4(ra);
+                        hi[k] = ptx::ld_shared_cluster_v4(ra + 16);
+                    } else {
+                        lo[k] = hi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < kMaxSplits; ++k) {
+                    acc[0] += lo[k].x; acc[1] += lo[k].y; acc[2] += lo[k].z; acc[3] += lo[k].w;
+                    acc[4] += hi[k].x; acc[5] += hi[k].y; acc[6] += hi[k].z; acc[7] += hi[k].w;
+                }
+                uint4 packed;
+                packed.x = pack_bf16x2(acc[0], acc[1]);
+                packed.y = pack_bf16x2(acc[2], acc[3]);
+                packed.z = pack_bf16x2(acc[4], acc[5]);
+                packed.w = pack_bf16x2(acc[6], acc[7]);
+                *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.h + hh) * kDV + d0) = packed;
             }
         }
         ptx::cluster_sync();  // no CTA leaves while a peer still reads its shared memory
