@@ -326,7 +326,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_source": peaks["source"],
                      "per_launch_algorithmic_bytes": avg_gb,
-                     "kernel": "sparse_mla_fwd_bf16_kernel"},
+                     "kernel": "sparse_mla_fwd_kernel"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks.summary(),

@@ -265,3 +265,54 @@ def test_full_prefill_sampled_tokens():
     g = torch.Generator().manual_seed(5)
     toks = sorted(set([0, 1, w.T - 1] + torch.randint(0, w.T, (29,), generator=g).tolist()))
     check_case(w.q, w.kv, w.indices, w.scale, 0, tokens=toks, what="prefill full")
+
+
+# ----------------------------------------------------------------------------- fp8 KV rows
+
+def _rand_fp8(seed, T, h, topk, S, p_invalid=0.05, dup=False):
+    from workloads import quantize_fp8_rows
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(T, h, 576, generator=g) * 0.5).to(torch.bfloat16)
+    kv = quantize_fp8_rows(torch.randn(S, 576, generator=g) * 0.5)
+    if dup:
+        idx = torch.randint(0, S, (T, topk), generator=g)
+    else:
+        idx = torch.stack([torch.randperm(S, generator=g)[:topk] for _ in range(T)])
+    idx = idx.masked_fill(torch.rand(T, topk, generator=g) < p_invalid, -1)
+    return q, kv, idx.to(torch.int32)
+
+
+@pytest.mark.parametrize("h", [8, 16, 32, 64])
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_fp8_random(h, splits):
+    q, kv, idx = _rand_fp8(200 + h, 5, h, 777, 5000, dup=(h == 16))
+    idx[0, 5] = 5000
+    idx[1, :] = -1
+    check_case(q, kv, idx, 576 ** -0.5, splits, kv_format="fp8", what=f"fp8 h={h} splits={splits}")
+
+
+def test_fp8_reduced_config():
+    w = wl("fp8_mixed", n_seq=1, n_tokens=48)
+    check_case(w.q, w.kv, w.indices, w.scale, 0, kv_format="fp8", what="fp8_mixed prefix")
+
+
+def test_fp8_single_entry_is_dequantised_row():
+    q, kv, _ = _rand_fp8(300, 3, 8, 1, 64)
+    idx = torch.tensor([[3], [40], [63]], dtype=torch.int32)
+    out, lse = run_gpu(q, kv, idx, 0.1, kv_format="fp8")
+    for t, s in enumerate([3, 40, 63]):
+        row = oracle.decode_row(kv, "fp8", s)[:512]
+        # e4m3 * scale is exact in fp64; the kernel rounds the fp32 product, then to bf16
+        ref = torch.from_numpy(row).float().to(torch.bfloat16).float()
+        assert torch.equal(out[t].float(), ref.expand(8, 512)), t
+
+
+def test_full_fp8_mixed_sampled_tokens():
+    w = wl("fp8_mixed")
+    g = torch.Generator().manual_seed(6)
+    toks = sorted(set([0, w.T - 1] + torch.randint(0, w.T, (30,), generator=g).tolist()))
+    check_case(w.q, w.kv, w.indices, w.scale, 0, kv_format="fp8", tokens=toks, what="fp8 full")
+    out, lse = run_gpu(pad_heads(w.q, 64), w.kv, w.indices, w.scale, kv_format="fp8")
+    ref_o, ref_l = oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format="fp8",
+                                         tokens=toks[:8])
+    assert_parity(out[toks[:8], :8], lse[toks[:8], :8], ref_o, ref_l, what="fp8 padded")

@@ -294,6 +294,44 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_nc_f32(const void* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Two e4m3 values (low byte first) -> exact f16 pair (hardware conversion) -> fp32 x scale
+// -> bf16 pair, round to nearest even; the low byte's value lands in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_bytes, float scale) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 in16;\n\tcvt.u16.u32 in16, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, in16;\n\t}"
+        : "=r"(h2)
+        : "r"(two_bytes));
+    float lo, hi;
+    asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+        "cvt.f32.f16 %0, l16;\n\tcvt.f32.f16 %1, h16;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    uint32_t out;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi * scale), "f"(lo * scale));
+    return out;
+}
+
 __device__ __forceinline__ int ld_nc_s32(const int32_t* p) {
     int v;
     asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(p));

@@ -49,9 +49,12 @@ EncodeTiledFn g_encode = nullptr;
 
 template <int HP>
 cudaError_t set_kernel_attrs() {
-    auto k = smla::sparse_mla_fwd_bf16_kernel<HP>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<HP, 0>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smla::Layout<HP>::kBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<HP, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smla::Layout<HP>::kBytes);
     return e;
 }
 
@@ -127,8 +130,6 @@ smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_
                     static_cast<long long>(num_slots));
     if (kv_format != SMLA_KV_BF16 && kv_format != SMLA_KV_FP8)
         return fail(SMLA_ERR_INVALID_ARG, "unknown kv_format %d", kv_format);
-    if (kv_format == SMLA_KV_FP8)
-        return fail(SMLA_ERR_UNSUPPORTED, "the fp8 KV format is not built in this library version");
     if (!std::isfinite(scale)) return fail(SMLA_ERR_INVALID_ARG, "scale must be finite");
     if (!(splits == 0 || splits == 1 || splits == 2 || splits == 4 || splits == 8))
         return fail(SMLA_ERR_INVALID_ARG, "splits must be 0 (auto), 1, 2, 4 or 8 (got %d)", splits);
@@ -181,7 +182,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     }
 
     smla::FwdParams prm;
-    prm.kv = reinterpret_cast<const __nv_bfloat16*>(kv);
+    prm.kv = kv;
     prm.indices = idx;
     prm.out = reinterpret_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
@@ -207,12 +208,16 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
         cfg.numAttrs = 1;
     }
     cudaError_t e;
+    const bool fp8 = kv_format == SMLA_KV_FP8;
     if (pl.hp == 16)
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<16>, tm_q, prm);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<16, 1>, tm_q, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<16, 0>, tm_q, prm);
     else if (pl.hp == 32)
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<32>, tm_q, prm);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<32, 1>, tm_q, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<32, 0>, tm_q, prm);
     else
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_bf16_kernel<64>, tm_q, prm);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<64, 1>, tm_q, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<64, 0>, tm_q, prm);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return SMLA_OK;
 }
@@ -306,7 +311,8 @@ smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t k
     if (T < 0 || topk < 1) return fail(SMLA_ERR_INVALID_ARG, "bad T or topk");
     if (!(h == 8 || h == 16 || h == 32 || h == 64))
         return fail(SMLA_ERR_UNSUPPORTED, "h must be 8, 16, 32 or 64 (got %d)", h);
-    if (kv_format != SMLA_KV_BF16) return fail(SMLA_ERR_UNSUPPORTED, "kv_format %d", kv_format);
+    if (kv_format != SMLA_KV_BF16 && kv_format != SMLA_KV_FP8)
+        return fail(SMLA_ERR_INVALID_ARG, "unknown kv_format %d", kv_format);
     int num_sms = 152;
     int dev = 0;
     DeviceState* ds = nullptr;

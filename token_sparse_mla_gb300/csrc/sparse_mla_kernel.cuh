@@ -51,6 +51,7 @@ constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1
 constexpr int kStages = 2;
 constexpr int kMaxSplits = 8;                       // CTAs per token (one portable cluster)
 constexpr int kProducerWarps = 7;
+constexpr int kFp8RowBytes = 656;
 constexpr int kThreads = 32 * (1 + kProducerWarps + 4);  // 384
 constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
 constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
@@ -89,7 +90,7 @@ struct Layout {
 };
 
 struct FwdParams {
-    const __nv_bfloat16* kv;  // [num_slots, 576]
+    const void* kv;           // [num_slots] rows: 576 bf16, or 656 bytes of fp8 + scales + rope
     const int32_t* indices;   // [T, topk]
     __nv_bfloat16* out;       // [T, h, 512]
     float* lse;               // [T, h]
@@ -127,9 +128,12 @@ __device__ __forceinline__ int entry_slot(const int32_t* idx_row, int j, int j1,
     return (s >= 0 && static_cast<int64_t>(s) < num_slots) ? s : -1;
 }
 
-template <int HP>
+// KVF: 0 = bf16 rows of 576 values (1152 bytes); 1 = fp8 rows of 656 bytes
+// ([512 e4m3 | 4 fp32 scales, one per 128 latent values | 64 bf16 rope]), dequantised by the
+// producers into the same bf16 operand tile.
+template <int HP, int KVF>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+    sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
     using L = Layout<HP>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -299,39 +303,104 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_owner = lane < 10 && my_row < kRows;
         // slots of the next block are loaded one block ahead, off the refill's critical path
         int next_slot = (row_owner && nb > 0) ? entry_slot(idx_row, j0 + my_row, j1, p.num_slots) : -1;
-        for (int b = 0; b < nb; ++b) {
-            const int s = b & 1;
-            const int my_slot = next_slot;
-            next_slot = (row_owner && b + 1 < nb)
-                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
-                            : -1;
-            if (b >= kStages) {
-                bool ok = true;
-                if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                __syncwarp();
-                if (!ok) break;
-            }
-            const uint32_t st = sKV + s * kStageBytes;
+        if constexpr (KVF == 0) {
+            for (int b = 0; b < nb; ++b) {
+                const int s = b & 1;
+                const int my_slot = next_slot;
+                next_slot = (row_owner && b + 1 < nb)
+                                ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
+                                : -1;
+                if (b >= kStages) {
+                    bool ok = true;
+                    if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __syncwarp();
+                    if (!ok) break;
+                }
+                const uint32_t st = sKV + s * kStageBytes;
 #pragma unroll 1
-            for (int i = 0; i < 10; ++i) {
-                const int r = pw + kProducerWarps * i;
-                if (r >= kRows) break;
-                const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-                const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
-                const uint32_t nbytes = slot < 0 ? 0u : 16u;
-                const uint32_t dst_row = st + r * 128;
-                const uint32_t sw = static_cast<uint32_t>(r & 7);
+                for (int i = 0; i < 10; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    if (r >= kRows) break;
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+                    const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
+                    const uint32_t nbytes = slot < 0 ? 0u : 16u;
+                    const uint32_t dst_row = st + r * 128;
+                    const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll
-                for (int cc = 0; cc < 3; ++cc) {
-                    const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
-                    if (c < 72) {
-                        const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
-                        ptx::cp_async_16(dst, src + c * 16, nbytes);
+                    for (int cc = 0; cc < 3; ++cc) {
+                        const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+                        if (c < 72) {
+                            const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
+                            ptx::cp_async_16(dst, src + c * 16, nbytes);
+                        }
                     }
                 }
+                ptx::cp_async_arrive_noinc(bar(kBarKvFull + s));
             }
-            ptx::cp_async_arrive_noinc(bar(kBarKvFull + s));
+        } else {
+            // fp8 rows: each lane of the warp takes 16 latent bytes of a row (dims 16*lane ..
+            // 16*lane+15, tile scale lane/8); lanes 0-7 also take 16 bytes of the bf16 rope.
+            // The loads of a block are issued before waiting for its stage to be free.
+            const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+            for (int b = 0; b < nb; ++b) {
+                const int s = b & 1;
+                const int my_slot = next_slot;
+                next_slot = (row_owner && b + 1 < nb)
+                                ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
+                                : -1;
+                uint4 lat[10], rope[10];
+                float scl[10];
+#pragma unroll
+                for (int i = 0; i < 10; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+                    lat[i] = make_uint4(0u, 0u, 0u, 0u);
+                    rope[i] = make_uint4(0u, 0u, 0u, 0u);
+                    scl[i] = 0.f;
+                    if (r < kRows && slot >= 0) {
+                        const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
+                        lat[i] = ptx::ld_nc_v4(row + 16 * lane);
+                        scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
+                        if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
+                    }
+                }
+                if (b >= kStages) {
+                    bool ok = true;
+                    if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __syncwarp();
+                    if (!ok) break;
+                }
+                const uint32_t st = sKV + s * kStageBytes;
+#pragma unroll
+                for (int i = 0; i < 10; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    if (r < kRows) {
+                        const uint32_t sw = static_cast<uint32_t>(r & 7);
+                        const uint32_t row_dst = st + r * 128;
+                        // 16 e4m3 values -> 16 bf16 (two 16-byte chunks of panel lane/4)
+                        uint4 v0, v1;
+                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
+                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
+                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
+                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
+                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
+                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
+                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
+                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
+                        const uint32_t pan = row_dst + (lane >> 2) * kPanelBytes;
+                        const uint32_t ch = static_cast<uint32_t>((lane & 3) * 2);
+                        ptx::st_shared_v4(pan + ((ch ^ sw) << 4), v0);
+                        ptx::st_shared_v4(pan + (((ch + 1) ^ sw) << 4), v1);
+                        if (lane < 8)
+                            ptx::st_shared_v4(row_dst + 8 * kPanelBytes + ((static_cast<uint32_t>(lane) ^ sw) << 4),
+                                              rope[i]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(bar(kBarKvFull + s));
+            }
         }
         ptx::cp_async_wait_all();  // no copy may still be in flight when the CTA leaves
     } else {
