@@ -12,6 +12,7 @@
 
 #include "sparse_mla.h"
 #include "sparse_mla_kernel.cuh"
+#include "sparse_mla_small_kernel.cuh"
 
 namespace {
 
@@ -47,14 +48,21 @@ DeviceState g_dev[kMaxDevices];
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
-template <int HP>
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 cudaError_t set_kernel_attrs() {
-    cudaError_t e = cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<HP, 0>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smla::Layout<HP>::kBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<HP, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smla::Layout<HP>::kBytes);
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0>, smla::SmallLayout<8>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1>, smla::SmallLayout<8>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0>, smla::SmallLayout<16>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1>, smla::SmallLayout<16>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 0>, smla::Layout<32>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 1>, smla::Layout<32>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 0>, smla::Layout<64>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 1>, smla::Layout<64>::kBytes);
     return e;
 }
 
@@ -69,9 +77,7 @@ smla_status device_state(int* dev_out, DeviceState** st_out) {
         cudaError_t err = cudaGetDeviceProperties(&prop, dev);
         if (err == cudaSuccess && prop.major < 10) err = cudaErrorInvalidDeviceFunction;
         if (err == cudaSuccess) st.num_sms = prop.multiProcessorCount;
-        if (err == cudaSuccess) err = set_kernel_attrs<16>();
-        if (err == cudaSuccess) err = set_kernel_attrs<32>();
-        if (err == cudaSuccess) err = set_kernel_attrs<64>();
+        if (err == cudaSuccess) err = set_kernel_attrs();
         st.init_error = err;
     });
     if (st.init_error != cudaSuccess) return cuda_fail(st.init_error, "device set-up");
@@ -96,7 +102,8 @@ smla_status encode_fn(EncodeTiledFn* fn) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int pick_mma_n(int h) { return h <= 16 ? 16 : h; }
+// 8 and 16 heads run the warp-MMA kernel (32-row stages); 32 and 64 the tcgen05 kernel.
+bool small_heads(int h) { return h <= 16; }
 
 // Split count: enough CTAs to cover the SMs once when there are few tokens.
 int auto_splits(int64_t T, int nblk, int num_sms) {
@@ -113,6 +120,7 @@ int auto_splits(int64_t T, int nblk, int num_sms) {
 
 struct Plan {
     int hp = 16;
+    int threads = 0;
     int splits = 1;
     int64_t ctas = 0;
     int smem = 0;
@@ -146,12 +154,16 @@ smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_
 
 Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms) {
     Plan pl;
-    pl.hp = pick_mma_n(h);
-    const int nblk = (topk + smla::kRows - 1) / smla::kRows;
+    pl.hp = h;
+    const int rows = small_heads(h) ? smla::kSmRows : smla::kRows;
+    const int nblk = (topk + rows - 1) / rows;
     pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
     pl.ctas = static_cast<int64_t>(T) * pl.splits;
-    pl.smem = pl.hp == 16 ? smla::Layout<16>::kBytes
-                          : (pl.hp == 32 ? smla::Layout<32>::kBytes : smla::Layout<64>::kBytes);
+    pl.threads = small_heads(h) ? smla::kSmThreads : smla::kThreads;
+    pl.smem = h == 8    ? smla::SmallLayout<8>::kBytes
+              : h == 16 ? smla::SmallLayout<16>::kBytes
+              : h == 32 ? smla::Layout<32>::kBytes
+                        : smla::Layout<64>::kBytes;
     return pl;
 }
 
@@ -182,6 +194,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     }
 
     smla::FwdParams prm;
+    prm.q = reinterpret_cast<const __nv_bfloat16*>(q);
     prm.kv = kv;
     prm.indices = idx;
     prm.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -195,7 +208,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
-    cfg.blockDim = dim3(smla::kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -209,15 +222,18 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     }
     cudaError_t e;
     const bool fp8 = kv_format == SMLA_KV_FP8;
-    if (pl.hp == 16)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<16, 1>, tm_q, prm)
-                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<16, 0>, tm_q, prm);
-    else if (pl.hp == 32)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<32, 1>, tm_q, prm)
-                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<32, 0>, tm_q, prm);
+    if (h == 8)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 1>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 0>, prm);
+    else if (h == 16)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 1>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 0>, prm);
+    else if (h == 32)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<32, 1>, tm_q, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<32, 0>, tm_q, prm);
     else
-        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<64, 1>, tm_q, prm)
-                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_kernel<64, 0>, tm_q, prm);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<64, 1>, tm_q, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<64, 0>, tm_q, prm);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return SMLA_OK;
 }

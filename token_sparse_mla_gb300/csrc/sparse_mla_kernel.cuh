@@ -32,35 +32,16 @@
 // the upper 8 query rows zero in shared memory; nothing is padded in HBM).
 #pragma once
 
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <math_constants.h>
-#include <stdint.h>
-
-#include "sm100_ptx.cuh"
+#include "sparse_mla_common.cuh"
 
 namespace smla {
 
-constexpr int kDQK = 576;
-constexpr int kDV = 512;
 constexpr int kRows = 64;                           // KV rows per pipeline stage
-constexpr int kPanels = kDQK / 64;                  // 9 panels of 64 bf16 = 128 bytes per row
 constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
 constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
 constexpr int kStages = 2;
-constexpr int kMaxSplits = 8;                       // CTAs per token (one portable cluster)
-constexpr int kProducerWarps = 7;
-constexpr int kFp8RowBytes = 656;
 constexpr int kThreads = 32 * (1 + kProducerWarps + 4);  // 384
 constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
-constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
-constexpr uint64_t kWaitLimitNs = 2000000000ull;    // bounded waits: 2 s
-constexpr uint64_t kDrainLimitNs = 200000000ull;    // draining in-flight work after an abort
-
-// device error word bits (read by sparse_mla_sync_status)
-constexpr unsigned int kErrTimeout = 1u;
-constexpr unsigned int kErrLayout = 2u;
 
 template <int HP>
 struct Layout {
@@ -89,18 +70,6 @@ struct Layout {
     static_assert(HP * kDV * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
 };
 
-struct FwdParams {
-    const void* kv;           // [num_slots] rows: 576 bf16, or 656 bytes of fp8 + scales + rope
-    const int32_t* indices;   // [T, topk]
-    __nv_bfloat16* out;       // [T, h, 512]
-    float* lse;               // [T, h]
-    int64_t num_slots;
-    int32_t T, h, topk, splits;
-    float sm_scale_log2;      // scale * log2(e)
-};
-
-__device__ unsigned int g_smla_error;
-
 // barrier slots
 enum : int {
     kBarQ = 0,
@@ -113,27 +82,12 @@ enum : int {
     kBarDrain = 11
 };
 
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(bf16_bits(lo)) | (static_cast<uint32_t>(bf16_bits(hi)) << 16);
-}
-
-// Slot of list entry j, or -1 when j is past this CTA's range or the index is invalid.
-__device__ __forceinline__ int entry_slot(const int32_t* idx_row, int j, int j1, int64_t num_slots) {
-    if (j >= j1) return -1;
-    const int s = ptx::ld_nc_s32(idx_row + j);
-    return (s >= 0 && static_cast<int64_t>(s) < num_slots) ? s : -1;
-}
-
 // KVF: 0 = bf16 rows of 576 values (1152 bytes); 1 = fp8 rows of 656 bytes
 // ([512 e4m3 | 4 fp32 scales, one per 128 latent values | 64 bf16 rope]), dequantised by the
 // producers into the same bf16 operand tile.
 template <int HP, int KVF>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
+    sparse_mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
     using L = Layout<HP>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -295,114 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp <= kProducerWarps) {
         // ================================================================ producers
-        // warp pw copies rows pw, pw + 7, pw + 14, ... of each 64-row block; lane i < 10
-        // holds the slot of the warp's i-th row.
-        const int pw = warp - 1;
-        const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
-        const int my_row = pw + kProducerWarps * lane;
-        const bool row_owner = lane < 10 && my_row < kRows;
-        // slots of the next block are loaded one block ahead, off the refill's critical path
-        int next_slot = (row_owner && nb > 0) ? entry_slot(idx_row, j0 + my_row, j1, p.num_slots) : -1;
-        if constexpr (KVF == 0) {
-            for (int b = 0; b < nb; ++b) {
-                const int s = b & 1;
-                const int my_slot = next_slot;
-                next_slot = (row_owner && b + 1 < nb)
-                                ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
-                                : -1;
-                if (b >= kStages) {
-                    bool ok = true;
-                    if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    __syncwarp();
-                    if (!ok) break;
-                }
-                const uint32_t st = sKV + s * kStageBytes;
-#pragma unroll 1
-                for (int i = 0; i < 10; ++i) {
-                    const int r = pw + kProducerWarps * i;
-                    if (r >= kRows) break;
-                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-                    const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
-                    const uint32_t nbytes = slot < 0 ? 0u : 16u;
-                    const uint32_t dst_row = st + r * 128;
-                    const uint32_t sw = static_cast<uint32_t>(r & 7);
-#pragma unroll
-                    for (int cc = 0; cc < 3; ++cc) {
-                        const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
-                        if (c < 72) {
-                            const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
-                            ptx::cp_async_16(dst, src + c * 16, nbytes);
-                        }
-                    }
-                }
-                ptx::cp_async_arrive_noinc(bar(kBarKvFull + s));
-            }
-        } else {
-            // fp8 rows: each lane of the warp takes 16 latent bytes of a row (dims 16*lane ..
-            // 16*lane+15, tile scale lane/8); lanes 0-7 also take 16 bytes of the bf16 rope.
-            // The loads of a block are issued before waiting for its stage to be free.
-            const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-            for (int b = 0; b < nb; ++b) {
-                const int s = b & 1;
-                const int my_slot = next_slot;
-                next_slot = (row_owner && b + 1 < nb)
-                                ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
-                                : -1;
-                uint4 lat[10], rope[10];
-                float scl[10];
-#pragma unroll
-                for (int i = 0; i < 10; ++i) {
-                    const int r = pw + kProducerWarps * i;
-                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-                    lat[i] = make_uint4(0u, 0u, 0u, 0u);
-                    rope[i] = make_uint4(0u, 0u, 0u, 0u);
-                    scl[i] = 0.f;
-                    if (r < kRows && slot >= 0) {
-                        const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
-                        lat[i] = ptx::ld_nc_v4(row + 16 * lane);
-                        scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
-                        if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
-                    }
-                }
-                if (b >= kStages) {
-                    bool ok = true;
-                    if (lane == 0) ok = wait(kBarKvEmpty + s, ((b >> 1) - 1) & 1);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    __syncwarp();
-                    if (!ok) break;
-                }
-                const uint32_t st = sKV + s * kStageBytes;
-#pragma unroll
-                for (int i = 0; i < 10; ++i) {
-                    const int r = pw + kProducerWarps * i;
-                    if (r < kRows) {
-                        const uint32_t sw = static_cast<uint32_t>(r & 7);
-                        const uint32_t row_dst = st + r * 128;
-                        // 16 e4m3 values -> 16 bf16 (two 16-byte chunks of panel lane/4)
-                        uint4 v0, v1;
-                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
-                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
-                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
-                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
-                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
-                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
-                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
-                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
-                        const uint32_t pan = row_dst + (lane >> 2) * kPanelBytes;
-                        const uint32_t ch = static_cast<uint32_t>((lane & 3) * 2);
-                        ptx::st_shared_v4(pan + ((ch ^ sw) << 4), v0);
-                        ptx::st_shared_v4(pan + (((ch + 1) ^ sw) << 4), v1);
-                        if (lane < 8)
-                            ptx::st_shared_v4(row_dst + 8 * kPanelBytes + ((static_cast<uint32_t>(lane) ^ sw) << 4),
-                                              rope[i]);
-                    }
-                }
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(bar(kBarKvFull + s));
-            }
-        }
-        ptx::cp_async_wait_all();  // no copy may still be in flight when the CTA leaves
+        gather_rows<kRows, kStages, KVF>(p, idx_row, j0, j1, nb, warp - 1, lane, sKV, bar(kBarKvFull),
+                                         bar(kBarKvEmpty), sAbort);
     } else {
         // ================================================================ softmax warpgroup
         const int wtid = threadIdx.x - kSoftmaxThread0;
