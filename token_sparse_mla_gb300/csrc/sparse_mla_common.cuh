@@ -83,15 +83,22 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
     const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
     const int my_row = pw + kProducerWarps * lane;
     const bool row_owner = lane < kPerWarp && my_row < kRows;
-    // slots of the next block are loaded one block ahead, off the refill's critical path
-    int next_slot = (row_owner && nb > 0) ? entry_slot(idx_row, j0 + my_row, j1, p.num_slots) : -1;
+    // the slots of this lane's row are loaded kAhead blocks (256 list entries) ahead, so a global
+    // load latency never sits between a free stage and its refill
+    constexpr int kAhead = 256 / ROWS;
+    int slot_q[kAhead];
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i)
+        slot_q[i] = (row_owner && i < nb) ? entry_slot(idx_row, j0 + i * kRows + my_row, j1, p.num_slots) : -1;
     if constexpr (KVF == 0) {
         for (int b = 0; b < nb; ++b) {
             const int s = b % NST;
-            const int my_slot = next_slot;
-            next_slot = (row_owner && b + 1 < nb)
-                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
-                            : -1;
+            const int my_slot = slot_q[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
+            slot_q[kAhead - 1] = (row_owner && b + kAhead < nb)
+                                     ? entry_slot(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, p.num_slots)
+                                     : -1;
             if (b >= NST) {
                 bool ok = true;
                 if (lane == 0) ok = wait_empty(s, ((b / NST) - 1) & 1);
@@ -127,10 +134,12 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
         const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
         for (int b = 0; b < nb; ++b) {
             const int s = b % NST;
-            const int my_slot = next_slot;
-            next_slot = (row_owner && b + 1 < nb)
-                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + my_row, j1, p.num_slots)
-                            : -1;
+            const int my_slot = slot_q[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
+            slot_q[kAhead - 1] = (row_owner && b + kAhead < nb)
+                                     ? entry_slot(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, p.num_slots)
+                                     : -1;
             uint4 lat[kPerWarp], rope[kPerWarp];
             float scl[kPerWarp];
 #pragma unroll

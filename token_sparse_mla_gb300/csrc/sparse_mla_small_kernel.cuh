@@ -44,16 +44,20 @@ struct SmallLayout {
     static constexpr int kRedBytes = kSmComputeWarps * 2 * kNT * 32 * 16;
     static constexpr int kPStride = 80;                              // bytes per head row of P^T
     static constexpr int kOffP = kOffRed + kRedBytes;
-    static constexpr int kOffHr = kOffP + H * kPStride;              // [4 warps][H] reductions
-    static constexpr int kOffM = kOffHr + kSmComputeWarps * H * 4;   // running max (log2 units)
+    static constexpr int kOffHr = kOffP + H * kPStride;              // [8][H]: per-warp reductions,
+                                                                     // per-source merge weights
+    static constexpr int kOffM = kOffHr + kMaxSplits * H * 4;        // running max (log2 units)
     static constexpr int kOffAlpha = kOffM + H * 4;                  // rescale factor / 1/L / weight
     static constexpr int kOffML = kOffAlpha + H * 4;                 // final m[H], L[H]
-    static constexpr int kOffBar = (kOffML + 2 * H * 4 + 7) / 8 * 8; // full[5], empty[5]
+    static constexpr int kOffRecvML = kOffML + 2 * H * 4;            // [kMaxSplits][2H] (m, L) of peers
+    static constexpr int kOffRecv = kOffRecvML + kMaxSplits * 2 * H * 4;  // [splits][H][512/splits] fp32
+    static constexpr int kOffBar = kOffRecv + H * kDV * 4;           // full[5], empty[5]
     static constexpr int kOffMisc = kOffBar + 2 * kSmStages * 8;     // abort flag
     static constexpr int kBytes = kOffMisc + 16;
     static_assert(kOffP % 16 == 0, "ldmatrix rows need 16-byte alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
-    static_assert(H * kDV * 4 <= kSmStages * kStageBytes, "merge buffer fits the stages");
+    static_assert(kOffRecv % 16 == 0 && kOffBar % 8 == 0, "alignment of the merge buffers");
+    static_assert(H * kDV * 2 <= kSmStages * kStageBytes, "output staging fits the stages");
 };
 
 namespace mma16816 {
@@ -133,6 +137,9 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     }
     if (threadIdx.x >= kSmCompute0 && threadIdx.x - kSmCompute0 < H) sM[threadIdx.x - kSmCompute0] = -CUDART_INF_F;
     __syncthreads();
+    // peers push into this CTA's receive buffers at the end; the matching wait below makes sure
+    // every CTA of the cluster has started before any of them writes to another
+    if (splits > 1) ptx::cluster_arrive_relaxed();
 
     // O^T accumulators of the compute warps (fragment layout: dims 128*cw + 16*mt + g (+8),
     // heads 8*nt + 2*tq (+1)); declared here because the cluster merge below reads them
@@ -176,7 +183,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         // this warp's softmax rows: 8 of the block's 32 (m-tile cw/2, half cw%2), one per lane group
         const int mt_s = cw >> 1, half = cw & 1;
         const int rr = mt_s * 16 + half * 8 + g;
-        int slot_next = nb > 0 ? entry_slot(idx_row, j0 + rr, j1, p.num_slots) : -1;
+        // slot validity of this lane's row, loaded kAhead blocks ahead
+        constexpr int kAhead = 8;
+        int slot_q[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i)
+            slot_q[i] = i < nb ? entry_slot(idx_row, j0 + i * kSmRows + rr, j1, p.num_slots) : -1;
 
         float lsum[NT][2];
 #pragma unroll
@@ -185,8 +197,11 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         for (int b = 0; b < nb; ++b) {
             const int s = b % kSmStages;
             const uint32_t stb = sKV + s * L::kStageBytes;
-            const bool valid = slot_next >= 0;
-            slot_next = (b + 1 < nb) ? entry_slot(idx_row, j0 + (b + 1) * kSmRows + rr, j1, p.num_slots) : -1;
+            const bool valid = slot_q[0] >= 0;
+#pragma unroll
+            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
+            slot_q[kAhead - 1] =
+                (b + kAhead < nb) ? entry_slot(idx_row, j0 + (b + kAhead) * kSmRows + rr, j1, p.num_slots) : -1;
             bool ok = true;
             if (lane == 0)
                 ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / kSmStages) & 1, sAbort, &g_smla_error, kErrTimeout,
@@ -389,90 +404,89 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
 
     if (splits > 1) {
         // ================================================================ cluster merge
-        ptx::cluster_sync();  // every CTA's (m, L) is in its shared memory
+        // CTA k of the cluster owns output dims [k*ds, (k+1)*ds).  Every CTA pushes its per-head
+        // (m, L) and its unnormalised partial O for each owner's dims into that owner's receive
+        // buffers; after one cluster barrier each owner weights the partials by 2^(m_j - M) / sum_j
+        // L_j 2^(m_j - M) and stores its dims.  No CTA reads another's memory after the barrier.
+        const int ds = kDV / splits;
+        ptx::cluster_wait();  // every CTA has started (pairs with the arrive at the top)
         if (warp >= kProducerWarps) {
             const int cw = warp - kProducerWarps;
             const int wtid = threadIdx.x - kSmCompute0;
             const int g = lane >> 2, tq = lane & 3;
-            const bool have_o = nb > 0 && *sAbort == 0;
+            const bool have = nb > 0 && *sAbort == 0;
+            const uint32_t recv = sbase + L::kOffRecv;
+            const uint32_t recv_ml = sbase + L::kOffRecvML;
             if (wtid < H) {
-                const uint32_t a_m = ptx::smem_u32(sML + wtid);
-                const uint32_t a_l = ptx::smem_u32(sML + H + wtid);
-                float mk[kMaxSplits], lk[kMaxSplits];
-#pragma unroll
-                for (int k = 0; k < kMaxSplits; ++k) {
-                    mk[k] = k < splits ? ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_m, k)) : -CUDART_INF_F;
-                    lk[k] = k < splits ? ptx::ld_shared_cluster_f32(ptx::map_shared_rank(a_l, k)) : 0.f;
+                const float m = have ? sML[wtid] : -CUDART_INF_F;
+                const float l = have ? sML[H + wtid] : 0.f;
+                for (int k = 0; k < splits; ++k) {
+                    ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + wtid) * 4, k), m);
+                    ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + H + wtid) * 4, k), l);
                 }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                    const int d = 128 * cw + 16 * mt + g + 8 * hi;
+                    const int k = d / ds;
+                    const int dd = d - k * ds;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int h = nt * 8 + 2 * tq + e;
+                            const uint32_t la = recv + static_cast<uint32_t>(((rank * H + h) * ds + dd) * 4);
+                            ptx::st_shared_cluster_f32(ptx::map_shared_rank(la, k), have ? o[mt][nt][2 * hi + e] : 0.f);
+                        }
+                    }
+                }
+            }
+        }
+        ptx::cluster_sync();  // all pushes are visible to their owners
+        if (warp >= kProducerWarps) {
+            const int wtid = threadIdx.x - kSmCompute0;
+            const float* rml = reinterpret_cast<const float*>(smem + L::kOffRecvML);
+            const float* rcv = reinterpret_cast<const float*>(smem + L::kOffRecv);
+            if (wtid < H) {
                 float M = -CUDART_INF_F;
-#pragma unroll
-                for (int k = 0; k < kMaxSplits; ++k) M = fmaxf(M, mk[k]);
+                for (int j = 0; j < splits; ++j) M = fmaxf(M, rml[j * 2 * H + wtid]);
                 float Lt = 0.f;
-#pragma unroll
-                for (int k = 0; k < kMaxSplits; ++k)
-                    if (mk[k] != -CUDART_INF_F && lk[k] > 0.f) Lt += lk[k] * ptx::ex2_approx(mk[k] - M);
-                const float mine = sML[wtid];
-                sAlpha[wtid] = (Lt > 0.f && mine != -CUDART_INF_F && sML[H + wtid] > 0.f)
-                                   ? ptx::ex2_approx(mine - M) / Lt
-                                   : 0.f;
+                for (int j = 0; j < splits; ++j) {
+                    const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
+                    if (mj != -CUDART_INF_F && lj > 0.f) Lt += lj * ptx::ex2_approx(mj - M);
+                }
+                for (int j = 0; j < splits; ++j) {
+                    const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
+                    sHr[j * H + wtid] = (Lt > 0.f && mj != -CUDART_INF_F && lj > 0.f) ? ptx::ex2_approx(mj - M) / Lt : 0.f;
+                }
                 if (rank == 0 && wtid < p.h)
                     p.lse[static_cast<int64_t>(t) * p.h + wtid] =
                         Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
             }
             ptx::named_bar_sync(1, 128);
-            float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);  // [H][512] fp32
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int d = 128 * cw + 16 * mt + g;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int h = nt * 8 + 2 * tq;
-                    const float w0 = have_o ? sAlpha[h] : 0.f, w1 = have_o ? sAlpha[h + 1] : 0.f;
-                    obuf[h * kDV + d] = o[mt][nt][0] * w0;
-                    obuf[(h + 1) * kDV + d] = o[mt][nt][1] * w1;
-                    obuf[h * kDV + d + 8] = o[mt][nt][2] * w0;
-                    obuf[(h + 1) * kDV + d + 8] = o[mt][nt][3] * w1;
-                }
-            }
-        }
-        ptx::cluster_sync();  // every CTA's weighted partial O is in its shared memory
-        if (warp >= kProducerWarps) {
-            // this CTA sums dims [rank*ds, (rank+1)*ds) of every head over the cluster, eight dims
-            // per item, and stores them as one 16-byte vector
-            const int wtid = threadIdx.x - kSmCompute0;
-            const int ds = kDV / splits;
+            // eight dims of one head per item, stored as one 16-byte vector
             const int per_head = ds / 8;
-            const uint32_t ob = sbase + L::kOffKV;
             for (int it = wtid; it < p.h * per_head; it += 128) {
                 const int hh = it / per_head;
-                const int d0 = rank * ds + (it % per_head) * 8;
-                const uint32_t a = ob + static_cast<uint32_t>((hh * kDV + d0) * 4);
-                float4 lo[kMaxSplits], hi[kMaxSplits];
-#pragma unroll
-                for (int k = 0; k < kMaxSplits; ++k) {
-                    if (k < splits) {
-                        const uint32_t ra = ptx::map_shared_rank(a, k);
-                        lo[k] = ptx::ld_shared_cluster_v4(ra);
-                        hi[k] = ptx::ld_shared_cluster_v4(ra + 16);
-                    } else {
-                        lo[k] = hi[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
+                const int dd = (it % per_head) * 8;
                 float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int k = 0; k < kMaxSplits; ++k) {
-                    acc[0] += lo[k].x; acc[1] += lo[k].y; acc[2] += lo[k].z; acc[3] += lo[k].w;
-                    acc[4] += hi[k].x; acc[5] += hi[k].y; acc[6] += hi[k].z; acc[7] += hi[k].w;
+                for (int j = 0; j < splits; ++j) {
+                    const float w = sHr[j * H + hh];
+                    const float4 lo = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd);
+                    const float4 hv = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd + 4);
+                    acc[0] += w * lo.x; acc[1] += w * lo.y; acc[2] += w * lo.z; acc[3] += w * lo.w;
+                    acc[4] += w * hv.x; acc[5] += w * hv.y; acc[6] += w * hv.z; acc[7] += w * hv.w;
                 }
                 uint4 packed;
                 packed.x = pack_bf16x2(acc[0], acc[1]);
                 packed.y = pack_bf16x2(acc[2], acc[3]);
                 packed.z = pack_bf16x2(acc[4], acc[5]);
                 packed.w = pack_bf16x2(acc[6], acc[7]);
-                *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.h + hh) * kDV + d0) = packed;
+                *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.h + hh) * kDV + rank * ds + dd) = packed;
             }
         }
-        ptx::cluster_sync();  // no CTA leaves while a peer still reads its shared memory
     }
 }
 
