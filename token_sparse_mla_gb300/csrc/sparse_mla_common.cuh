@@ -48,10 +48,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Slot of list entry j, or -1 when j is past this CTA's range or the index is invalid.
-__device__ __forceinline__ int entry_slot(const int32_t* idx_row, int j, int j1, int64_t num_slots) {
-    if (j >= j1) return -1;
-    const int s = ptx::ld_nc_s32(idx_row + j);
-    return (s >= 0 && static_cast<int64_t>(s) < num_slots) ? s : -1;
+// Raw list entry j of a row (-1 when j is past the CTA's range or pred is false).  The load is
+// not checked here: the check reads the value, and a read right after the load would wait for
+// it.  Callers hold raw entries in a ring and check them with valid_slot when they are used.
+__device__ __forceinline__ int fetch_entry(const int32_t* idx_row, int j, int j1, bool pred) {
+    int v = -1;
+    if (pred && j < j1) v = __ldg(idx_row + j);
+    return v;
+}
+
+// A list entry names a cache row when 0 <= entry < num_slots; anything else is masked (-1).
+__device__ __forceinline__ int valid_slot(int raw, int64_t num_slots) {
+    return (raw >= 0 && static_cast<int64_t>(raw) < num_slots) ? raw : -1;
 }
 
 // The KV row gather, run by producer warp pw (of kProducerWarps) for this CTA's nb blocks of
@@ -83,114 +91,113 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
     const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
     const int my_row = pw + kProducerWarps * lane;
     const bool row_owner = lane < kPerWarp && my_row < kRows;
-    // the slots of this lane's row are loaded kAhead blocks (256 list entries) ahead, so a global
-    // load latency never sits between a free stage and its refill
+    // The entries of this lane's row are loaded kAhead blocks (256 list entries) ahead into a
+    // ring indexed by b % kAhead; the block loop is unrolled kAhead times so every ring index is
+    // static and a load is first read kAhead blocks after it was issued.
     constexpr int kAhead = 256 / ROWS;
-    int slot_q[kAhead];
+    int ring[kAhead];
 #pragma unroll
-    for (int i = 0; i < kAhead; ++i)
-        slot_q[i] = (row_owner && i < nb) ? entry_slot(idx_row, j0 + i * kRows + my_row, j1, p.num_slots) : -1;
-    if constexpr (KVF == 0) {
-        for (int b = 0; b < nb; ++b) {
+    for (int u = 0; u < kAhead; ++u) ring[u] = fetch_entry(idx_row, j0 + u * kRows + my_row, j1, row_owner && u < nb);
+    bool aborted = false;
+    for (int b0 = 0; b0 < nb && !aborted; b0 += kAhead) {
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int b = b0 + u;
+            if (b >= nb) break;
             const int s = b % NST;
-            const int my_slot = slot_q[0];
-#pragma unroll
-            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
-            slot_q[kAhead - 1] = (row_owner && b + kAhead < nb)
-                                     ? entry_slot(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, p.num_slots)
-                                     : -1;
-            if (b >= NST) {
-                bool ok = true;
-                if (lane == 0) ok = wait_empty(s, ((b / NST) - 1) & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                __syncwarp();
-                if (!ok) break;
-            }
-            const uint32_t st = sKV + s * kStageBytes;
-#pragma unroll 1
-            for (int i = 0; i < kPerWarp; ++i) {
-                const int r = pw + kProducerWarps * i;
-                if (r >= kRows) break;
-                const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-                const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
-                const uint32_t nbytes = slot < 0 ? 0u : 16u;
-                const uint32_t dst_row = st + r * 128;
-                const uint32_t sw = static_cast<uint32_t>(r & 7);
-#pragma unroll
-                for (int cc = 0; cc < 3; ++cc) {
-                    const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
-                    if (c < 72) {
-                        const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
-                        ptx::cp_async_16(dst, src + c * 16, nbytes);
+            const int my_slot = valid_slot(ring[u], p.num_slots);
+            ring[u] = fetch_entry(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, row_owner && b + kAhead < nb);
+            if constexpr (KVF == 0) {
+                if (b >= NST) {
+                    bool ok = true;
+                    if (lane == 0) ok = wait_empty(s, ((b / NST) - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __syncwarp();
+                    if (!ok) {
+                        aborted = true;
+                        break;
                     }
                 }
-            }
-            ptx::cp_async_arrive_noinc(bar_full0 + 8u * s);
-        }
-    } else {
-        // fp8 rows: each lane of the warp takes 16 latent bytes of a row (dims 16*lane ..
-        // 16*lane+15, tile scale lane/8); lanes 0-7 also take 16 bytes of the bf16 rope.
-        // The loads of a block are issued before waiting for its stage to be free.
-        const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-        for (int b = 0; b < nb; ++b) {
-            const int s = b % NST;
-            const int my_slot = slot_q[0];
-#pragma unroll
-            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
-            slot_q[kAhead - 1] = (row_owner && b + kAhead < nb)
-                                     ? entry_slot(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, p.num_slots)
-                                     : -1;
-            uint4 lat[kPerWarp], rope[kPerWarp];
-            float scl[kPerWarp];
-#pragma unroll
-            for (int i = 0; i < kPerWarp; ++i) {
-                const int r = pw + kProducerWarps * i;
-                const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-                lat[i] = make_uint4(0u, 0u, 0u, 0u);
-                rope[i] = make_uint4(0u, 0u, 0u, 0u);
-                scl[i] = 0.f;
-                if (r < kRows && slot >= 0) {
-                    const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
-                    lat[i] = ptx::ld_nc_v4(row + 16 * lane);
-                    scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
-                    if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
-                }
-            }
-            if (b >= NST) {
-                bool ok = true;
-                if (lane == 0) ok = wait_empty(s, ((b / NST) - 1) & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                __syncwarp();
-                if (!ok) break;
-            }
-            const uint32_t st = sKV + s * kStageBytes;
-#pragma unroll
-            for (int i = 0; i < kPerWarp; ++i) {
-                const int r = pw + kProducerWarps * i;
-                if (r < kRows) {
+                const uint32_t st = sKV + s * kStageBytes;
+#pragma unroll 1
+                for (int i = 0; i < kPerWarp; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    if (r >= kRows) break;
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+                    const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
+                    const uint32_t nbytes = slot < 0 ? 0u : 16u;
+                    const uint32_t dst_row = st + r * 128;
                     const uint32_t sw = static_cast<uint32_t>(r & 7);
-                    const uint32_t row_dst = st + r * 128;
-                    // 16 e4m3 values -> 16 bf16 (two 16-byte chunks of panel lane/4)
-                    uint4 v0, v1;
-                    v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
-                    v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
-                    v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
-                    v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
-                    v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
-                    v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
-                    v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
-                    v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
-                    const uint32_t pan = row_dst + (lane >> 2) * kPanelBytes;
-                    const uint32_t ch = static_cast<uint32_t>((lane & 3) * 2);
-                    ptx::st_shared_v4(pan + ((ch ^ sw) << 4), v0);
-                    ptx::st_shared_v4(pan + (((ch + 1) ^ sw) << 4), v1);
-                    if (lane < 8)
-                        ptx::st_shared_v4(row_dst + 8 * kPanelBytes + ((static_cast<uint32_t>(lane) ^ sw) << 4),
-                                          rope[i]);
+#pragma unroll
+                    for (int cc = 0; cc < 3; ++cc) {
+                        const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+                        if (c < 72) {
+                            const uint32_t dst = dst_row + (c >> 3) * kPanelBytes + (((c & 7) ^ sw) << 4);
+                            ptx::cp_async_16(dst, src + c * 16, nbytes);
+                        }
+                    }
                 }
+                ptx::cp_async_arrive_noinc(bar_full0 + 8u * s);
+            } else {
+                // fp8 rows: each lane of the warp takes 16 latent bytes of a row (dims 16*lane ..
+                // 16*lane+15, tile scale lane/8); lanes 0-7 also take 16 bytes of the bf16 rope.
+                // The loads of a block are issued before waiting for its stage to be free.
+                const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+                uint4 lat[kPerWarp], rope[kPerWarp];
+                float scl[kPerWarp];
+#pragma unroll
+                for (int i = 0; i < kPerWarp; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+                    lat[i] = make_uint4(0u, 0u, 0u, 0u);
+                    rope[i] = make_uint4(0u, 0u, 0u, 0u);
+                    scl[i] = 0.f;
+                    if (r < kRows && slot >= 0) {
+                        const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
+                        lat[i] = ptx::ld_nc_v4(row + 16 * lane);
+                        scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
+                        if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
+                    }
+                }
+                if (b >= NST) {
+                    bool ok = true;
+                    if (lane == 0) ok = wait_empty(s, ((b / NST) - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __syncwarp();
+                    if (!ok) {
+                        aborted = true;
+                        break;
+                    }
+                }
+                const uint32_t st = sKV + s * kStageBytes;
+#pragma unroll
+                for (int i = 0; i < kPerWarp; ++i) {
+                    const int r = pw + kProducerWarps * i;
+                    if (r < kRows) {
+                        const uint32_t sw = static_cast<uint32_t>(r & 7);
+                        const uint32_t row_dst = st + r * 128;
+                        // 16 e4m3 values -> 16 bf16 (two 16-byte chunks of panel lane/4)
+                        uint4 v0, v1;
+                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
+                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
+                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
+                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
+                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
+                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
+                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
+                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
+                        const uint32_t pan = row_dst + (lane >> 2) * kPanelBytes;
+                        const uint32_t ch = static_cast<uint32_t>((lane & 3) * 2);
+                        ptx::st_shared_v4(pan + ((ch ^ sw) << 4), v0);
+                        ptx::st_shared_v4(pan + (((ch + 1) ^ sw) << 4), v1);
+                        if (lane < 8)
+                            ptx::st_shared_v4(row_dst + 8 * kPanelBytes + ((static_cast<uint32_t>(lane) ^ sw) << 4),
+                                              rope[i]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(bar_full0 + 8u * s);
             }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar_full0 + 8u * s);
         }
     }
     ptx::cp_async_wait_all();  // no copy may still be in flight when the CTA leaves

@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_lane = lane < 16;
         const float c = p.sm_scale_log2;
         bool failed = false;
-        int slot_next = row_lane && nb > 0 ? entry_slot(idx_row, j0 + r, j1, p.num_slots) : -1;
+        // raw list entry of this lane's row for the next block (checked when it is used)
+        int raw_next = fetch_entry(idx_row, j0 + r, j1, row_lane && nb > 0);
         // P^T[h][r] sits at pbase[h & 7] + (h >> 3) * 1024 (128B-swizzled K-major rows of 64 bf16)
         uint32_t pbase[8];
 #pragma unroll
@@ -274,10 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         for (int b = 0; b < nb; ++b) {
             const int s = b & 1;
-            const bool valid = slot_next >= 0;
-            slot_next = (row_lane && b + 1 < nb)
-                            ? entry_slot(idx_row, j0 + (b + 1) * kRows + r, j1, p.num_slots)
-                            : -1;
+            const bool valid = valid_slot(raw_next, p.num_slots) >= 0;
+            raw_next = fetch_entry(idx_row, j0 + (b + 1) * kRows + r, j1, row_lane && b + 1 < nb);
             bool ok = true;
             if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);

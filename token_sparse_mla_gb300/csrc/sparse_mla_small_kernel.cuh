@@ -14,8 +14,8 @@
 //                                                V^T comes from the SAME shared-memory tile as K
 //                                                through ldmatrix.trans.
 //
-// Rows arrive in 32-row stages (36,864 bytes; five in flight) gathered by seven producer warps
-// (gather_rows, shared with the tcgen05 kernel).  Each compute warp takes eight of the block's
+// Rows arrive in 32-row stages (five in flight) gathered by seven producer warps
+// (small_gather).  Each compute warp takes eight of the block's
 // rows for the softmax: masking, a running max per head in log2 units with conditional
 // rescaling (only when the max grows by more than 2^8), fp32 partial sums, P^T (bf16) to shared
 // memory.  Splits over a thread-block cluster merge through distributed shared memory exactly as
@@ -32,13 +32,21 @@ constexpr int kSmComputeWarps = 4;
 constexpr int kSmThreads = 32 * (kProducerWarps + kSmComputeWarps);  // 352
 constexpr int kSmCompute0 = 32 * kProducerWarps;                     // first compute thread
 constexpr int kSmKSteps = kDQK / 16 / kSmComputeWarps;               // 9 k-steps per warp
+// Stage layout: row r at r * 1168 bytes (1152 + 16).  Consecutive rows then start four banks
+// apart, so the eight row addresses of every ldmatrix hit disjoint banks without a swizzle, and
+// a whole row can be copied as one contiguous block.
+constexpr int kSmRowStride = 1168;
+constexpr int kSmStageBytes = kSmRows * kSmRowStride;                 // 37376
+// bf16 rows [0, kSmBulkRows) of each stage are copied by one producer warp with one bulk copy
+// (TMA) per row, the other rows by six warps with 16-byte cp.async: the two copy engines keep
+// separate requests in flight, and one of them alone tops out below the SM's share of HBM.
+constexpr int kSmBulkRows = 14;
 
 template <int H>
 struct SmallLayout {
     static_assert(H == 8 || H == 16, "the small-head kernel runs 8 or 16 heads");
     static constexpr int kNT = H / 8;                                // n-tiles of 8 heads
-    static constexpr int kPanelBytes = kSmRows * 128;                // 4096
-    static constexpr int kStageBytes = kPanels * kPanelBytes;        // 36864
+    static constexpr int kStageBytes = kSmStageBytes;
     static constexpr int kOffKV = 0;
     static constexpr int kOffRed = kSmStages * kStageBytes;          // S partials, float4 per lane
     static constexpr int kRedBytes = kSmComputeWarps * 2 * kNT * 32 * 16;
@@ -53,7 +61,8 @@ struct SmallLayout {
     static constexpr int kOffRecv = kOffRecvML + kMaxSplits * 2 * H * 4;  // [splits][H][512/splits] fp32
     static constexpr int kOffBar = kOffRecv + H * kDV * 4;           // full[5], empty[5]
     static constexpr int kOffMisc = kOffBar + 2 * kSmStages * 8;     // abort flag
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffMask = kOffMisc + 16;                   // [5] valid-row mask per stage
+    static constexpr int kBytes = kOffMask + 32;
     static_assert(kOffP % 16 == 0, "ldmatrix rows need 16-byte alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kOffRecv % 16 == 0 && kOffBar % 8 == 0, "alignment of the merge buffers");
@@ -90,6 +99,147 @@ __device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t add
                  : "memory");
 }
 }  // namespace mma16816
+
+// Full-barrier arrivals per stage: bf16 -> six cp.async warps (one per thread) + the bulk warp's
+// lane 0 (with the expected bytes); fp8 -> all seven warps (one per thread).
+template <int KVF>
+__host__ __device__ constexpr int small_full_count() {
+    return KVF == 0 ? 32 * (kProducerWarps - 1) + 1 : 32 * kProducerWarps;
+}
+
+// KV row gather of the small-head kernel (producer warp pw), into kSmStages stages of kSmRows
+// rows in the padded row-major layout.  Invalid entries become zero rows.  Lane i of every
+// producer warp holds the list entry of row i; the last warp also publishes the stage's mask of
+// valid rows (bit i = row i) in sMask[stage] before its arrival on the full barrier, so the
+// compute warps read validity from shared memory after their wait.
+//   bf16: warp 6 takes rows [0, kSmBulkRows), one row per lane, one cp.async.bulk of 1152 bytes
+//         each; warps 0-5 take rows kSmBulkRows + pw + 6 i with 16-byte cp.async.
+//   fp8:  warps 0-6 take rows pw + 7 i; each lane loads 16 latent bytes, its tile scale and
+//         (lanes 0-7) 16 rope bytes into registers, dequantises (e4m3 -> f16 exactly, x scale in
+//         fp32, -> bf16 round to nearest even) and stores the bf16 row.
+template <int KVF>
+__device__ __forceinline__ void small_gather(const FwdParams& p, const int32_t* idx_row, int j0, int j1, int nb,
+                                             int pw, int lane, uint32_t sKV, uint32_t bar_full0,
+                                             uint32_t bar_empty0, uint32_t sMask, volatile int* sAbort) {
+    // List entries are loaded kAhead blocks (256 entries) ahead into a ring indexed by
+    // b % kAhead; the block loop is unrolled kAhead times so each ring index is static and an
+    // entry is first read kAhead blocks after its load was issued.
+    constexpr int kAhead = 8;
+    constexpr int kRow0 = KVF == 0 ? kSmBulkRows : 0;
+    constexpr int kWarps = KVF == 0 ? kProducerWarps - 1 : kProducerWarps;
+    constexpr int kPerWarp = (kSmRows - kRow0 + kWarps - 1) / kWarps;
+    constexpr uint32_t kBulkMask = kSmBulkRows >= 32 ? 0xffffffffu : ((1u << kSmBulkRows) - 1u);
+    const bool mask_warp = pw == kProducerWarps - 1;
+    int ring[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) ring[u] = fetch_entry(idx_row, j0 + u * kSmRows + lane, j1, u < nb);
+    bool aborted = false;
+    for (int b0 = 0; b0 < nb && !aborted; b0 += kAhead) {
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int b = b0 + u;
+            if (b >= nb) break;
+            const int s = b % kSmStages;
+            const uint32_t full = bar_full0 + 8u * s;
+            const int my_slot = valid_slot(ring[u], p.num_slots);  // slot of row `lane`
+            ring[u] = fetch_entry(idx_row, j0 + (b + kAhead) * kSmRows + lane, j1, b + kAhead < nb);
+            const uint32_t vmask = __ballot_sync(0xffffffffu, my_slot >= 0);
+            if (b >= kSmStages) {
+                bool ok = true;
+                if (lane == 0)
+                    ok = ptx::mbar_wait(bar_empty0 + 8u * s, ((b / kSmStages) - 1) & 1, sAbort, &g_smla_error,
+                                        kErrTimeout, kWaitLimitNs);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                __syncwarp();
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+            }
+            const uint32_t st = sKV + s * kSmStageBytes;
+            if constexpr (KVF == 0) {
+                if (mask_warp) {
+                    const bool bulk_row = lane < kSmBulkRows;
+                    if (bulk_row && my_slot < 0)  // zero row; written before this warp's arrive below
+                        for (int c = 0; c < 72; ++c)
+                            ptx::st_shared_v4(st + lane * kSmRowStride + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::st_shared_u32(sMask + 4u * s, vmask);
+                        ptx::mbar_arrive_expect_tx(full, __popc(vmask & kBulkMask) * (kDQK * 2));
+                    }
+                    __syncwarp();
+                    if (bulk_row && my_slot >= 0)
+                        ptx::bulk_load(st + lane * kSmRowStride,
+                                       reinterpret_cast<const char*>(p.kv) + static_cast<int64_t>(my_slot) * (kDQK * 2),
+                                       kDQK * 2, full);
+                } else {
+#pragma unroll 1
+                    for (int i = 0; i < kPerWarp; ++i) {
+                        const int r = kRow0 + pw + kWarps * i;
+                        if (r >= kSmRows) break;
+                        const int slot = __shfl_sync(0xffffffffu, my_slot, r);
+                        const char* src =
+                            reinterpret_cast<const char*>(p.kv) + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
+                        const uint32_t nbytes = slot < 0 ? 0u : 16u;
+#pragma unroll
+                        for (int cc = 0; cc < 3; ++cc) {
+                            const int c = lane + 32 * cc;  // 16-byte chunk of the 1152-byte row
+                            if (c < 72) ptx::cp_async_16(st + r * kSmRowStride + c * 16, src + c * 16, nbytes);
+                        }
+                    }
+                    ptx::cp_async_arrive_noinc(full);
+                }
+            } else {
+                const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+                uint4 lat[kPerWarp], rope[kPerWarp];
+                float scl[kPerWarp];
+#pragma unroll
+                for (int i = 0; i < kPerWarp; ++i) {
+                    const int r = pw + kWarps * i;
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, r & 31);
+                    lat[i] = make_uint4(0u, 0u, 0u, 0u);
+                    rope[i] = make_uint4(0u, 0u, 0u, 0u);
+                    scl[i] = 0.f;
+                    if (r < kSmRows && slot >= 0) {
+                        const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
+                        lat[i] = ptx::ld_nc_v4(row + 16 * lane);
+                        scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
+                        if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kPerWarp; ++i) {
+                    const int r = pw + kWarps * i;
+                    if (r < kSmRows) {
+                        uint4 v0, v1;
+                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
+                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
+                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
+                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
+                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
+                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
+                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
+                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
+                        const uint32_t rd = st + r * kSmRowStride;
+                        ptx::st_shared_v4(rd + (2 * lane) * 16, v0);      // dims 16 lane .. +7
+                        ptx::st_shared_v4(rd + (2 * lane + 1) * 16, v1);  // dims 16 lane + 8 .. +15
+                        if (lane < 8) ptx::st_shared_v4(rd + (64 + lane) * 16, rope[i]);
+                    }
+                }
+                if (mask_warp && lane == 0) ptx::st_shared_u32(sMask + 4u * s, vmask);
+                ptx::mbar_arrive(full);
+            }
+        }
+    }
+    ptx::cp_async_wait_all();  // no cp.async may still be in flight when the CTA leaves
+    if (KVF == 0 && mask_warp && (aborted || *sAbort)) {
+        // bulk copies have no per-thread wait: give any still in flight time to land (bounded)
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+        }
+    }
+}
 
 template <int H, int KVF>
 __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
@@ -130,7 +280,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     if (threadIdx.x == 0) {
         *sAbort = 0;
         for (int s = 0; s < kSmStages; ++s) {
-            ptx::mbar_init(bar_full0 + 8 * s, 32 * kProducerWarps);
+            ptx::mbar_init(bar_full0 + 8 * s, small_full_count<KVF>());
             ptx::mbar_init(bar_empty0 + 8 * s, kSmComputeWarps);
         }
         ptx::fence_mbarrier_init();
@@ -153,8 +303,8 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
 
     if (warp < kProducerWarps) {
         // ================================================================ producers
-        gather_rows<kSmRows, kSmStages, KVF>(p, idx_row, j0, j1, nb, warp, lane, sKV, bar_full0, bar_empty0,
-                                             sAbort);
+        small_gather<KVF>(p, idx_row, j0, j1, nb, warp, lane, sKV, bar_full0, bar_empty0, sbase + L::kOffMask,
+                          sAbort);
     } else {
         // ================================================================ compute warps
         const int cw = warp - kProducerWarps;   // 0..3
@@ -183,13 +333,6 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         // this warp's softmax rows: 8 of the block's 32 (m-tile cw/2, half cw%2), one per lane group
         const int mt_s = cw >> 1, half = cw & 1;
         const int rr = mt_s * 16 + half * 8 + g;
-        // slot validity of this lane's row, loaded kAhead blocks ahead
-        constexpr int kAhead = 8;
-        int slot_q[kAhead];
-#pragma unroll
-        for (int i = 0; i < kAhead; ++i)
-            slot_q[i] = i < nb ? entry_slot(idx_row, j0 + i * kSmRows + rr, j1, p.num_slots) : -1;
-
         float lsum[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
@@ -197,11 +340,6 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         for (int b = 0; b < nb; ++b) {
             const int s = b % kSmStages;
             const uint32_t stb = sKV + s * L::kStageBytes;
-            const bool valid = slot_q[0] >= 0;
-#pragma unroll
-            for (int i = 0; i + 1 < kAhead; ++i) slot_q[i] = slot_q[i + 1];
-            slot_q[kAhead - 1] =
-                (b + kAhead < nb) ? entry_slot(idx_row, j0 + (b + kAhead) * kSmRows + rr, j1, p.num_slots) : -1;
             bool ok = true;
             if (lane == 0)
                 ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / kSmStages) & 1, sAbort, &g_smla_error, kErrTimeout,
@@ -209,6 +347,8 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();
             if (!ok) failed = true;
+            // valid rows of this block, published by the producers before their arrival
+            const bool valid = (ptx::ld_shared_u32(sbase + L::kOffMask + 4u * s) >> rr) & 1u;
 
             // ---- partial S^T over this warp's 144 dims, all 32 rows
             float cs[2][NT][4];
@@ -222,13 +362,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
 #pragma unroll
                 for (int kk = 0; kk < kSmKSteps; ++kk) {
                     const int K = kSmKSteps * cw + kk;
-                    const uint32_t pan = stb + (K >> 2) * L::kPanelBytes;
-                    const int chunk = (K & 3) * 2 + (lj >> 1);
+                    const uint32_t kchunk = static_cast<uint32_t>((2 * K + (lj >> 1)) * 16);
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
-                        const int row = mt * 16 + (lj & 1) * 8 + li;  // row & 7 == li
+                        const int row = mt * 16 + (lj & 1) * 8 + li;
                         uint32_t a[4];
-                        mma16816::ldsm_x4(a, pan + row * 128 + ((chunk ^ li) << 4));
+                        mma16816::ldsm_x4(a, stb + row * kSmRowStride + kchunk);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) mma16816::mma(cs[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
                     }
@@ -330,13 +469,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
                         bp[0][0] = r4[0]; bp[0][1] = r4[1];
                         bp[NT - 1][0] = r4[2]; bp[NT - 1][1] = r4[3];
                     }
-                    const int krow = 16 * kk + (lj >> 1) * 8 + li;  // krow & 7 == li
+                    const int krow = 16 * kk + (lj >> 1) * 8 + li;
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
                         const int d0 = 128 * cw + 16 * mt;
-                        const int chunk = ((d0 & 63) >> 3) + (lj & 1);
                         uint32_t a[4];
-                        mma16816::ldsm_x4_trans(a, stb + (d0 >> 6) * L::kPanelBytes + krow * 128 + ((chunk ^ li) << 4));
+                        mma16816::ldsm_x4_trans(a, stb + krow * kSmRowStride + (d0 / 8 + (lj & 1)) * 16);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) mma16816::mma(o[mt][nt], a, bp[nt][0], bp[nt][1]);
                     }
