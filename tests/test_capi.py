@@ -79,9 +79,18 @@ def test_zero_tokens_is_a_noop(lib):
 
 
 def test_launch_info_without_device(lib):
+    # 8/16 heads: 32 tokens x 64 row blocks on 152 SMs (assumed without a device): four CTAs
+    # per token (the largest power of two dividing 64 with 32 x s <= 152), no cluster
     info = smla.launch_info(32, 8, 2048)
-    assert info["launches"] == 1 and info["splits"] in (1, 2, 4, 8)
-    assert info["ctas"] == 32 * info["splits"]
+    assert info["launches"] == 1 and info["splits"] == 0 and info["ctas"] == 128
+    # as many tokens as SMs: one CTA per token
+    assert smla.launch_info(152, 8, 2048)["ctas"] == 152
+    assert info["smem_bytes"] <= 232448
+    # fewer blocks than SMs: one CTA per 32-entry block
+    assert smla.launch_info(2, 16, 100)["ctas"] == 2 * 4
+    # 32/64 heads: a cluster of `splits` CTAs per token
+    info = smla.launch_info(32, 64, 2048)
+    assert info["splits"] in (1, 2, 4, 8) and info["ctas"] == 32 * info["splits"]
     assert info["smem_bytes"] <= 232448
     assert smla.launch_info(0, 8, 2048)["launches"] == 0
     with pytest.raises(smla.SparseMLAError):

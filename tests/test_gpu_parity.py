@@ -96,6 +96,44 @@ def test_ragged_topk(topk, h):
         check_case(q, kv, idx, 576 ** -0.5, splits, what=f"topk={topk} h={h} splits={splits}")
 
 
+@pytest.mark.parametrize("T,topk,splits", [(1, 4096, 0), (5, 2048, 0), (3, 33, 8), (7, 300, 4),
+                                           (200, 2048, 2), (153, 300, 4)])
+@pytest.mark.parametrize("h", [8, 16])
+def test_balanced_partition_cuts_lists_anywhere(T, topk, splits, h):
+    # 8/16 heads cut the T x ceil(topk/32) row blocks into equal ranges, one per CTA: aligned
+    # (16 CTAs per list, one block per CTA) and unaligned (ranges that end inside one list and
+    # start inside another, up to one CTA per SM); cut lists merge after the grid barrier
+    q, kv, idx = _rand(300 + T + topk, T, h, topk, 8192, p_invalid=0.05)
+    check_case(q, kv, idx, 576 ** -0.5, splits, what=f"balanced T={T} topk={topk} splits={splits} h={h}")
+
+
+def test_balanced_partition_repeats_bit_for_bit():
+    # the merge counters return to zero after every launch and partials are summed in CTA order:
+    # repeated calls, a second stream and a replayed CUDA graph all give identical bytes
+    q, kv, idx = _rand(77, 7, 8, 300, 8192, p_invalid=0.05)  # splits=4: unaligned cuts
+    q, kv, idx = q.to(DEV), kv.to(DEV), idx.to(DEV)
+    o1, l1 = smla.sparse_mla_fwd(q, kv, idx, 0.05, splits=4)
+    o2, l2 = smla.sparse_mla_fwd(q, kv, idx, 0.05, splits=4)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o3, l3 = smla.sparse_mla_fwd(q, kv, idx, 0.05, splits=4, stream=s)  # sizes this stream's scratch
+        g = torch.cuda.CUDAGraph()
+        og = torch.empty_like(o1)
+        lg = torch.empty_like(l1)
+    with torch.cuda.graph(g, stream=s):
+        smla.sparse_mla_fwd(q, kv, idx, 0.05, out=og, lse=lg, splits=4, stream=s)
+    for _ in range(3):
+        og.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(og, o1) and torch.equal(lg, l1)
+    smla.sync_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+    ref_o, ref_l = oracle.sparse_mla_fwd(q.cpu(), kv.cpu(), idx.cpu(), 0.05)
+    assert_parity(o1.cpu(), l1.cpu(), ref_o, ref_l, what="balanced repeat")
+
+
 def test_out_of_range_and_negative_indices_are_masked():
     q, kv, idx = _rand(7, 4, 16, 200, 1000, p_invalid=0.2)
     idx[0, 3] = 1000          # == num_slots

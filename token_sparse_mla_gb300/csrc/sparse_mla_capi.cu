@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "sparse_mla.h"
 #include "sparse_mla_kernel.cuh"
@@ -102,6 +103,8 @@ smla_status encode_fn(EncodeTiledFn* fn) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 // 8 and 16 heads run the warp-MMA kernel (32-row stages); 32 and 64 the tcgen05 kernel.
 bool small_heads(int h) { return h <= 16; }
 
@@ -121,10 +124,20 @@ int auto_splits(int64_t T, int nblk, int num_sms) {
 struct Plan {
     int hp = 16;
     int threads = 0;
-    int splits = 1;
+    int splits = 1;       // tcgen05 kernel: CTAs (cluster) per token; small-head kernel: 0
     int64_t ctas = 0;
     int smem = 0;
+    int nblk = 0;         // row blocks per token
+    size_t scratch = 0;   // small-head kernel: bytes of merge scratch (0 = no token is cut)
 };
+
+// Scratch of the small-head kernel's balanced partition: the grid-barrier words (arrival count
+// and generation, in a 256-byte head that starts zeroed) followed by grid x 2 partial slots of
+// (2h + 512h) floats.
+constexpr size_t kScratchHead = 256;
+size_t small_scratch_bytes(int64_t grid, int h) {
+    return kScratchHead + static_cast<size_t>(grid) * 2 * (2 * h + h * smla::kDV) * 4;
+}
 
 smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
                        int32_t topk, int64_t num_slots, int32_t kv_format, float scale,
@@ -149,6 +162,7 @@ smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_
         return fail(SMLA_ERR_INVALID_ARG, "indices and lse must be 4-byte aligned");
     if (static_cast<int64_t>(T) * 8 > 0x7fffffffLL)
         return fail(SMLA_ERR_INVALID_ARG, "T too large for one launch (%d)", T);
+    if (topk > (1 << 20)) return fail(SMLA_ERR_INVALID_ARG, "topk above 2^20 (%d)", topk);
     return SMLA_OK;
 }
 
@@ -157,14 +171,92 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms) 
     pl.hp = h;
     const int rows = small_heads(h) ? smla::kSmRows : smla::kRows;
     const int nblk = (topk + rows - 1) / rows;
-    pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
-    pl.ctas = static_cast<int64_t>(T) * pl.splits;
+    pl.nblk = nblk;
+    if (small_heads(h)) {
+        // The T * nblk row blocks are cut into `ctas` equal contiguous ranges.  Default: whole
+        // lists (one CTA per token) once the tokens alone fill the SMs; otherwise s CTAs per
+        // token, s the largest power of two that divides nblk with T * s <= #SMs and s <= 16,
+        // so every range lies within one list (each CTA then merges one cut list).  Given
+        // `splits`: T * splits CTAs, wherever the cuts fall.  Cut lists are merged after a
+        // grid-wide barrier, so such a launch never has more CTAs than SMs.
+        const int64_t W = static_cast<int64_t>(T) * nblk;
+        int64_t want = T;
+        if (splits > 0) {
+            want = static_cast<int64_t>(T) * splits;
+        } else {
+            for (int c = smla::kMaxParts; c > 1; c >>= 1) {
+                if (nblk % c == 0 && static_cast<int64_t>(T) * c <= num_sms) {
+                    want = static_cast<int64_t>(T) * c;
+                    break;
+                }
+            }
+        }
+        pl.splits = 0;
+        pl.ctas = W < want ? W : want;
+        auto whole_lists = [&](int64_t g) { return W % g == 0 && (W / g) % nblk == 0; };
+        if (pl.ctas > num_sms && !whole_lists(pl.ctas)) pl.ctas = num_sms;
+        if (pl.ctas > 0 && !whole_lists(pl.ctas)) pl.scratch = small_scratch_bytes(pl.ctas, h);
+    } else {
+        pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
+        pl.ctas = static_cast<int64_t>(T) * pl.splits;
+    }
     pl.threads = small_heads(h) ? smla::kSmThreads : smla::kThreads;
     pl.smem = h == 8    ? smla::SmallLayout<8>::kBytes
               : h == 16 ? smla::SmallLayout<16>::kBytes
               : h == 32 ? smla::Layout<32>::kBytes
                         : smla::Layout<64>::kBytes;
     return pl;
+}
+
+// Library-owned merge scratch, one buffer per (device, stream), grown on demand.  Calls on one
+// stream are ordered, so they can share it; calls on different streams get different buffers.
+struct Scratch {
+    int dev = 0;
+    cudaStream_t stream = nullptr;
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_scratch_mu;
+std::vector<Scratch> g_scratch;
+
+smla_status stream_scratch(int dev, cudaStream_t stream, size_t need, void** ptr) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    Scratch* sc = nullptr;
+    for (Scratch& x : g_scratch)
+        if (x.dev == dev && x.stream == stream) sc = &x;
+    if (!sc) {
+        g_scratch.push_back(Scratch{});
+        sc = &g_scratch.back();
+        sc->dev = dev;
+        sc->stream = stream;
+    }
+    if (sc->bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(SMLA_ERR_INVALID_ARG,
+                        "stream capture needs %zu bytes of merge scratch on this stream; make one call of "
+                        "the same size on the stream before capturing", need);
+        if (sc->ptr) {
+            e = cudaStreamSynchronize(stream);  // earlier launches may still use the old buffer
+            if (e == cudaSuccess) e = cudaFree(sc->ptr);
+            sc->ptr = nullptr;
+            sc->bytes = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "releasing the merge scratch");
+        }
+        void* p = nullptr;
+        e = cudaMalloc(&p, need);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, need, stream);
+        if (e != cudaSuccess) {
+            if (p) cudaFree(p);
+            return cuda_fail(e, "allocating the merge scratch");
+        }
+        sc->ptr = p;
+        sc->bytes = need;
+    }
+    *ptr = sc->ptr;
+    return SMLA_OK;
 }
 
 smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
@@ -176,11 +268,11 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     DeviceState* ds = nullptr;
     if ((st = device_state(&dev, &ds)) != SMLA_OK) return st;
     EncodeTiledFn enc = nullptr;
-    if ((st = encode_fn(&enc)) != SMLA_OK) return st;
+    if (!small_heads(h) && (st = encode_fn(&enc)) != SMLA_OK) return st;
     const Plan pl = make_plan(T, h, topk, splits, ds->num_sms);
 
     alignas(64) CUtensorMap tm_q;
-    {
+    if (!small_heads(h)) {  // the tcgen05 kernel loads Q^T with TMA
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(smla::kDQK), static_cast<cuuint64_t>(h),
                                     static_cast<cuuint64_t>(T)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(smla::kDQK) * 2,
@@ -205,6 +297,16 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     prm.topk = topk;
     prm.splits = pl.splits;
     prm.sm_scale_log2 = scale * 1.4426950408889634f;
+    prm.grid = static_cast<int32_t>(pl.ctas);
+    prm.nblk = pl.nblk;
+    prm.part = nullptr;
+    prm.gbar = nullptr;
+    if (pl.scratch > 0) {
+        void* sp = nullptr;
+        if ((st = stream_scratch(dev, stream, pl.scratch, &sp)) != SMLA_OK) return st;
+        prm.gbar = static_cast<unsigned int*>(sp);
+        prm.part = reinterpret_cast<float*>(static_cast<char*>(sp) + kScratchHead);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
@@ -217,6 +319,12 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
         attr[0].val.clusterDim.x = static_cast<unsigned>(pl.splits);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else if (pl.scratch > 0) {
+        // the merge of cut lists waits at a grid-wide barrier: all CTAs must be co-resident
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
@@ -237,8 +345,6 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return SMLA_OK;
 }
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
@@ -314,8 +420,17 @@ smla_status sparse_mla_sync_status(void* stream) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(smla::g_smla_error, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
-        if (word & smla::kErrTimeout)
+        if (word & smla::kErrTimeout) {
+            // a launch gave up part-way: its grid-barrier words may be left mid-count, so every
+            // library-owned scratch of this device starts again from cleared words
+            int dev = 0;
+            if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess) {
+                std::lock_guard<std::mutex> lock(g_scratch_mu);
+                for (Scratch& x : g_scratch)
+                    if (x.dev == dev && x.ptr) cudaMemset(x.ptr, 0, kScratchHead);
+            }
             return fail(SMLA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (error word 0x%x)", word);
+        }
         return fail(SMLA_ERR_CUDA, "kernel reported an error (error word 0x%x)", word);
     }
     return SMLA_OK;

@@ -16,6 +16,7 @@ constexpr int kDQK = 576;                           // 512 latent + 64 rope dims
 constexpr int kDV = 512;                            // value / output dims (the latent part)
 constexpr int kPanels = kDQK / 64;                  // 9 panels of 64 bf16 = 128 bytes per row
 constexpr int kMaxSplits = 8;                       // CTAs per token (one portable cluster)
+constexpr int kMaxParts = 16;                       // CTAs sharing one token (balanced partition)
 constexpr int kProducerWarps = 7;
 constexpr int kFp8RowBytes = 656;
 constexpr float kRescaleLog2 = 8.0f;                // rescale O only when max grows by > 2^8
@@ -35,6 +36,13 @@ struct FwdParams {
     int64_t num_slots;
     int32_t T, h, topk, splits;
     float sm_scale_log2;      // scale * log2(e)
+    // balanced partition (small-head kernel): `grid` CTAs take equal contiguous ranges of the
+    // token-major sequence of T * nblk row blocks; the parts of a list cut between CTAs go to
+    // `part` ([grid][2] slots of 2h + 512h floats) and are merged after a grid-wide barrier on
+    // the counter words `gbar` (cooperative launch).  part == nullptr: no list is cut.
+    int32_t grid, nblk;
+    float* part;
+    unsigned int* gbar;
 };
 
 __device__ unsigned int g_smla_error;

@@ -15,11 +15,18 @@
 //                                                through ldmatrix.trans.
 //
 // Rows arrive in 32-row stages (five in flight) gathered by seven producer warps
-// (small_gather).  Each compute warp takes eight of the block's
-// rows for the softmax: masking, a running max per head in log2 units with conditional
-// rescaling (only when the max grows by more than 2^8), fp32 partial sums, P^T (bf16) to shared
-// memory.  Splits over a thread-block cluster merge through distributed shared memory exactly as
-// in the tcgen05 kernel.
+// (small_gather).  Each compute warp takes eight of the block's rows for the softmax: masking, a
+// running max per head in log2 units with conditional rescaling (only when the max grows by more
+// than 2^8), fp32 partial sums, P^T (bf16) to shared memory.
+//
+// Work partition: the T * nblk row blocks (nblk = ceil(topk / 32) per token, token-major) are
+// cut into `grid` equal contiguous ranges, one per CTA (grid = the SM count by default), so every
+// SM gets the same number of rows whatever T is.  A CTA walks its range as consecutive token
+// segments; its producers stream straight across token boundaries.  A token whose whole list
+// lies in one CTA is normalised and stored directly; a token cut between CTAs leaves one partial
+// (m, L, unnormalised O) per CTA in a global scratch slot, and the last CTA to arrive on the
+// token's counter merges them (weights 2^(m_j - M) / sum_j L_j 2^(m_j - M), in CTA order, so
+// the result does not depend on which CTA merges).
 #pragma once
 
 #include "sparse_mla_common.cuh"
@@ -52,22 +59,57 @@ struct SmallLayout {
     static constexpr int kRedBytes = kSmComputeWarps * 2 * kNT * 32 * 16;
     static constexpr int kPStride = 80;                              // bytes per head row of P^T
     static constexpr int kOffP = kOffRed + kRedBytes;
-    static constexpr int kOffHr = kOffP + H * kPStride;              // [8][H]: per-warp reductions,
-                                                                     // per-source merge weights
-    static constexpr int kOffM = kOffHr + kMaxSplits * H * 4;        // running max (log2 units)
-    static constexpr int kOffAlpha = kOffM + H * 4;                  // rescale factor / 1/L / weight
-    static constexpr int kOffML = kOffAlpha + H * 4;                 // final m[H], L[H]
-    static constexpr int kOffRecvML = kOffML + 2 * H * 4;            // [kMaxSplits][2H] (m, L) of peers
-    static constexpr int kOffRecv = kOffRecvML + kMaxSplits * 2 * H * 4;  // [splits][H][512/splits] fp32
-    static constexpr int kOffBar = kOffRecv + H * kDV * 4;           // full[5], empty[5]
-    static constexpr int kOffMisc = kOffBar + 2 * kSmStages * 8;     // abort flag
+    static constexpr int kOffHr = kOffP + H * kPStride;              // [4][H] per-warp reductions
+    static constexpr int kOffM = kOffHr + kSmComputeWarps * H * 4;   // running max (log2 units)
+    static constexpr int kOffAlpha = kOffM + H * 4;                  // rescale factor / 1/L
+    static constexpr int kOffML = kOffAlpha + H * 4;                 // segment m[H], L[H]
+    static constexpr int kOffOut = kOffML + 2 * H * 4;               // bf16 output staging [H][512]
+    static constexpr int kOffBar = kOffOut + H * kDV * 2;            // full[5], empty[5]
+    static constexpr int kOffMisc = kOffBar + 2 * kSmStages * 8;     // abort flag, last-arrival flag
     static constexpr int kOffMask = kOffMisc + 16;                   // [5] valid-row mask per stage
-    static constexpr int kBytes = kOffMask + 32;
-    static_assert(kOffP % 16 == 0, "ldmatrix rows need 16-byte alignment");
+    static constexpr int kOffMrg = kOffMask + 32;                    // merge: m, L, weight [16][H] each
+    static constexpr int kBytes = kOffMrg + 3 * kMaxParts * H * 4;
+    // scratch slot of one partial segment: m[H], L[H], then O^T unnormalised as [H][512] fp32
+    static constexpr int kSlotFloats = 2 * H + H * kDV;
+    static_assert(kOffP % 16 == 0 && kOffOut % 16 == 0, "16-byte aligned shared buffers");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
-    static_assert(kOffRecv % 16 == 0 && kOffBar % 8 == 0, "alignment of the merge buffers");
-    static_assert(H * kDV * 2 <= kSmStages * kStageBytes, "output staging fits the stages");
+    static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
+
+// Balanced partition of W row blocks over G CTAs: CTA i takes q + (i < r) blocks (q = W / G,
+// r = W % G), starting at flat_begin(i).  G <= W, so q >= 1 and no range is empty.
+__device__ __forceinline__ int64_t flat_begin(int64_t i, int64_t q, int64_t r) { return i * q + (i < r ? i : r); }
+
+// The CTA whose range holds block x.
+__device__ __forceinline__ int64_t flat_owner(int64_t x, int64_t q, int64_t r) {
+    const int64_t big = r * (q + 1);
+    return x < big ? x / (q + 1) : r + (x - big) / q;
+}
+
+// Grid-wide barrier of a cooperative launch (sense reversal): bar[0] counts arrivals, bar[32]
+// is the generation.  Each CTA reads the generation, then arrives; the last arrival resets the
+// count and advances the generation, which releases the others.  The count is back at zero after
+// every completed barrier, so launches of any grid size (and CUDA graph replays) can share the
+// words.  Bounded: gives up after kWaitLimitNs and reports a timeout.
+__device__ __forceinline__ bool grid_barrier(unsigned int* bar, unsigned int grid) {
+    unsigned int* count = bar;
+    unsigned int* gen = bar + 32;  // its own 128-byte line
+    const unsigned int g = ptx::ld_acquire_gpu_u32(gen);
+    if (atomicAdd(count, 1u) == grid - 1u) {
+        *reinterpret_cast<volatile unsigned int*>(count) = 0u;
+        ptx::st_release_gpu_u32(gen, g + 1u);
+        return true;
+    }
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::ld_acquire_gpu_u32(gen) == g) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_smla_error, kErrTimeout);
+            return false;
+        }
+        __nanosleep(100);
+    }
+    return true;
+}
 
 namespace mma16816 {
 // D (16x8 fp32) += A (16x16 bf16, row) . B (16x8 bf16, col)
@@ -118,9 +160,9 @@ __host__ __device__ constexpr int small_full_count() {
 //         (lanes 0-7) 16 rope bytes into registers, dequantises (e4m3 -> f16 exactly, x scale in
 //         fp32, -> bf16 round to nearest even) and stores the bf16 row.
 template <int KVF>
-__device__ __forceinline__ void small_gather(const FwdParams& p, const int32_t* idx_row, int j0, int j1, int nb,
-                                             int pw, int lane, uint32_t sKV, uint32_t bar_full0,
-                                             uint32_t bar_empty0, uint32_t sMask, volatile int* sAbort) {
+__device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int nb, int pw, int lane, uint32_t sKV,
+                                             uint32_t bar_full0, uint32_t bar_empty0, uint32_t sMask,
+                                             volatile int* sAbort) {
     // List entries are loaded kAhead blocks (256 entries) ahead into a ring indexed by
     // b % kAhead; the block loop is unrolled kAhead times so each ring index is static and an
     // entry is first read kAhead blocks after its load was issued.
@@ -130,9 +172,22 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, const int32_t* 
     constexpr int kPerWarp = (kSmRows - kRow0 + kWarps - 1) / kWarps;
     constexpr uint32_t kBulkMask = kSmBulkRows >= 32 ? 0xffffffffu : ((1u << kSmBulkRows) - 1u);
     const bool mask_warp = pw == kProducerWarps - 1;
+    // fetch cursor: token ft, first list entry fj of the next block to fetch (blocks x0, x0+1, ...)
+    const int kpad = p.nblk * kSmRows;
+    int ft = static_cast<int>(x0 / p.nblk);
+    int fj = static_cast<int>(x0 - static_cast<int64_t>(ft) * p.nblk) * kSmRows;
+    auto fetch = [&](bool pred) -> int {
+        const int v = fetch_entry(p.indices + static_cast<int64_t>(ft) * p.topk, fj + lane, p.topk, pred);
+        fj += kSmRows;
+        if (fj >= kpad) {
+            fj = 0;
+            ++ft;
+        }
+        return v;
+    };
     int ring[kAhead];
 #pragma unroll
-    for (int u = 0; u < kAhead; ++u) ring[u] = fetch_entry(idx_row, j0 + u * kSmRows + lane, j1, u < nb);
+    for (int u = 0; u < kAhead; ++u) ring[u] = fetch(u < nb);
     bool aborted = false;
     for (int b0 = 0; b0 < nb && !aborted; b0 += kAhead) {
 #pragma unroll
@@ -142,7 +197,7 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, const int32_t* 
             const int s = b % kSmStages;
             const uint32_t full = bar_full0 + 8u * s;
             const int my_slot = valid_slot(ring[u], p.num_slots);  // slot of row `lane`
-            ring[u] = fetch_entry(idx_row, j0 + (b + kAhead) * kSmRows + lane, j1, b + kAhead < nb);
+            ring[u] = fetch(b + kAhead < nb);
             const uint32_t vmask = __ballot_sync(0xffffffffu, my_slot >= 0);
             if (b >= kSmStages) {
                 bool ok = true;
@@ -241,6 +296,24 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, const int32_t* 
     }
 }
 
+// Q^T fragments (B operand of S^T) of token t for compute warp cw's nine 16-dim k-steps.
+template <int H>
+__device__ __forceinline__ void load_q_frags(const FwdParams& p, int t, int cw, int lane,
+                                             uint32_t (&bq)[kSmKSteps][H / 8][2]) {
+    const int g = lane >> 2, tq = lane & 3;
+    const __nv_bfloat16* qt = p.q + static_cast<int64_t>(t) * H * kDQK;
+#pragma unroll
+    for (int kk = 0; kk < kSmKSteps; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < H / 8; ++nt) {
+            const unsigned int* qr = reinterpret_cast<const unsigned int*>(
+                qt + (nt * 8 + g) * kDQK + 16 * (kSmKSteps * cw + kk) + 2 * tq);
+            bq[kk][nt][0] = __ldg(qr);
+            bq[kk][nt][1] = __ldg(qr + 4);
+        }
+    }
+}
+
 template <int H, int KVF>
 __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
     using L = SmallLayout<H>;
@@ -264,18 +337,11 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     const uint32_t bar_full0 = sbase + L::kOffBar;
     const uint32_t bar_empty0 = sbase + L::kOffBar + 8 * kSmStages;
 
-    // ---- work of this CTA
-    const int splits = p.splits;
-    const int t = blockIdx.x / splits;
-    const int rank = blockIdx.x % splits;  // == %cluster_ctarank when splits > 1
-    const int nblk_total = (p.topk + kSmRows - 1) / kSmRows;
-    const int per_split = (nblk_total + splits - 1) / splits;
-    const int b_begin = min(nblk_total, rank * per_split);
-    const int b_end = min(nblk_total, b_begin + per_split);
-    const int nb = b_end - b_begin;
-    const int j0 = b_begin * kSmRows;
-    const int j1 = min(p.topk, b_end * kSmRows);
-    const int32_t* idx_row = p.indices + static_cast<int64_t>(t) * p.topk;
+    // ---- this CTA's blocks [x0, x0 + nb) of the token-major block sequence
+    const int64_t W = static_cast<int64_t>(p.T) * p.nblk;
+    const int64_t fq = W / p.grid, fr = W % p.grid;
+    const int64_t x0 = flat_begin(blockIdx.x, fq, fr);
+    const int nb = static_cast<int>(fq + (static_cast<int64_t>(blockIdx.x) < fr ? 1 : 0));
 
     if (threadIdx.x == 0) {
         *sAbort = 0;
@@ -287,205 +353,198 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     }
     if (threadIdx.x >= kSmCompute0 && threadIdx.x - kSmCompute0 < H) sM[threadIdx.x - kSmCompute0] = -CUDART_INF_F;
     __syncthreads();
-    // peers push into this CTA's receive buffers at the end; the matching wait below makes sure
-    // every CTA of the cluster has started before any of them writes to another
-    if (splits > 1) ptx::cluster_arrive_relaxed();
 
-    // O^T accumulators of the compute warps (fragment layout: dims 128*cw + 16*mt + g (+8),
-    // heads 8*nt + 2*tq (+1)); declared here because the cluster merge below reads them
-    float o[8][SmallLayout<H>::kNT][4];
+    if (warp < kProducerWarps) {
+        // ================================================================ producers
+        small_gather<KVF>(p, x0, nb, warp, lane, sKV, bar_full0, bar_empty0, sbase + L::kOffMask, sAbort);
+        return;
+    }
+    // ==================================================================== compute warps
+    const int cw = warp - kProducerWarps;   // 0..3
+    const int wtid = threadIdx.x - kSmCompute0;
+    const int g = lane >> 2;                // MMA fragment row group
+    const int tq = lane & 3;                // MMA fragment column pair
+    const int li = lane & 7, lj = lane >> 3;  // ldmatrix: row within matrix, matrix index
+    const float c = p.sm_scale_log2;
+    bool failed = false;
+
+    // O^T accumulators (fragment layout: dims 128*cw + 16*mt + g (+8), heads 8*nt + 2*tq (+1))
+    float o[8][NT][4];
+    float lsum[NT][2];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
 
-    if (warp < kProducerWarps) {
-        // ================================================================ producers
-        small_gather<KVF>(p, idx_row, j0, j1, nb, warp, lane, sKV, bar_full0, bar_empty0, sbase + L::kOffMask,
-                          sAbort);
-    } else {
-        // ================================================================ compute warps
-        const int cw = warp - kProducerWarps;   // 0..3
-        const int wtid = threadIdx.x - kSmCompute0;
-        const int g = lane >> 2;                // MMA fragment row group
-        const int tq = lane & 3;                // MMA fragment column pair
-        const int li = lane & 7, lj = lane >> 3;  // ldmatrix: row within matrix, matrix index
-        const float c = p.sm_scale_log2;
-        bool failed = false;
+    // this warp's softmax rows: 8 of the block's 32 (m-tile cw/2, half cw%2), one per lane group
+    const int mt_s = cw >> 1, half = cw & 1;
+    const int rr = mt_s * 16 + half * 8 + g;
 
-        // Q^T fragments (B operand of S^T) for this warp's nine 16-dim k-steps, all heads
-        uint32_t bq[kSmKSteps][NT][2];
-        {
-            const __nv_bfloat16* qt = p.q + static_cast<int64_t>(t) * p.h * kDQK;
+    // segment cursor: token t, first list entry jb of the current block
+    const int kpad = p.nblk * kSmRows;
+    const int t_first = static_cast<int>(x0 / p.nblk);
+    int t = t_first;
+    int jb = static_cast<int>(x0 - static_cast<int64_t>(t) * p.nblk) * kSmRows;
+    bool seg_from_start = jb == 0;
+    uint32_t bq[kSmKSteps][NT][2];
+    load_q_frags<H>(p, t, cw, lane, bq);
+
+    for (int b = 0; b < nb; ++b) {
+        const int s = b % kSmStages;
+        const uint32_t stb = sKV + s * L::kStageBytes;
+        bool ok = true;
+        if (lane == 0)
+            ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / kSmStages) & 1, sAbort, &g_smla_error, kErrTimeout,
+                                kWaitLimitNs);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (!ok) failed = true;
+        // valid rows of this block, published by the producers before their arrival
+        const bool valid = (ptx::ld_shared_u32(sbase + L::kOffMask + 4u * s) >> rr) & 1u;
+
+        // ---- partial S^T over this warp's 144 dims, all 32 rows
+        float cs[2][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cs[mt][nt][e] = 0.f;
+        if (ok) {
 #pragma unroll
             for (int kk = 0; kk < kSmKSteps; ++kk) {
+                const int K = kSmKSteps * cw + kk;
+                const uint32_t kchunk = static_cast<uint32_t>((2 * K + (lj >> 1)) * 16);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const unsigned int* qr = reinterpret_cast<const unsigned int*>(
-                        qt + (nt * 8 + g) * kDQK + 16 * (kSmKSteps * cw + kk) + 2 * tq);
-                    bq[kk][nt][0] = __ldg(qr);
-                    bq[kk][nt][1] = __ldg(qr + 4);
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int row = mt * 16 + (lj & 1) * 8 + li;
+                    uint32_t a[4];
+                    mma16816::ldsm_x4(a, stb + row * kSmRowStride + kchunk);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816::mma(cs[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
                 }
             }
         }
-        // this warp's softmax rows: 8 of the block's 32 (m-tile cw/2, half cw%2), one per lane group
-        const int mt_s = cw >> 1, half = cw & 1;
-        const int rr = mt_s * 16 + half * 8 + g;
-        float lsum[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                sRedS[((cw * 2 + mt) * NT + nt) * 32 + lane] =
+                    make_float4(cs[mt][nt][0], cs[mt][nt][1], cs[mt][nt][2], cs[mt][nt][3]);
+        ptx::named_bar_sync(1, 128);
 
-        for (int b = 0; b < nb; ++b) {
-            const int s = b % kSmStages;
-            const uint32_t stb = sKV + s * L::kStageBytes;
-            bool ok = true;
-            if (lane == 0)
-                ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / kSmStages) & 1, sAbort, &g_smla_error, kErrTimeout,
-                                    kWaitLimitNs);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
-            if (!ok) failed = true;
-            // valid rows of this block, published by the producers before their arrival
-            const bool valid = (ptx::ld_shared_u32(sbase + L::kOffMask + 4u * s) >> rr) & 1u;
-
-            // ---- partial S^T over this warp's 144 dims, all 32 rows
-            float cs[2][NT][4];
+        // ---- logits of this warp's rows: sum of the four partials, scaled and masked
+        float x[NT][2];
+        bool need = false;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < NT; ++nt) {
+            float4 acc = sRedS[((0 * 2 + mt_s) * NT + nt) * 32 + lane];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) cs[mt][nt][e] = 0.f;
-            if (ok) {
-#pragma unroll
-                for (int kk = 0; kk < kSmKSteps; ++kk) {
-                    const int K = kSmKSteps * cw + kk;
-                    const uint32_t kchunk = static_cast<uint32_t>((2 * K + (lj >> 1)) * 16);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        const int row = mt * 16 + (lj & 1) * 8 + li;
-                        uint32_t a[4];
-                        mma16816::ldsm_x4(a, stb + row * kSmRowStride + kchunk);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma16816::mma(cs[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
-                    }
-                }
+            for (int w = 1; w < kSmComputeWarps; ++w) {
+                const float4 v = sRedS[((w * 2 + mt_s) * NT + nt) * 32 + lane];
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
             }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    sRedS[((cw * 2 + mt) * NT + nt) * 32 + lane] =
-                        make_float4(cs[mt][nt][0], cs[mt][nt][1], cs[mt][nt][2], cs[mt][nt][3]);
-            ptx::named_bar_sync(1, 128);
-
-            // ---- logits of this warp's rows: sum of the four partials, scaled and masked
-            float x[NT][2];
-            bool need = false;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float4 acc = sRedS[((0 * 2 + mt_s) * NT + nt) * 32 + lane];
-#pragma unroll
-                for (int w = 1; w < kSmComputeWarps; ++w) {
-                    const float4 v = sRedS[((w * 2 + mt_s) * NT + nt) * 32 + lane];
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-                }
-                const float s0 = half ? acc.z : acc.x;
-                const float s1 = half ? acc.w : acc.y;
-                x[nt][0] = valid ? s0 * c : -CUDART_INF_F;
-                x[nt][1] = valid ? s1 * c : -CUDART_INF_F;
-                need |= x[nt][0] > sM[nt * 8 + 2 * tq] + kRescaleLog2;
-                need |= x[nt][1] > sM[nt * 8 + 2 * tq + 1] + kRescaleLog2;
+            const float s0 = half ? acc.z : acc.x;
+            const float s1 = half ? acc.w : acc.y;
+            x[nt][0] = valid ? s0 * c : -CUDART_INF_F;
+            x[nt][1] = valid ? s1 * c : -CUDART_INF_F;
+            need |= x[nt][0] > sM[nt * 8 + 2 * tq] + kRescaleLog2;
+            need |= x[nt][1] > sM[nt * 8 + 2 * tq + 1] + kRescaleLog2;
+        }
+        // one warp-set barrier per block in the common case (no new max, no abort)
+        if (ptx::named_bar_red_or(1, 128, need || failed || *sAbort)) {
+            if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
+                failed = true;
+                break;
             }
-            // one warp-set barrier per block in the common case (no new max, no abort)
-            if (ptx::named_bar_red_or(1, 128, need || failed || *sAbort)) {
-                if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
-                    failed = true;
-                    break;
-                }
-                // the running max of some head grew: new max per head, rescale O and the sums
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float mx = x[nt][e];
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        if (lane < 4) sHr[cw * H + nt * 8 + 2 * lane + e] = mx;
-                    }
-                }
-                ptx::named_bar_sync(1, 128);
-                if (wtid < H) {
-                    const float mo = sM[wtid];
-                    float mb = sHr[wtid];
-#pragma unroll
-                    for (int w = 1; w < kSmComputeWarps; ++w) mb = fmaxf(mb, sHr[w * H + wtid]);
-                    const float mn = fmaxf(mo, mb);
-                    sAlpha[wtid] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(mo - mn);
-                    sM[wtid] = mn;
-                }
-                ptx::named_bar_sync(1, 128);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float a = sAlpha[nt * 8 + 2 * tq + e];
-                        lsum[nt][e] *= a;
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            o[mt][nt][e] *= a;
-                            o[mt][nt][2 + e] *= a;
-                        }
-                    }
-                }
-            }
-            // ---- P = 2^(x - m): fp32 partial sums, bf16 P^T[h][row] for the PV product
+            // the running max of some head grew: new max per head, rescale O and the sums
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int h = nt * 8 + 2 * tq + e;
-                    const float pr = (x[nt][e] == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x[nt][e] - sM[h]);
-                    lsum[nt][e] += pr;
-                    ptx::st_shared_u16(sP + h * L::kPStride + rr * 2, bf16_bits(pr));
+                    float mx = x[nt][e];
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    if (lane < 4) sHr[cw * H + nt * 8 + 2 * lane + e] = mx;
                 }
             }
             ptx::named_bar_sync(1, 128);
-
-            // ---- O^T[this warp's 128 dims, h] += V^T . P^T over the block's 32 rows
-            if (ok) {
+            if (wtid < H) {
+                const float mo = sM[wtid];
+                float mb = sHr[wtid];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    uint32_t bp[NT][2];
-                    if constexpr (NT == 1) {
-                        mma16816::ldsm_x2(bp[0][0], bp[0][1],
-                                          sP + li * L::kPStride + (16 * kk + 8 * (lj & 1)) * 2);
-                    } else {
-                        uint32_t r4[4];
-                        mma16816::ldsm_x4(r4, sP + ((lj >> 1) * 8 + li) * L::kPStride + (16 * kk + 8 * (lj & 1)) * 2);
-                        bp[0][0] = r4[0]; bp[0][1] = r4[1];
-                        bp[NT - 1][0] = r4[2]; bp[NT - 1][1] = r4[3];
-                    }
-                    const int krow = 16 * kk + (lj >> 1) * 8 + li;
+                for (int w = 1; w < kSmComputeWarps; ++w) mb = fmaxf(mb, sHr[w * H + wtid]);
+                const float mn = fmaxf(mo, mb);
+                sAlpha[wtid] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(mo - mn);
+                sM[wtid] = mn;
+            }
+            ptx::named_bar_sync(1, 128);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float a = sAlpha[nt * 8 + 2 * tq + e];
+                    lsum[nt][e] *= a;
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
-                        const int d0 = 128 * cw + 16 * mt;
-                        uint32_t a[4];
-                        mma16816::ldsm_x4_trans(a, stb + krow * kSmRowStride + (d0 / 8 + (lj & 1)) * 16);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma16816::mma(o[mt][nt], a, bp[nt][0], bp[nt][1]);
+                        o[mt][nt][e] *= a;
+                        o[mt][nt][2 + e] *= a;
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_empty0 + 8 * s);  // this warp is done with the stage
         }
+        // ---- P = 2^(x - m): fp32 partial sums, bf16 P^T[h][row] for the PV product
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = nt * 8 + 2 * tq + e;
+                const float pr = (x[nt][e] == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x[nt][e] - sM[h]);
+                lsum[nt][e] += pr;
+                ptx::st_shared_u16(sP + h * L::kPStride + rr * 2, bf16_bits(pr));
+            }
+        }
+        ptx::named_bar_sync(1, 128);
 
+        // ---- O^T[this warp's 128 dims, h] += V^T . P^T over the block's 32 rows
+        if (ok) {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t bp[NT][2];
+                if constexpr (NT == 1) {
+                    mma16816::ldsm_x2(bp[0][0], bp[0][1], sP + li * L::kPStride + (16 * kk + 8 * (lj & 1)) * 2);
+                } else {
+                    uint32_t r4[4];
+                    mma16816::ldsm_x4(r4, sP + ((lj >> 1) * 8 + li) * L::kPStride + (16 * kk + 8 * (lj & 1)) * 2);
+                    bp[0][0] = r4[0]; bp[0][1] = r4[1];
+                    bp[NT - 1][0] = r4[2]; bp[NT - 1][1] = r4[3];
+                }
+                const int krow = 16 * kk + (lj >> 1) * 8 + li;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int d0 = 128 * cw + 16 * mt;
+                    uint32_t a[4];
+                    mma16816::ldsm_x4_trans(a, stb + krow * kSmRowStride + (d0 / 8 + (lj & 1)) * 16);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816::mma(o[mt][nt], a, bp[nt][0], bp[nt][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_empty0 + 8 * s);  // this warp is done with the stage
+
+        const bool token_end = jb + kSmRows >= kpad;
+        if (!token_end && b + 1 < nb) {
+            jb += kSmRows;
+            continue;
+        }
+        // ================================================================ end of a token segment
         // ---- per-head totals L over the block rows of all four warps
-        const bool aborted = ptx::named_bar_red_or(1, 128, failed || *sAbort);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -502,17 +561,15 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
             float tot = 0.f;
 #pragma unroll
             for (int w = 0; w < kSmComputeWarps; ++w) tot += sHr[w * H + wtid];
-            if (aborted || nb == 0) tot = 0.f;
             sML[wtid] = sM[wtid];
             sML[H + wtid] = tot;
             sAlpha[wtid] = tot > 0.f ? 1.0f / tot : 0.f;
         }
         ptx::named_bar_sync(1, 128);
 
-        if (splits == 1 && !aborted) {
-            // O = O^T / L as bf16, staged as out[t] ([h][512], contiguous) in the free stage
-            // memory, then written with 16-byte stores
-            uint16_t* so = reinterpret_cast<uint16_t*>(smem + L::kOffKV);
+        if (seg_from_start && token_end) {
+            // ---- the whole list was here: O = O^T / L as bf16, staged as out[t] ([h][512])
+            uint16_t* so = reinterpret_cast<uint16_t*>(smem + L::kOffOut);
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const int d = 128 * cw + 16 * mt + g;
@@ -527,104 +584,160 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
             }
             ptx::named_bar_sync(1, 128);
             const uint4* src = reinterpret_cast<const uint4*>(so);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * p.h * kDV);
-            for (int v = wtid; v < p.h * (kDV / 8); v += 128) dst[v] = src[v];
-            if (wtid < p.h) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * H * kDV);
+            for (int v = wtid; v < H * (kDV / 8); v += 128) dst[v] = src[v];
+            if (wtid < H) {
                 const float tot = sML[H + wtid];
-                p.lse[static_cast<int64_t>(t) * p.h + wtid] =
+                p.lse[static_cast<int64_t>(t) * H + wtid] =
                     tot > 0.f ? (sML[wtid] + log2f(tot)) * 0.69314718055994531f : -CUDART_INF_F;
             }
-        }
-        if (splits > 1 && (failed || aborted)) sAbort[0] = 1;
-    }
-
-    __syncthreads();
-
-    if (splits > 1) {
-        // ================================================================ cluster merge
-        // CTA k of the cluster owns output dims [k*ds, (k+1)*ds).  Every CTA pushes its per-head
-        // (m, L) and its unnormalised partial O for each owner's dims into that owner's receive
-        // buffers; after one cluster barrier each owner weights the partials by 2^(m_j - M) / sum_j
-        // L_j 2^(m_j - M) and stores its dims.  No CTA reads another's memory after the barrier.
-        const int ds = kDV / splits;
-        ptx::cluster_wait();  // every CTA has started (pairs with the arrive at the top)
-        if (warp >= kProducerWarps) {
-            const int cw = warp - kProducerWarps;
-            const int wtid = threadIdx.x - kSmCompute0;
-            const int g = lane >> 2, tq = lane & 3;
-            const bool have = nb > 0 && *sAbort == 0;
-            const uint32_t recv = sbase + L::kOffRecv;
-            const uint32_t recv_ml = sbase + L::kOffRecvML;
+        } else {
+            // ---- part of a list cut between CTAs: leave (m, L, O^T) in this CTA's slot; the
+            // parts are merged after the grid barrier below
+            float* slot = p.part + (static_cast<int64_t>(blockIdx.x) * 2 + (t == t_first ? 0 : 1)) * L::kSlotFloats;
             if (wtid < H) {
-                const float m = have ? sML[wtid] : -CUDART_INF_F;
-                const float l = have ? sML[H + wtid] : 0.f;
-                for (int k = 0; k < splits; ++k) {
-                    ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + wtid) * 4, k), m);
-                    ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + H + wtid) * 4, k), l);
-                }
+                slot[wtid] = sML[wtid];
+                slot[H + wtid] = sML[H + wtid];
             }
+            float* so = slot + 2 * H;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
+                const int d = 128 * cw + 16 * mt + g;
 #pragma unroll
-                for (int hi = 0; hi < 2; ++hi) {
-                    const int d = 128 * cw + 16 * mt + g + 8 * hi;
-                    const int k = d / ds;
-                    const int dd = d - k * ds;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int h = nt * 8 + 2 * tq;
+                    so[h * kDV + d] = o[mt][nt][0];
+                    so[(h + 1) * kDV + d] = o[mt][nt][1];
+                    so[h * kDV + d + 8] = o[mt][nt][2];
+                    so[(h + 1) * kDV + d + 8] = o[mt][nt][3];
+                }
+            }
+        }
+        if (b + 1 == nb) break;
+        // ---- next token: fresh running state and its Q^T fragments
+        ptx::named_bar_sync(1, 128);  // every warp is done with sM / sML / sAlpha / the staging
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int h = nt * 8 + 2 * tq + e;
-                            const uint32_t la = recv + static_cast<uint32_t>(((rank * H + h) * ds + dd) * 4);
-                            ptx::st_shared_cluster_f32(ptx::map_shared_rank(la, k), have ? o[mt][nt][2 * hi + e] : 0.f);
-                        }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
+        if (wtid < H) sM[wtid] = -CUDART_INF_F;
+        ++t;
+        jb = 0;
+        seg_from_start = true;
+        load_q_frags<H>(p, t, cw, lane, bq);
+    }
+    if (failed) *sAbort = 1;  // producers still waiting for a free stage give up
+    if (p.part == nullptr) return;  // every list lay within one CTA
+
+    // ==================================================================== merge of cut lists
+    // Every CTA arrives once (also after an abort, so no CTA waits for ever); the launch is
+    // cooperative, so all CTAs are resident and the barrier cannot wait on an unscheduled CTA.
+    __threadfence();
+    ptx::named_bar_sync(1, 128);
+    if (wtid == 0) {
+        const bool ok = grid_barrier(p.gbar, static_cast<unsigned int>(p.grid));
+        if (!ok) *sAbort = 1;
+    }
+    ptx::named_bar_sync(1, 128);
+    if (*sAbort) return;
+    __threadfence();
+    // This CTA takes, for each cut list it holds a part of (its first and its last token), one
+    // slice of the 512 output dims: participant k of n takes dims [8 floor(64k/n), 8 floor(64(k+1)/n)).
+    const int t_last = static_cast<int>((x0 + nb - 1) / p.nblk);
+    float* mM = reinterpret_cast<float*>(smem + L::kOffMrg);
+    float* mL = mM + kMaxParts * H;
+    float* mW = mL + kMaxParts * H;
+    for (int tt = t_first; tt <= t_last; tt += (t_last > t_first ? t_last - t_first : 1)) {
+        const int64_t tok0 = static_cast<int64_t>(tt) * p.nblk;
+        const int64_t i_first = flat_owner(tok0, fq, fr);
+        const int64_t i_last = flat_owner(tok0 + p.nblk - 1, fq, fr);
+        if (i_first == i_last) continue;  // a whole list: already stored
+        const int n = static_cast<int>(i_last - i_first + 1);  // <= kMaxParts (host plan)
+        const int k = static_cast<int>(blockIdx.x - i_first);
+        auto slot_of = [&](int64_t j) -> const float* {
+            const int64_t tj = flat_begin(j, fq, fr) / p.nblk;  // first token of CTA j
+            return p.part + (j * 2 + (tt == tj ? 0 : 1)) * L::kSlotFloats;
+        };
+        // items of this CTA's slice: (head, 8 dims); the parts are summed in CTA order, four at
+        // a time.  The loads of the first four parts of this thread's first item are issued
+        // before the weights are known, so a cut list held by at most four CTAs costs one
+        // round trip to L2.
+        const int c0 = (64 * k) / n, c1 = (64 * (k + 1)) / n;
+        const int items = H * (c1 - c0);
+        auto load_group = [&](int it, int j0, float4 (&v)[4][2]) {
+            const int hh = it / (c1 - c0);
+            const int dd = (c0 + it % (c1 - c0)) * 8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = j0 + u < n;
+                const float* oj = slot_of(i_first + (in ? j0 + u : 0)) + 2 * H + hh * kDV + dd;
+                v[u][0] = in ? __ldcg(reinterpret_cast<const float4*>(oj)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[u][1] = in ? __ldcg(reinterpret_cast<const float4*>(oj + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        float4 pre[4][2];
+        if (wtid < items) load_group(wtid, 0, pre);
+        ptx::named_bar_sync(1, 128);  // the previous list's weights are no longer read
+        for (int e = wtid; e < n * H; e += 128) {
+            const float* sj = slot_of(i_first + e / H);
+            mM[e] = __ldcg(sj + e % H);
+            mL[e] = __ldcg(sj + H + e % H);
+        }
+        ptx::named_bar_sync(1, 128);
+        if (wtid < H) {
+            float M = -CUDART_INF_F;
+            for (int j = 0; j < n; ++j) M = fmaxf(M, mM[j * H + wtid]);
+            float Lt = 0.f;
+            for (int j = 0; j < n; ++j) {
+                const float mj = mM[j * H + wtid], lj = mL[j * H + wtid];
+                if (mj != -CUDART_INF_F && lj > 0.f) Lt += lj * ptx::ex2_approx(mj - M);
+            }
+            const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
+            for (int j = 0; j < n; ++j) {
+                const float mj = mM[j * H + wtid], lj = mL[j * H + wtid];
+                mW[j * H + wtid] = (mj != -CUDART_INF_F && lj > 0.f) ? ptx::ex2_approx(mj - M) * inv : 0.f;
+            }
+            if (k == 0)
+                p.lse[static_cast<int64_t>(tt) * H + wtid] =
+                    Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
+        }
+        ptx::named_bar_sync(1, 128);
+        for (int it = wtid; it < items; it += 128) {
+            const int hh = it / (c1 - c0);
+            const int dd = (c0 + it % (c1 - c0)) * 8;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j0 = 0; j0 < n; j0 += 4) {
+                float4 v[4][2];
+                if (it == wtid && j0 == 0) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[u][0] = pre[u][0];
+                        v[u][1] = pre[u][1];
                     }
+                } else {
+                    load_group(it, j0, v);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float w = j0 + u < n ? mW[(j0 + u) * H + hh] : 0.f;
+                    acc[0] += w * v[u][0].x; acc[1] += w * v[u][0].y;
+                    acc[2] += w * v[u][0].z; acc[3] += w * v[u][0].w;
+                    acc[4] += w * v[u][1].x; acc[5] += w * v[u][1].y;
+                    acc[6] += w * v[u][1].z; acc[7] += w * v[u][1].w;
                 }
             }
+            uint4 packed;
+            packed.x = pack_bf16x2(acc[0], acc[1]);
+            packed.y = pack_bf16x2(acc[2], acc[3]);
+            packed.z = pack_bf16x2(acc[4], acc[5]);
+            packed.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(tt) * H + hh) * kDV + dd) = packed;
         }
-        ptx::cluster_sync();  // all pushes are visible to their owners
-        if (warp >= kProducerWarps) {
-            const int wtid = threadIdx.x - kSmCompute0;
-            const float* rml = reinterpret_cast<const float*>(smem + L::kOffRecvML);
-            const float* rcv = reinterpret_cast<const float*>(smem + L::kOffRecv);
-            if (wtid < H) {
-                float M = -CUDART_INF_F;
-                for (int j = 0; j < splits; ++j) M = fmaxf(M, rml[j * 2 * H + wtid]);
-                float Lt = 0.f;
-                for (int j = 0; j < splits; ++j) {
-                    const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
-                    if (mj != -CUDART_INF_F && lj > 0.f) Lt += lj * ptx::ex2_approx(mj - M);
-                }
-                for (int j = 0; j < splits; ++j) {
-                    const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
-                    sHr[j * H + wtid] = (Lt > 0.f && mj != -CUDART_INF_F && lj > 0.f) ? ptx::ex2_approx(mj - M) / Lt : 0.f;
-                }
-                if (rank == 0 && wtid < p.h)
-                    p.lse[static_cast<int64_t>(t) * p.h + wtid] =
-                        Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
-            }
-            ptx::named_bar_sync(1, 128);
-            // eight dims of one head per item, stored as one 16-byte vector
-            const int per_head = ds / 8;
-            for (int it = wtid; it < p.h * per_head; it += 128) {
-                const int hh = it / per_head;
-                const int dd = (it % per_head) * 8;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int j = 0; j < splits; ++j) {
-                    const float w = sHr[j * H + hh];
-                    const float4 lo = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd);
-                    const float4 hv = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd + 4);
-                    acc[0] += w * lo.x; acc[1] += w * lo.y; acc[2] += w * lo.z; acc[3] += w * lo.w;
-                    acc[4] += w * hv.x; acc[5] += w * hv.y; acc[6] += w * hv.z; acc[7] += w * hv.w;
-                }
-                uint4 packed;
-                packed.x = pack_bf16x2(acc[0], acc[1]);
-                packed.y = pack_bf16x2(acc[2], acc[3]);
-                packed.z = pack_bf16x2(acc[4], acc[5]);
-                packed.w = pack_bf16x2(acc[6], acc[7]);
-                *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.h + hh) * kDV + rank * ds + dd) = packed;
-            }
-        }
+        if (t_last == t_first) break;
     }
 }
 
