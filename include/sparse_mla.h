@@ -28,8 +28,13 @@
  *   Summary: the index lists are fixed-width int32.
  *
  * Conventions for every entry point below:
- *   - Device pointers belong to the caller; the library allocates no device or
- *     host memory per call and keeps no per-call state.
+ *   - Device pointers belong to the caller.  The library allocates nothing per
+ *     call.  With 8 or 16 heads, a launch that cuts token lists between CTAs
+ *     (see sparse_mla_fwd_ex) merges the parts through a scratch buffer: one per
+ *     (device, stream), allocated at the first call on that stream that needs it
+ *     (or a larger one), cleared once, and reused.  Calls on one stream are
+ *     ordered and share it; a stream capture needs one uncaptured call of the
+ *     same size on that stream first (otherwise SMLA_ERR_INVALID_ARG).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).
  *   - A non-OK return means nothing was launched.  Device-side failures (a
@@ -91,16 +96,43 @@ smla_status sparse_mla_fwd(const void* q, const void* kv_cache, const int32_t* i
 
 /*
  * sparse_mla_fwd_ex -- sparse_mla_fwd with an explicit split count.
- * splits = 0 lets the library choose (what sparse_mla_fwd does).  splits in
- * {1, 2, 4, 8} splits each token's list over that many CTAs of one thread-block
- * cluster, merged on chip by log-sum-exp weights; other values are
- * SMLA_ERR_INVALID_ARG.  Results agree with any other split count up to fp32
- * rounding.
+ * splits = 0 lets the library choose (what sparse_mla_fwd does); other values
+ * than 0, 1, 2, 4, 8 are SMLA_ERR_INVALID_ARG.
+ *   h = 32, 64: each token's list is split over `splits` CTAs of one
+ *     thread-block cluster and merged on chip by log-sum-exp weights.
+ *   h = 8, 16: the T x ceil(topk/32) row blocks are cut into T * splits equal
+ *     contiguous ranges, one per CTA (at most one per SM when a list is cut),
+ *     wherever the cuts fall; the parts of a cut list are merged through the
+ *     scratch after a grid-wide barrier (cooperative launch), in CTA order.
+ * Results agree with any other split count up to fp32 rounding, and repeated
+ * calls with the same arguments give identical bytes.
  */
 smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t* indices,
                               int32_t T, int32_t h, int32_t topk, int64_t num_slots,
                               int32_t kv_format, float scale, void* out, float* lse,
                               int32_t splits, void* stream);
+
+/*
+ * sparse_mla_fwd_noalloc -- sparse_mla_fwd_ex with the merge scratch taken from
+ * a fixed array inside the library (file scope, about 10 MiB per device,
+ * enough for 16 heads on up to 160 CTAs) instead of a per-stream buffer, so it
+ * never allocates device memory.  The pages describe no counterpart; it exists
+ * for callers that must not allocate at all (e.g. under a memory pool).
+ *   - The array's address is looked up, and its barrier words cleared, at the
+ *     first call on each device; that call synchronises the device and must
+ *     not be inside a stream capture (SMLA_ERR_INVALID_ARG).  Later calls,
+ *     captured or not, only launch.
+ *   - Every call on a device uses the same array: calls that may overlap in
+ *     time (different streams without ordering) race on it and must not be
+ *     issued.  Launches that cut no list do not touch it.
+ *   - A launch that would need more scratch than the array holds returns
+ *     SMLA_ERR_UNSUPPORTED and launches nothing.
+ * Arguments, results and errors are otherwise those of sparse_mla_fwd_ex.
+ */
+smla_status sparse_mla_fwd_noalloc(const void* q, const void* kv_cache, const int32_t* indices,
+                                   int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                                   int32_t kv_format, float scale, void* out, float* lse,
+                                   int32_t splits, void* stream);
 
 /*
  * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the
@@ -123,8 +155,10 @@ smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_cache,
 /*
  * sparse_mla_sync_status -- synchronise `stream`, then read and clear the
  * device error word of the current device.  Returns SMLA_ERR_TIMEOUT if a
- * kernel gave up on a bounded wait since the last call, SMLA_ERR_CUDA if the
- * synchronisation failed, SMLA_OK otherwise.  Not for the hot path.
+ * kernel gave up on a bounded wait since the last call (the device is then
+ * synchronised and the barrier words of every merge scratch on it cleared),
+ * SMLA_ERR_CUDA if the synchronisation failed, SMLA_OK otherwise.  Not for the
+ * hot path.
  */
 smla_status sparse_mla_sync_status(void* stream);
 

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     library,
     sparse_mla_fwd,
     sparse_mla_fwd_host,
+    sparse_mla_fwd_noalloc,
     sync_status,
     version,
 )
@@ -34,6 +35,7 @@ __all__ = [
     "library",
     "sparse_mla_fwd",
     "sparse_mla_fwd_host",
+    "sparse_mla_fwd_noalloc",
     "sync_status",
     "version",
 ]

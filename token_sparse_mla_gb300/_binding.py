@@ -45,6 +45,8 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp]
     lib.sparse_mla_fwd_ex.restype = ctypes.c_int
     lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_fwd_noalloc.restype = ctypes.c_int
+    lib.sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_host_workspace_bytes.restype = sz
     lib.sparse_mla_host_workspace_bytes.argtypes = [i32, i32, i32]
     lib.sparse_mla_fwd_host.restype = ctypes.c_int
@@ -132,6 +134,27 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
         _stream_handle(stream))
     _check(st)
     return out, lse
+
+
+def sparse_mla_fwd_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                           scale: Optional[float] = None, *, out: torch.Tensor, lse: torch.Tensor,
+                           kv_format: str = "bf16", splits: int = 0, stream=None) -> None:
+    """sparse_mla_fwd with the library's static merge scratch: nothing is allocated, so out and
+    lse are required (see include/sparse_mla.h for the rules on first call and streams)."""
+    T, h, topk, num_slots = _dims(q, kv_cache, indices, kv_format)
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices), ("out", out), ("lse", lse)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if scale is None:
+        scale = D_QK ** -0.5
+    if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
+    if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
+    _check(library().sparse_mla_fwd_noalloc(
+        q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
+        KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
+        _stream_handle(stream)))
 
 
 def host_workspace_bytes(T: int, h: int, topk: int) -> int:

@@ -43,6 +43,9 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_error = cudaSuccess;
     int num_sms = 0;
+    // the static merge scratch of sparse_mla_fwd_noalloc on this device (set once, under
+    // g_static_mu)
+    void* static_ptr = nullptr;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -138,6 +141,12 @@ constexpr size_t kScratchHead = 256;
 size_t small_scratch_bytes(int64_t grid, int h) {
     return kScratchHead + static_cast<size_t>(grid) * 2 * (2 * h + h * smla::kDV) * 4;
 }
+
+// File-scope merge scratch of sparse_mla_fwd_noalloc: sized for 16 heads on up to 160 CTAs (a
+// launch that cuts lists never has more CTAs than SMs).  Zero-initialised when the module loads;
+// its head (the grid-barrier words) is cleared once more per device at first use.
+constexpr size_t kStaticScratchBytes = kScratchHead + static_cast<size_t>(160) * 2 * (2 * 16 + 16 * smla::kDV) * 4;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
                        int32_t topk, int64_t num_slots, int32_t kv_format, float scale,
@@ -259,9 +268,36 @@ smla_status stream_scratch(int dev, cudaStream_t stream, size_t need, void** ptr
     return SMLA_OK;
 }
 
+// The device address of the static scratch, looked up (and its head cleared) once per device.
+// That first call must not be inside a stream capture (it synchronises the device).
+std::mutex g_static_mu;
+
+smla_status static_scratch(DeviceState* ds, cudaStream_t stream, void** ptr) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!ds->static_ptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(SMLA_ERR_INVALID_ARG,
+                        "the first sparse_mla_fwd_noalloc call on a device must not be captured");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e == cudaSuccess) e = cudaMemset(p, 0, kScratchHead);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "setting up the static merge scratch");
+        ds->static_ptr = p;
+    }
+    *ptr = ds->static_ptr;
+    return SMLA_OK;
+}
+
+enum class ScratchSource { kStream, kStatic };
+
 smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
                    int32_t topk, int64_t num_slots, int32_t kv_format, float scale, void* out,
-                   float* lse, int32_t splits, cudaStream_t stream) {
+                   float* lse, int32_t splits, cudaStream_t stream,
+                   ScratchSource source = ScratchSource::kStream) {
     smla_status st = check_args(q, kv, idx, T, h, topk, num_slots, kv_format, scale, out, lse, splits);
     if (st != SMLA_OK || T == 0) return st;
     int dev = 0;
@@ -303,7 +339,14 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     prm.gbar = nullptr;
     if (pl.scratch > 0) {
         void* sp = nullptr;
-        if ((st = stream_scratch(dev, stream, pl.scratch, &sp)) != SMLA_OK) return st;
+        if (source == ScratchSource::kStatic) {
+            if (pl.scratch > kStaticScratchBytes)
+                return fail(SMLA_ERR_UNSUPPORTED, "this launch needs %zu bytes of merge scratch; the static scratch has %zu",
+                            pl.scratch, kStaticScratchBytes);
+            if ((st = static_scratch(ds, stream, &sp)) != SMLA_OK) return st;
+        } else if ((st = stream_scratch(dev, stream, pl.scratch, &sp)) != SMLA_OK) {
+            return st;
+        }
         prm.gbar = static_cast<unsigned int*>(sp);
         prm.part = reinterpret_cast<float*>(static_cast<char*>(sp) + kScratchHead);
     }
@@ -363,6 +406,14 @@ smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t
                               void* stream) {
     return launch(q, kv_cache, indices, T, h, topk, num_slots, kv_format, scale, out, lse, splits,
                   static_cast<cudaStream_t>(stream));
+}
+
+smla_status sparse_mla_fwd_noalloc(const void* q, const void* kv_cache, const int32_t* indices,
+                                   int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                                   int32_t kv_format, float scale, void* out, float* lse,
+                                   int32_t splits, void* stream) {
+    return launch(q, kv_cache, indices, T, h, topk, num_slots, kv_format, scale, out, lse, splits,
+                  static_cast<cudaStream_t>(stream), ScratchSource::kStatic);
 }
 
 size_t sparse_mla_host_workspace_bytes(int32_t T, int32_t h, int32_t topk) {
@@ -428,6 +479,9 @@ smla_status sparse_mla_sync_status(void* stream) {
                 std::lock_guard<std::mutex> lock(g_scratch_mu);
                 for (Scratch& x : g_scratch)
                     if (x.dev == dev && x.ptr) cudaMemset(x.ptr, 0, kScratchHead);
+                std::lock_guard<std::mutex> lock2(g_static_mu);
+                if (dev >= 0 && dev < kMaxDevices && g_dev[dev].static_ptr)
+                    cudaMemset(g_dev[dev].static_ptr, 0, kScratchHead);
             }
             return fail(SMLA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (error word 0x%x)", word);
         }
