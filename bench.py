@@ -213,7 +213,9 @@ def run_reference(args, rank, world):
 
 def workload_config(w, args, splits, rot, ctas=None):
     cfg = w.cfg
+    launch = getattr(args, "launch", "eager")
     return {"workload": cfg.name, "T": w.T, "h": int(w.q.shape[1]), "h_real": w.h,
+            "launch": "CUDA graph of consecutive steps" if launch == "graph" else "eager launches",
             "padded_to_64": bool(args.pad), "topk": w.topk, "kv_format": cfg.kv_format,
             "num_slots": w.num_slots, "block_size": 64, "splits": splits, "ctas": ctas,
             "l2": f"rotating {rot} independently drawn input sets (cache, indices, q); "
@@ -242,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
     outs = [torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev) for _ in sets]
     lses = [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in sets]
     gbytes = [gathered_bytes(w.indices, w.num_slots, cfg.row_bytes) for w in sets]
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)  # a side stream: CUDA graphs cannot capture the default one
     info = smla.launch_info(T, H, topk, cfg.kv_format)
 
     def step(i):
@@ -250,30 +252,59 @@ def run_ours(args, rank, world, local_rank):
         smla.sparse_mla_fwd(qs[k], kvs[k], ids[k], sets[k].scale, out=outs[k], lse=lses[k],
                             kv_format=cfg.kv_format, stream=stream)
 
+    # CUDA graphs of consecutive steps (the launch path a serving loop uses): one of `glen`
+    # steps replayed K // glen times, and one of the K % glen remaining steps
+    graphs = []
+
+    def capture(n_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                step(i)
+        return g
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for i in range(args.warmup):
-        step(i)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
     smla.sync_status(stream)
+    glen = rot * max(1, 32 // rot)
+    if args.launch == "graph":
+        graphs = [capture(glen), capture(args.steps % glen) if args.steps % glen else None]
+        for _ in range(2):
+            graphs[0].replay()
+        torch.cuda.synchronize(dev)
+
+    def timed_steps(k_steps):
+        if args.launch == "graph":
+            for _ in range(k_steps // glen):
+                graphs[0].replay()
+            if k_steps % glen:
+                graphs[1].replay()
+        else:
+            for i in range(k_steps):
+                step(i)
     clocks = ClockSampler(local_rank)
     clocks.start()
     # keep the GPU busy (0.3 s by default) before the timed region so the clock samples see load
     t_pre = time.time()
     i = 0
     while time.time() - t_pre < args.prerun:
-        step(i)
+        with torch.cuda.stream(stream):
+            timed_steps(glen)
         i += 1
-        if i % 256 == 0:
+        if i % 8 == 0:
             torch.cuda.synchronize(dev)
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    with torch.cuda.stream(stream):
+        timed_steps(args.steps)
     ev1.record(stream)
     barrier()
     t_dev = ev0.elapsed_time(ev1) / 1e3
@@ -371,6 +402,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
+                    help="replay the timed steps from CUDA graphs, or launch each step eagerly")
     ap.add_argument("--prerun", type=float, default=0.3,
                     help="seconds of untimed steps before the timed region (clock samples)")
     args = ap.parse_args()
