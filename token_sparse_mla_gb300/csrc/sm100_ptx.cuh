@@ -51,6 +51,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after `limit_ns` nanoseconds; on a
 // timeout it sets *abort and ORs `err_code` into *err so that the host sees it.
@@ -259,6 +271,14 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "r"((r)[6]), "r"((r)[7]), "r"((r)[8]), "r"((r)[9]), "r"((r)[10]), "r"((r)[11]),          \
         "r"((r)[12]), "r"((r)[13]), "r"((r)[14]), "r"((r)[15])                                    \
         : "memory")
+
+// 16 TMEM lanes x 256 bits: thread (g = lane/4, q = lane%4) receives columns 2q, 2q+1 of
+// lanes g and g+8 of the warp's quadrant (the layout of an m16n8 mma accumulator).
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

@@ -21,12 +21,13 @@
 //               V^T is read from the SAME shared-memory tile as K, as an MN-major
 //               operand.
 //   warps 1-7   producers: cp.async gather of 64 rows per stage, 2 stages.
-//   warps 8-11  softmax warpgroup: reads S^T from TMEM (one KV row per thread, all
-//               heads), masks invalid entries, keeps a running max per head in
-//               log2 units and only rescales O when that max grows by more than
-//               2^8, writes P^T (bf16) to shared memory, runs the epilogue.  Each
-//               row thread keeps its fp32 partial softmax sums (one per head) in
-//               its own TMEM lane, which keeps them out of the register file.
+//   warps 8-11  softmax warpgroup: reads S^T from TMEM (16x256b loads: two KV rows and
+//               a quarter of the heads per thread, all 32 lanes busy), masks invalid
+//               entries, keeps a running max per head in log2 units and only rescales
+//               O when that max grows by more than 2^8, keeps fp32 partial softmax sums
+//               in registers, writes P^T (bf16) to shared memory, runs the epilogue.
+//   The MMA thread issues PV(b) and S^T(b+1) in whichever order their inputs arrive, so
+//   the softmax of one block overlaps the MMAs of its neighbours.
 //
 // HP is the MMA N size: the head count rounded up to 16 (h = 8 runs N = 16 with
 // the upper 8 query rows zero in shared memory; nothing is padded in HBM).
@@ -59,12 +60,10 @@ struct Layout {
     static constexpr int kNumBars = 12;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kOffMisc + 16;
-    // TMEM columns: O^T [0,4HP) | per-lane partial sums Lp [4HP,5HP) | S^T x2 [5HP,7HP)
-    static constexpr int kColL = 4 * HP;
-    static constexpr int kColS = 5 * HP;
-    static constexpr int kTmemCols = (7 * HP <= 128) ? 128 : ((7 * HP <= 256) ? 256 : 512);
-    static constexpr bool kSumsInTmem = HP == 64;  // softmax partial sums: TMEM at 64 heads
-    static_assert(7 * HP <= kTmemCols, "TMEM budget");
+    // TMEM columns: O^T [0,4HP) | S^T x2 [4HP,6HP)
+    static constexpr int kColS = 4 * HP;
+    static constexpr int kTmemCols = (6 * HP <= 128) ? 128 : ((6 * HP <= 256) ? 256 : 512);
+    static_assert(6 * HP <= kTmemCols, "TMEM budget");
     static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(HP * kDV * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
@@ -164,19 +163,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *sTmem;
-    if (warp > kProducerWarps) {
-        // partial softmax sums start at zero in every lane of this warp's quadrant
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        uint32_t zeros[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) zeros[e] = 0u;
-#pragma unroll
-        for (int c = 0; c < HP; c += 16) SMLA_TMEM_ST16(tmem + lane_base + L::kColL + c, zeros);
-        ptx::tmem_wait_st();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
 
     if (warp == 0) {
         // ================================================================ MMA issuer
@@ -215,12 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_s(0);
                 }
             }
-            // PV(b) is issued before waiting for block b+1's rows, so the stage of block b
-            // is released (and refilled with block b+2) while block b+1 is still landing.
-            for (int b = 0; ok && b < nb; ++b) {
-                ok = wait(kBarPFull, b & 1);
-                if (!ok) break;
-                ptx::tc_fence_after();
+            // Each iteration issues PV(b) and S^T(b+1), in whichever order their inputs arrive
+            // (P^T of block b from the softmax, rows of block b+1 from the producers): neither
+            // waits behind the other, so the softmax of one block overlaps its neighbours' MMAs.
+            auto issue_pv = [&](int b) {
                 const int s = b & 1;
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * kStageBytes) >> 4);
 #pragma unroll
@@ -233,10 +217,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
-                if (b + 1 < nb) {
-                    const int s1 = (b + 1) & 1;
-                    ok = wait(kBarKvFull + s1, ((b + 1) >> 1) & 1);
-                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, (((b + 1) >> 1) - 1) & 1);
+            };
+            for (int b = 0; ok && b < nb; ++b) {
+                const int s1 = (b + 1) & 1;
+                const uint32_t kv_par = ((b + 1) >> 1) & 1, se_par = (((b + 1) >> 1) - 1) & 1;
+                bool s_pending = b + 1 < nb;
+                bool pv_pending = true;
+                const uint64_t t0 = ptx::globaltimer_ns();
+                for (uint32_t it = 0; pv_pending; ++it) {
+                    if (s_pending && ptx::mbar_test_wait(bar(kBarKvFull + s1), kv_par) &&
+                        (b + 1 < 2 || ptx::mbar_test_wait(bar(kBarSEmpty + s1), se_par))) {
+                        ptx::tc_fence_after();
+                        issue_s(b + 1);
+                        s_pending = false;
+                    }
+                    if (ptx::mbar_test_wait(bar(kBarPFull), b & 1)) {
+                        ptx::tc_fence_after();
+                        issue_pv(b);
+                        pv_pending = false;
+                    } else if ((it & 15u) == 15u) {
+                        if (*sAbort) {
+                            ok = false;
+                            break;
+                        }
+                        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                            *sAbort = 1;
+                            atomicOr(&g_smla_error, kErrTimeout);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (ok && s_pending) {
+                    ok = wait(kBarKvFull + s1, kv_par);
+                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, se_par);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_s(b + 1);
@@ -253,55 +267,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          bar(kBarKvEmpty), sAbort);
     } else {
         // ================================================================ softmax warpgroup
+        // Warp `quad` owns block rows quad*16 .. quad*16+15 (M=64 accumulator: TMEM lanes
+        // 32*quad + 0..15).  The 16x256b TMEM load hands thread (g = lane/4, tq = lane%4) rows
+        // g and g+8 of them and, in each 8-column group i, heads 8i + 2tq and 8i + 2tq + 1 (the
+        // mma accumulator layout), so all 32 lanes work.
         const int wtid = threadIdx.x - kSoftmaxThread0;
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const int r = quad * 16 + lane;  // KV row within the block (M=64 layout: lanes 0-15)
-        const bool row_lane = lane < 16;
+        const int g = lane >> 2, tq = lane & 3;
+        const int r0 = quad * 16 + g, r1 = r0 + 8;
+        constexpr int NG = HP / 8;
         const float c = p.sm_scale_log2;
         bool failed = false;
-        // raw list entry of this lane's row for the next block (checked when it is used)
-        int raw_next = fetch_entry(idx_row, j0 + r, j1, row_lane && nb > 0);
-        // P^T[h][r] sits at pbase[h & 7] + (h >> 3) * 1024 (128B-swizzled K-major rows of 64 bf16)
-        uint32_t pbase[8];
+        // raw list entries of this thread's two rows for the next block (checked when used)
+        int raw0 = fetch_entry(idx_row, j0 + r0, j1, nb > 0);
+        int raw1 = fetch_entry(idx_row, j0 + r1, j1, nb > 0);
+        // P^T[h][r] (128B-swizzled K-major rows of 64 bf16, eight heads per 1 KB atom)
+        auto p_addr = [&](int h, int r) -> uint32_t {
+            return sP + (h >> 3) * 1024 + (h & 7) * 128 + ((((r >> 3) ^ (h & 7)) << 4) | ((r & 7) << 1));
+        };
+        // fp32 partial softmax sums of this thread's heads 8i + 2tq + e over its two rows
+        float lsum[NG][2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            pbase[k] = sP + k * 128 + ((((r >> 3) ^ k) << 4) | ((r & 7) << 1));
-        // fp32 partial softmax sums of this row lane, per head: registers up to 32 heads,
-        // this lane's TMEM columns [4HP, 5HP) at 64 heads
-        float lreg[L::kSumsInTmem ? 1 : HP];
-#pragma unroll
-        for (int h = 0; h < (L::kSumsInTmem ? 1 : HP); ++h) lreg[h] = 0.f;
+        for (int i = 0; i < NG; ++i) lsum[i][0] = lsum[i][1] = 0.f;
 
         for (int b = 0; b < nb; ++b) {
             const int s = b & 1;
-            const bool valid = valid_slot(raw_next, p.num_slots) >= 0;
-            raw_next = fetch_entry(idx_row, j0 + (b + 1) * kRows + r, j1, row_lane && b + 1 < nb);
+            const bool v0 = valid_slot(raw0, p.num_slots) >= 0;
+            const bool v1 = valid_slot(raw1, p.num_slots) >= 0;
+            raw0 = fetch_entry(idx_row, j0 + (b + 1) * kRows + r0, j1, b + 1 < nb);
+            raw1 = fetch_entry(idx_row, j0 + (b + 1) * kRows + r1, j1, b + 1 < nb);
             bool ok = true;
             if (lane == 0) ok = wait(kBarSFull + s, (b >> 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();
-            uint32_t sv[HP];
+            // sv[i] = {row g: head 8i+2tq, 8i+2tq+1 | row g+8: same heads}, as scaled logits
+            uint32_t sv[NG][4];
             bool need = false;
             if (ok) {
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < HP / 16; ++cc)
-                    SMLA_TMEM_LD16(tmem + lane_base + L::kColS + s * HP + cc * 16, &sv[cc * 16]);
+                for (int i = 0; i < NG; ++i) ptx::tmem_ld_16x256b(tmem + lane_base + L::kColS + s * HP + 8 * i, sv[i]);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + s));
 #pragma unroll
-                for (int h = 0; h < HP; ++h) {
-                    const float x = valid ? __uint_as_float(sv[h]) * c : -CUDART_INF_F;
-                    sv[h] = __float_as_uint(x);
-                    need |= x > sM[h] + kRescaleLog2;
+                for (int i = 0; i < NG; ++i) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float mo = sM[8 * i + 2 * tq + e] + kRescaleLog2;
+                        const float x0 = v0 ? __uint_as_float(sv[i][e]) * c : -CUDART_INF_F;
+                        const float x1 = v1 ? __uint_as_float(sv[i][2 + e]) * c : -CUDART_INF_F;
+                        sv[i][e] = __float_as_uint(x0);
+                        sv[i][2 + e] = __float_as_uint(x1);
+                        need |= (x0 > mo) || (x1 > mo);
+                    }
                 }
             } else {
                 failed = true;
 #pragma unroll
-                for (int h = 0; h < HP; ++h) sv[h] = __float_as_uint(-CUDART_INF_F);
+                for (int i = 0; i < NG; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sv[i][e] = __float_as_uint(-CUDART_INF_F);
             }
             bool pv_waited = false;
             // one warpgroup barrier per block in the common case (no new max, no abort)
@@ -312,9 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // the running max of some head grew: new max, rescale O and the partial sums
 #pragma unroll
-                for (int h = 0; h < HP; ++h) {
-                    const float v = ptx::warp_max_f32(__uint_as_float(sv[h]));
-                    if (lane == 0) sRed[quad * HP + h] = v;
+                for (int i = 0; i < NG; ++i) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float mx = fmaxf(__uint_as_float(sv[i][e]), __uint_as_float(sv[i][2 + e]));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        if (g == 0) sRed[quad * HP + 8 * i + 2 * tq + e] = mx;
+                    }
                 }
                 ptx::named_bar_sync(1, 128);
                 if (wtid < HP) {
@@ -326,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sM[wtid] = mn;
                 }
                 ptx::named_bar_sync(1, 128);
-                if constexpr (!L::kSumsInTmem) {
 #pragma unroll
-                    for (int h = 0; h < HP; ++h) lreg[h] *= sAlpha[h];
+                for (int i = 0; i < NG; ++i) {
+                    lsum[i][0] *= sAlpha[8 * i + 2 * tq];
+                    lsum[i][1] *= sAlpha[8 * i + 2 * tq + 1];
                 }
                 if (b > 0) {
                     bool okw = true;
@@ -338,16 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pv_waited = true;
                     if (okw) {
                         ptx::tc_fence_after();
-                        constexpr int kScaledBlocks = L::kSumsInTmem ? 5 : 4;  // O^T blocks (+ sums)
 #pragma unroll 1
                         for (int cc = 0; cc < HP / 16; ++cc) {
                             float a[16];
 #pragma unroll
                             for (int e = 0; e < 16; ++e) a[e] = sAlpha[cc * 16 + e];
 #pragma unroll 1
-                            for (int i = 0; i < kScaledBlocks; ++i) {
+                            for (int blk = 0; blk < 4; ++blk) {  // the four O^T column blocks
                                 uint32_t o[16];
-                                const uint32_t ta = tmem + lane_base + i * HP + cc * 16;
+                                const uint32_t ta = tmem + lane_base + blk * HP + cc * 16;
                                 SMLA_TMEM_LD16(ta, o);
                                 ptx::tmem_wait_ld();
 #pragma unroll
@@ -362,39 +396,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (b > 0 && !pv_waited) {  // P^T has one buffer: the previous PV must be done
+            // P = 2^(x - m) for this thread's 2 rows x 2*NG heads; exponentials before the wait
+            // for the previous PV (the single P^T buffer is still being read until then)
+            uint16_t pb[NG][4];
+#pragma unroll
+            for (int i = 0; i < NG; ++i) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float m = sM[8 * i + 2 * tq + e];
+                    const float x0 = __uint_as_float(sv[i][e]), x1 = __uint_as_float(sv[i][2 + e]);
+                    const float p0 = (x0 == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x0 - m);
+                    const float p1 = (x1 == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x1 - m);
+                    lsum[i][e] += p0 + p1;
+                    pb[i][e] = bf16_bits(p0);
+                    pb[i][2 + e] = bf16_bits(p1);
+                }
+            }
+            if (b > 0 && !pv_waited) {
                 bool okw = true;
                 if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) failed = true;
                 __syncwarp();
             }
-            // P = 2^(x - m), written transposed (P^T[h][row]) in the 128B-swizzled K-major layout,
-            // and added in fp32 to this lane's partial sums
-            if constexpr (L::kSumsInTmem) {
 #pragma unroll
-                for (int cc = 0; cc < HP / 16; ++cc) {
-                    uint32_t lp[16];
-                    const uint32_t ta = tmem + lane_base + L::kColL + cc * 16;
-                    SMLA_TMEM_LD16(ta, lp);
-                    ptx::tmem_wait_ld();
+            for (int i = 0; i < NG; ++i) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int h = cc * 16 + e;
-                        const float x = __uint_as_float(sv[h]);
-                        const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
-                        lp[e] = __float_as_uint(__uint_as_float(lp[e]) + pr);
-                        if (row_lane) ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
-                    }
-                    SMLA_TMEM_ST16(ta, lp);
-                }
-                ptx::tmem_wait_st();
-            } else {
-#pragma unroll
-                for (int h = 0; h < HP; ++h) {
-                    const float x = __uint_as_float(sv[h]);
-                    const float pr = (x == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(x - sM[h]);
-                    lreg[h] += pr;
-                    if (row_lane) ptx::st_shared_u16(pbase[h & 7] + (h >> 3) * 1024, bf16_bits(pr));
+                for (int e = 0; e < 2; ++e) {
+                    const int h = 8 * i + 2 * tq + e;
+                    ptx::st_shared_u16(p_addr(h, r0), pb[i][e]);
+                    ptx::st_shared_u16(p_addr(h, r1), pb[i][2 + e]);
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -403,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));
         }
 
-        // ---- the last PV, then per-head totals L = sum of the row lanes' partial sums
+        // ---- the last PV, then per-head totals L = sum of the threads' partial sums
         const bool aborted = ptx::named_bar_red_or(1, 128, failed || *sAbort);
         failed = aborted;
         if (nb > 0 && !aborted) {
@@ -416,24 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool have_o = nb > 0 && !failed;
 #pragma unroll
-        for (int cc = 0; cc < HP / 16; ++cc) {
-            uint32_t lv[16];
-            if constexpr (L::kSumsInTmem) {
-                SMLA_TMEM_LD16(tmem + lane_base + L::kColL + cc * 16, lv);
-                ptx::tmem_wait_ld();
-            } else {
+        for (int i = 0; i < NG; ++i) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) lv[e] = __float_as_uint(lreg[cc * 16 + e]);
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                float v = __uint_as_float(lv[e]);
-                v += __shfl_xor_sync(0xffffffffu, v, 16);
-                v += __shfl_xor_sync(0xffffffffu, v, 8);
+            for (int e = 0; e < 2; ++e) {
+                float v = lsum[i][e];
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                if (lane == 0) sRed[quad * HP + cc * 16 + e] = v;
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                if (g == 0) sRed[quad * HP + 8 * i + 2 * tq + e] = v;
             }
         }
         ptx::named_bar_sync(1, 128);
