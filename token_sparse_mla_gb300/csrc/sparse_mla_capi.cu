@@ -59,10 +59,10 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 cudaError_t set_kernel_attrs() {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0>, smla::SmallLayout<8>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1>, smla::SmallLayout<8>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0>, smla::SmallLayout<16>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1>, smla::SmallLayout<16>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0>, smla::SmallLayout<8, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1>, smla::SmallLayout<8, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0>, smla::SmallLayout<16, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1>, smla::SmallLayout<16, 1>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 0>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 1>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 0>, smla::Layout<64>::kBytes);
@@ -175,7 +175,7 @@ smla_status check_args(const void* q, const void* kv, const int32_t* idx, int32_
     return SMLA_OK;
 }
 
-Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms) {
+Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms, bool fp8) {
     Plan pl;
     pl.hp = h;
     const int rows = small_heads(h) ? smla::kSmRows : smla::kRows;
@@ -210,8 +210,8 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms) 
         pl.ctas = static_cast<int64_t>(T) * pl.splits;
     }
     pl.threads = small_heads(h) ? smla::kSmThreads : smla::kThreads;
-    pl.smem = h == 8    ? smla::SmallLayout<8>::kBytes
-              : h == 16 ? smla::SmallLayout<16>::kBytes
+    pl.smem = h == 8    ? (fp8 ? smla::SmallLayout<8, 1>::kBytes : smla::SmallLayout<8, 0>::kBytes)
+              : h == 16 ? (fp8 ? smla::SmallLayout<16, 1>::kBytes : smla::SmallLayout<16, 0>::kBytes)
               : h == 32 ? smla::Layout<32>::kBytes
                         : smla::Layout<64>::kBytes;
     return pl;
@@ -305,7 +305,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     if ((st = device_state(&dev, &ds)) != SMLA_OK) return st;
     EncodeTiledFn enc = nullptr;
     if (!small_heads(h) && (st = encode_fn(&enc)) != SMLA_OK) return st;
-    const Plan pl = make_plan(T, h, topk, splits, ds->num_sms);
+    const Plan pl = make_plan(T, h, topk, splits, ds->num_sms, kv_format == SMLA_KV_FP8);
 
     alignas(64) CUtensorMap tm_q;
     if (!small_heads(h)) {  // the tcgen05 kernel loads Q^T with TMA
@@ -502,7 +502,7 @@ smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t k
     int dev = 0;
     DeviceState* ds = nullptr;
     if (device_state(&dev, &ds) == SMLA_OK) num_sms = ds->num_sms;
-    const Plan pl = make_plan(T, h, topk, 0, num_sms);
+    const Plan pl = make_plan(T, h, topk, 0, num_sms, kv_format == SMLA_KV_FP8);
     if (splits) *splits = pl.splits;
     if (ctas) *ctas = static_cast<int32_t>(pl.ctas);
     if (smem_bytes) *smem_bytes = pl.smem;

@@ -34,7 +34,10 @@
 namespace smla {
 
 constexpr int kSmRows = 32;                                          // KV rows per stage
-constexpr int kSmStages = 5;
+constexpr int kSmStagesBf16 = 5;                                     // bf16 cache: operand stages
+constexpr int kSmStagesFp8 = 3;                                      // fp8 cache: operand stages ...
+constexpr int kSmRawStages = 4;                                      // ... fed by a raw-row ring
+constexpr int kSmRawStageBytes = kSmRows * kFp8RowBytes;             // 20992
 constexpr int kSmComputeWarps = 4;
 constexpr int kSmThreads = 32 * (kProducerWarps + kSmComputeWarps);  // 352
 constexpr int kSmCompute0 = 32 * kProducerWarps;                     // first compute thread
@@ -49,13 +52,16 @@ constexpr int kSmStageBytes = kSmRows * kSmRowStride;                 // 37376
 // separate requests in flight, and one of them alone tops out below the SM's share of HBM.
 constexpr int kSmBulkRows = 14;
 
-template <int H>
+template <int H, int KVF>
 struct SmallLayout {
     static_assert(H == 8 || H == 16, "the small-head kernel runs 8 or 16 heads");
     static constexpr int kNT = H / 8;                                // n-tiles of 8 heads
+    static constexpr int kStages = KVF == 0 ? kSmStagesBf16 : kSmStagesFp8;
     static constexpr int kStageBytes = kSmStageBytes;
     static constexpr int kOffKV = 0;
-    static constexpr int kOffRed = kSmStages * kStageBytes;          // S partials, float4 per lane
+    static constexpr int kOffRaw = kStages * kStageBytes;            // fp8: raw 656-byte rows
+    static constexpr int kRawBytes = KVF == 0 ? 0 : kSmRawStages * kSmRawStageBytes;
+    static constexpr int kOffRed = kOffRaw + kRawBytes;              // S partials, float4 per lane
     static constexpr int kRedBytes = kSmComputeWarps * 2 * kNT * 32 * 16;
     static constexpr int kPStride = 80;                              // bytes per head row of P^T
     static constexpr int kOffP = kOffRed + kRedBytes;
@@ -64,14 +70,15 @@ struct SmallLayout {
     static constexpr int kOffAlpha = kOffM + H * 4;                  // rescale factor / 1/L
     static constexpr int kOffML = kOffAlpha + H * 4;                 // segment m[H], L[H]
     static constexpr int kOffOut = kOffML + 2 * H * 4;               // bf16 output staging [H][512]
-    static constexpr int kOffBar = kOffOut + H * kDV * 2;            // full[5], empty[5]
-    static constexpr int kOffMisc = kOffBar + 2 * kSmStages * 8;     // abort flag, last-arrival flag
-    static constexpr int kOffMask = kOffMisc + 16;                   // [5] valid-row mask per stage
+    static constexpr int kOffBar = kOffOut + H * kDV * 2;            // full[stages], empty[stages]
+    static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;       // abort flag
+    static constexpr int kOffMask = kOffMisc + 16;                   // valid-row mask per stage
     static constexpr int kOffMrg = kOffMask + 32;                    // merge: m, L, weight [16][H] each
     static constexpr int kBytes = kOffMrg + 3 * kMaxParts * H * 4;
     // scratch slot of one partial segment: m[H], L[H], then O^T unnormalised as [H][512] fp32
     static constexpr int kSlotFloats = 2 * H + H * kDV;
-    static_assert(kOffP % 16 == 0 && kOffOut % 16 == 0, "16-byte aligned shared buffers");
+    static_assert(kOffP % 16 == 0 && kOffOut % 16 == 0 && kOffRaw % 16 == 0, "16-byte aligned shared buffers");
+    static_assert(kStages * 4 <= 32, "stage masks fit their slot");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
@@ -149,20 +156,22 @@ __host__ __device__ constexpr int small_full_count() {
     return KVF == 0 ? 32 * (kProducerWarps - 1) + 1 : 32 * kProducerWarps;
 }
 
-// KV row gather of the small-head kernel (producer warp pw), into kSmStages stages of kSmRows
+// KV row gather of the small-head kernel (producer warp pw), into NST stages of kSmRows
 // rows in the padded row-major layout.  Invalid entries become zero rows.  Lane i of every
 // producer warp holds the list entry of row i; the last warp also publishes the stage's mask of
 // valid rows (bit i = row i) in sMask[stage] before its arrival on the full barrier, so the
 // compute warps read validity from shared memory after their wait.
 //   bf16: warp 6 takes rows [0, kSmBulkRows), one row per lane, one cp.async.bulk of 1152 bytes
 //         each; warps 0-5 take rows kSmBulkRows + pw + 6 i with 16-byte cp.async.
-//   fp8:  warps 0-6 take rows pw + 7 i; each lane loads 16 latent bytes, its tile scale and
-//         (lanes 0-7) 16 rope bytes into registers, dequantises (e4m3 -> f16 exactly, x scale in
-//         fp32, -> bf16 round to nearest even) and stores the bf16 row.
-template <int KVF>
+//   fp8:  warps 0-6 take rows pw + 7 i.  Raw 656-byte rows are copied with cp.async into a ring
+//         of kSmRawStages blocks, kSmRawStages - 1 blocks ahead of use (about 63 KB in flight);
+//         then each lane dequantises 16 latent bytes of a row with its tile scale (e4m3 -> f16
+//         exactly, x scale in fp32, -> bf16 round to nearest even) into the bf16 operand stage,
+//         and lanes 0-7 copy the 128 bf16 rope bytes.
+template <int KVF, int NST>
 __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int nb, int pw, int lane, uint32_t sKV,
-                                             uint32_t bar_full0, uint32_t bar_empty0, uint32_t sMask,
-                                             volatile int* sAbort) {
+                                             uint32_t sRaw, uint32_t bar_full0, uint32_t bar_empty0,
+                                             uint32_t sMask, volatile int* sAbort) {
     // List entries are loaded kAhead blocks (256 entries) ahead into a ring indexed by
     // b % kAhead; the block loop is unrolled kAhead times so each ring index is static and an
     // entry is first read kAhead blocks after its load was issued.
@@ -188,21 +197,53 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int
     int ring[kAhead];
 #pragma unroll
     for (int u = 0; u < kAhead; ++u) ring[u] = fetch(u < nb);
+    // fp8: this warp's rows pw + 7 i of block bb, raw (656 bytes each) into raw stage
+    // bb % kSmRawStages: lanes copy the 32 latent chunks, lanes 0-8 the scales and rope.
+    // Invalid entries copy nothing and leave zeros (src-size 0), which dequantise to zeros.
+    auto issue_raw = [&](int bb, int slot_lane) {
+        const uint32_t rs = sRaw + (bb % kSmRawStages) * kSmRawStageBytes;
+        const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+#pragma unroll
+        for (int i = 0; i < kPerWarp; ++i) {
+            const int r = pw + kWarps * i;
+            if (r < kSmRows) {
+                const int slot = __shfl_sync(0xffffffffu, slot_lane, r);
+                const uint8_t* src = kv8 + static_cast<int64_t>(slot < 0 ? 0 : slot) * kFp8RowBytes;
+                const uint32_t nbytes = slot < 0 ? 0u : 16u;
+                const uint32_t rd = rs + r * kFp8RowBytes;
+                ptx::cp_async_16(rd + lane * 16, src + lane * 16, nbytes);
+                if (lane < 9) ptx::cp_async_16(rd + 512 + lane * 16, src + 512 + lane * 16, nbytes);
+            }
+        }
+    };
+    if constexpr (KVF == 1) {
+#pragma unroll
+        for (int k = 0; k + 1 < kSmRawStages; ++k) {
+            if (k < nb) issue_raw(k, valid_slot(ring[k], p.num_slots));
+            ptx::cp_async_commit();
+        }
+    }
     bool aborted = false;
     for (int b0 = 0; b0 < nb && !aborted; b0 += kAhead) {
 #pragma unroll
         for (int u = 0; u < kAhead; ++u) {
             const int b = b0 + u;
             if (b >= nb) break;
-            const int s = b % kSmStages;
+            const int s = b % NST;
             const uint32_t full = bar_full0 + 8u * s;
             const int my_slot = valid_slot(ring[u], p.num_slots);  // slot of row `lane`
+            if constexpr (KVF == 1) {
+                // raw rows of block b + kSmRawStages - 1 (their entries sit in the ring already)
+                const int ahead = valid_slot(ring[(u + kSmRawStages - 1) % kAhead], p.num_slots);
+                if (b + kSmRawStages - 1 < nb) issue_raw(b + kSmRawStages - 1, ahead);
+                ptx::cp_async_commit();  // one group per block, empty past the end
+            }
             ring[u] = fetch(b + kAhead < nb);
             const uint32_t vmask = __ballot_sync(0xffffffffu, my_slot >= 0);
-            if (b >= kSmStages) {
+            if (b >= NST) {
                 bool ok = true;
                 if (lane == 0)
-                    ok = ptx::mbar_wait(bar_empty0 + 8u * s, ((b / kSmStages) - 1) & 1, sAbort, &g_smla_error,
+                    ok = ptx::mbar_wait(bar_empty0 + 8u * s, ((b / NST) - 1) & 1, sAbort, &g_smla_error,
                                         kErrTimeout, kWaitLimitNs);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 __syncwarp();
@@ -246,40 +287,31 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int
                     ptx::cp_async_arrive_noinc(full);
                 }
             } else {
-                const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-                uint4 lat[kPerWarp], rope[kPerWarp];
-                float scl[kPerWarp];
-#pragma unroll
-                for (int i = 0; i < kPerWarp; ++i) {
-                    const int r = pw + kWarps * i;
-                    const int slot = __shfl_sync(0xffffffffu, my_slot, r & 31);
-                    lat[i] = make_uint4(0u, 0u, 0u, 0u);
-                    rope[i] = make_uint4(0u, 0u, 0u, 0u);
-                    scl[i] = 0.f;
-                    if (r < kSmRows && slot >= 0) {
-                        const uint8_t* row = kv8 + static_cast<int64_t>(slot) * kFp8RowBytes;
-                        lat[i] = ptx::ld_nc_v4(row + 16 * lane);
-                        scl[i] = ptx::ld_nc_f32(row + 512 + 4 * (lane >> 3));
-                        if (lane < 8) rope[i] = ptx::ld_nc_v4(row + 528 + 16 * lane);
-                    }
-                }
+                // block b's raw rows are complete for this thread's own copies once at most
+                // kSmRawStages - 1 younger groups are pending; the warp barrier shares them
+                ptx::cp_async_wait_group<kSmRawStages - 1>();
+                __syncwarp();
+                const uint32_t rs = sRaw + (b % kSmRawStages) * kSmRawStageBytes;
 #pragma unroll
                 for (int i = 0; i < kPerWarp; ++i) {
                     const int r = pw + kWarps * i;
                     if (r < kSmRows) {
+                        const uint32_t rr = rs + r * kFp8RowBytes;
+                        const uint4 lat = ptx::ld_shared_v4(rr + 16 * lane);
+                        const float scl = ptx::ld_shared_f32(rr + 512 + 4 * (lane >> 3));
                         uint4 v0, v1;
-                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat[i].x & 0xFFFFu, scl[i]);
-                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat[i].x >> 16, scl[i]);
-                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat[i].y & 0xFFFFu, scl[i]);
-                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat[i].y >> 16, scl[i]);
-                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat[i].z & 0xFFFFu, scl[i]);
-                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat[i].z >> 16, scl[i]);
-                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat[i].w & 0xFFFFu, scl[i]);
-                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat[i].w >> 16, scl[i]);
+                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat.x & 0xFFFFu, scl);
+                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat.x >> 16, scl);
+                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat.y & 0xFFFFu, scl);
+                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat.y >> 16, scl);
+                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat.z & 0xFFFFu, scl);
+                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat.z >> 16, scl);
+                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat.w & 0xFFFFu, scl);
+                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat.w >> 16, scl);
                         const uint32_t rd = st + r * kSmRowStride;
                         ptx::st_shared_v4(rd + (2 * lane) * 16, v0);      // dims 16 lane .. +7
                         ptx::st_shared_v4(rd + (2 * lane + 1) * 16, v1);  // dims 16 lane + 8 .. +15
-                        if (lane < 8) ptx::st_shared_v4(rd + (64 + lane) * 16, rope[i]);
+                        if (lane < 8) ptx::st_shared_v4(rd + (64 + lane) * 16, ptx::ld_shared_v4(rr + 528 + 16 * lane));
                     }
                 }
                 if (mask_warp && lane == 0) ptx::st_shared_u32(sMask + 4u * s, vmask);
@@ -316,8 +348,9 @@ __device__ __forceinline__ void load_q_frags(const FwdParams& p, int t, int cw, 
 
 template <int H, int KVF>
 __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
-    using L = SmallLayout<H>;
+    using L = SmallLayout<H, KVF>;
     constexpr int NT = L::kNT;
+    constexpr int NST = L::kStages;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
     if (sbase & 1023u) {  // uniform across the grid: every CTA leaves before any barrier
@@ -335,7 +368,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     float* sML = reinterpret_cast<float*>(smem + L::kOffML);
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::kOffMisc);
     const uint32_t bar_full0 = sbase + L::kOffBar;
-    const uint32_t bar_empty0 = sbase + L::kOffBar + 8 * kSmStages;
+    const uint32_t bar_empty0 = sbase + L::kOffBar + 8 * NST;
 
     // ---- this CTA's blocks [x0, x0 + nb) of the token-major block sequence
     const int64_t W = static_cast<int64_t>(p.T) * p.nblk;
@@ -345,7 +378,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
 
     if (threadIdx.x == 0) {
         *sAbort = 0;
-        for (int s = 0; s < kSmStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(bar_full0 + 8 * s, small_full_count<KVF>());
             ptx::mbar_init(bar_empty0 + 8 * s, kSmComputeWarps);
         }
@@ -356,7 +389,8 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
 
     if (warp < kProducerWarps) {
         // ================================================================ producers
-        small_gather<KVF>(p, x0, nb, warp, lane, sKV, bar_full0, bar_empty0, sbase + L::kOffMask, sAbort);
+        small_gather<KVF, NST>(p, x0, nb, warp, lane, sKV, sbase + L::kOffRaw, bar_full0, bar_empty0,
+                               sbase + L::kOffMask, sAbort);
         return;
     }
     // ==================================================================== compute warps
@@ -394,11 +428,11 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     load_q_frags<H>(p, t, cw, lane, bq);
 
     for (int b = 0; b < nb; ++b) {
-        const int s = b % kSmStages;
+        const int s = b % NST;
         const uint32_t stb = sKV + s * L::kStageBytes;
         bool ok = true;
         if (lane == 0)
-            ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / kSmStages) & 1, sAbort, &g_smla_error, kErrTimeout,
+            ok = ptx::mbar_wait(bar_full0 + 8 * s, (b / NST) & 1, sAbort, &g_smla_error, kErrTimeout,
                                 kWaitLimitNs);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
