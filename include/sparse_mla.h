@@ -29,8 +29,9 @@
  *
  * Conventions for every entry point below:
  *   - Device pointers belong to the caller.  The library allocates nothing per
- *     call.  With 8 or 16 heads, a launch that cuts token lists between CTAs
- *     (see sparse_mla_fwd_ex) merges the parts through a scratch buffer: one per
+ *     call.  With 8 or 16 heads, a launch that cuts token lists between CTAs at
+ *     arbitrary points (only sparse_mla_fwd_ex with a split count that does not
+ *     divide ceil(topk/32) does) merges the parts through a scratch buffer: one per
  *     (device, stream), allocated at the first call on that stream that needs it
  *     (or a larger one), cleared once, and reused.  Calls on one stream are
  *     ordered and share it; a stream capture needs one uncaptured call of the
@@ -101,9 +102,11 @@ smla_status sparse_mla_fwd(const void* q, const void* kv_cache, const int32_t* i
  *   h = 32, 64: each token's list is split over `splits` CTAs of one
  *     thread-block cluster and merged on chip by log-sum-exp weights.
  *   h = 8, 16: the T x ceil(topk/32) row blocks are cut into T * splits equal
- *     contiguous ranges, one per CTA (at most one per SM when a list is cut),
- *     wherever the cuts fall; the parts of a cut list are merged through the
- *     scratch after a grid-wide barrier (cooperative launch), in CTA order.
+ *     contiguous ranges, one per CTA.  When splits divides ceil(topk/32) each
+ *     list falls into `splits` whole parts, one thread-block cluster per token,
+ *     merged on chip; otherwise the cuts fall anywhere (at most one CTA per SM)
+ *     and the parts of a cut list are merged through the scratch after a
+ *     grid-wide barrier (cooperative launch), in CTA order.
  * Results agree with any other split count up to fp32 rounding, and repeated
  * calls with the same arguments give identical bytes.
  */

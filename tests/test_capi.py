@@ -79,10 +79,10 @@ def test_zero_tokens_is_a_noop(lib):
 
 
 def test_launch_info_without_device(lib):
-    # 8/16 heads: 32 tokens x 64 row blocks on 152 SMs (assumed without a device): four CTAs
-    # per token (the largest power of two dividing 64 with 32 x s <= 152), no cluster
+    # 8/16 heads: 32 tokens x 64 row blocks on 152 SMs (assumed without a device): a cluster
+    # of four CTAs per token (the largest power of two dividing 64 with 32 x s <= 152)
     info = smla.launch_info(32, 8, 2048)
-    assert info["launches"] == 1 and info["splits"] == 0 and info["ctas"] == 128
+    assert info["launches"] == 1 and info["splits"] == 4 and info["ctas"] == 128
     # as many tokens as SMs: one CTA per token
     assert smla.launch_info(152, 8, 2048)["ctas"] == 152
     assert info["smem_bytes"] <= 232448

@@ -184,16 +184,17 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms, 
     if (small_heads(h)) {
         // The T * nblk row blocks are cut into `ctas` equal contiguous ranges.  Default: whole
         // lists (one CTA per token) once the tokens alone fill the SMs; otherwise s CTAs per
-        // token, s the largest power of two that divides nblk with T * s <= #SMs and s <= 16,
-        // so every range lies within one list (each CTA then merges one cut list).  Given
-        // `splits`: T * splits CTAs, wherever the cuts fall.  Cut lists are merged after a
+        // token, s the largest power of two that divides nblk with T * s <= #SMs and s <= 8,
+        // so every range is an aligned part of one list: one thread-block cluster per token,
+        // merged through distributed shared memory.  Given `splits`: T * splits CTAs; if the
+        // cuts do not fall on whole parts, the parts are merged through the scratch after a
         // grid-wide barrier, so such a launch never has more CTAs than SMs.
         const int64_t W = static_cast<int64_t>(T) * nblk;
         int64_t want = T;
         if (splits > 0) {
             want = static_cast<int64_t>(T) * splits;
         } else {
-            for (int c = smla::kMaxParts; c > 1; c >>= 1) {
+            for (int c = smla::kMaxSplits; c > 1; c >>= 1) {
                 if (nblk % c == 0 && static_cast<int64_t>(T) * c <= num_sms) {
                     want = static_cast<int64_t>(T) * c;
                     break;
@@ -203,8 +204,17 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms, 
         pl.splits = 0;
         pl.ctas = W < want ? W : want;
         auto whole_lists = [&](int64_t g) { return W % g == 0 && (W / g) % nblk == 0; };
-        if (pl.ctas > num_sms && !whole_lists(pl.ctas)) pl.ctas = num_sms;
-        if (pl.ctas > 0 && !whole_lists(pl.ctas)) pl.scratch = small_scratch_bytes(pl.ctas, h);
+        const int64_t per_token = pl.ctas % T == 0 ? pl.ctas / T : 0;
+        const bool pow2 = per_token > 0 && (per_token & (per_token - 1)) == 0;
+        if (pow2 && per_token >= 2 && per_token <= smla::kMaxSplits && nblk % per_token == 0) {
+            // aligned parts, 2, 4 or 8 per list (so each CTA of the cluster owns 512 / parts
+            // output dims, a multiple of 8): one thread-block cluster per token, merged through
+            // distributed shared memory (no scratch, no grid barrier)
+            pl.splits = static_cast<int>(per_token);
+        } else {
+            if (pl.ctas > num_sms && !whole_lists(pl.ctas)) pl.ctas = num_sms;
+            if (pl.ctas > 0 && !whole_lists(pl.ctas)) pl.scratch = small_scratch_bytes(pl.ctas, h);
+        }
     } else {
         pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
         pl.ctas = static_cast<int64_t>(T) * pl.splits;

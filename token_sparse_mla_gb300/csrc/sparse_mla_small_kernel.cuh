@@ -79,6 +79,7 @@ struct SmallLayout {
     static constexpr int kSlotFloats = 2 * H + H * kDV;
     static_assert(kOffP % 16 == 0 && kOffOut % 16 == 0 && kOffRaw % 16 == 0, "16-byte aligned shared buffers");
     static_assert(kStages * 4 <= 32, "stage masks fit their slot");
+    static_assert(H * kDV * 4 + kMaxSplits * 2 * H * 4 <= kStages * kStageBytes, "cluster merge buffers fit the stages");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
@@ -391,6 +392,10 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         // ================================================================ producers
         small_gather<KVF, NST>(p, x0, nb, warp, lane, sKV, sbase + L::kOffRaw, bar_full0, bar_empty0,
                                sbase + L::kOffMask, sAbort);
+        if (p.splits > 1) {  // the cluster merge below: every thread takes part in its barriers
+            ptx::cluster_sync();
+            ptx::cluster_sync();
+        }
         return;
     }
     // ==================================================================== compute warps
@@ -625,6 +630,9 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
                 p.lse[static_cast<int64_t>(t) * H + wtid] =
                     tot > 0.f ? (sML[wtid] + log2f(tot)) * 0.69314718055994531f : -CUDART_INF_F;
             }
+        } else if (p.splits > 1) {
+            // ---- an aligned part of a list (one per CTA of the cluster): (m, L) stay in sML and
+            // O^T in registers for the cluster merge after the loop
         } else {
             // ---- part of a list cut between CTAs: leave (m, L, O^T) in this CTA's slot; the
             // parts are merged after the grid barrier below
@@ -665,6 +673,91 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         load_q_frags<H>(p, t, cw, lane, bq);
     }
     if (failed) *sAbort = 1;  // producers still waiting for a free stage give up
+    if (p.splits > 1) {
+        // ================================================================ cluster merge
+        // The list of token t is cut into p.splits aligned parts, one per CTA of a thread-block
+        // cluster (rank = part).  After every CTA has left its loop (so stage memory is free),
+        // each pushes its per-head (m, L) to all CTAs and its unnormalised O^T fragments for
+        // dims [k*ds, (k+1)*ds) to CTA k (ds = 512 / splits), into stage memory; after a second
+        // cluster barrier CTA k weights the parts by 2^(m_j - M) / sum_j L_j 2^(m_j - M) and
+        // stores its dims.  No CTA touches another's memory after that barrier.
+        const int ns = p.splits;  // 2, 4 or 8 (host plan): ds below is a multiple of 8
+        const int rank = static_cast<int>(blockIdx.x) % ns;
+        const int ds = kDV / ns;
+        const uint32_t recv = sKV;                            // [ns][H][ds] fp32
+        const uint32_t recv_ml = sKV + H * kDV * 4;           // [ns][2H] fp32
+        const bool have = nb > 0 && !failed;
+        ptx::cluster_sync();
+        if (wtid < H) {
+            const float m = have ? sML[wtid] : -CUDART_INF_F;
+            const float l = have ? sML[H + wtid] : 0.f;
+            for (int k = 0; k < ns; ++k) {
+                ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + wtid) * 4, k), m);
+                ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + H + wtid) * 4, k), l);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+                const int d = 128 * cw + 16 * mt + g + 8 * hi;
+                const int k = d / ds;
+                const int dd = d - k * ds;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = nt * 8 + 2 * tq + e;
+                        const uint32_t la = recv + static_cast<uint32_t>(((rank * H + h) * ds + dd) * 4);
+                        ptx::st_shared_cluster_f32(ptx::map_shared_rank(la, k), have ? o[mt][nt][2 * hi + e] : 0.f);
+                    }
+                }
+            }
+        }
+        ptx::cluster_sync();
+        const float* rml = reinterpret_cast<const float*>(smem + H * kDV * 4);
+        const float* rcv = reinterpret_cast<const float*>(smem);
+        float* mW = reinterpret_cast<float*>(smem + L::kOffMrg);
+        if (wtid < H) {
+            float M = -CUDART_INF_F;
+            for (int j = 0; j < ns; ++j) M = fmaxf(M, rml[j * 2 * H + wtid]);
+            float Lt = 0.f;
+            for (int j = 0; j < ns; ++j) {
+                const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
+                if (mj != -CUDART_INF_F && lj > 0.f) Lt += lj * ptx::ex2_approx(mj - M);
+            }
+            const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
+            for (int j = 0; j < ns; ++j) {
+                const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
+                mW[j * H + wtid] = (mj != -CUDART_INF_F && lj > 0.f) ? ptx::ex2_approx(mj - M) * inv : 0.f;
+            }
+            if (rank == 0)
+                p.lse[static_cast<int64_t>(t) * H + wtid] =
+                    Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
+        }
+        ptx::named_bar_sync(1, 128);
+        // eight dims of one head per item, stored as one 16-byte vector
+        const int per_head = ds / 8;
+        for (int it = wtid; it < H * per_head; it += 128) {
+            const int hh = it / per_head;
+            const int dd = (it % per_head) * 8;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < ns; ++j) {
+                const float w = mW[j * H + hh];
+                const float4 lo = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd);
+                const float4 hv = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd + 4);
+                acc[0] += w * lo.x; acc[1] += w * lo.y; acc[2] += w * lo.z; acc[3] += w * lo.w;
+                acc[4] += w * hv.x; acc[5] += w * hv.y; acc[6] += w * hv.z; acc[7] += w * hv.w;
+            }
+            uint4 packed;
+            packed.x = pack_bf16x2(acc[0], acc[1]);
+            packed.y = pack_bf16x2(acc[2], acc[3]);
+            packed.z = pack_bf16x2(acc[4], acc[5]);
+            packed.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * H + hh) * kDV + rank * ds + dd) = packed;
+        }
+        return;
+    }
     if (p.part == nullptr) return;  // every list lay within one CTA
 
     // ==================================================================== merge of cut lists
