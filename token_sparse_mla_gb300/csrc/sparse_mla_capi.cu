@@ -366,21 +366,29 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
     if (pl.splits > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(pl.splits);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(pl.splits);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
     } else if (pl.scratch > 0) {
         // the merge of cut lists waits at a grid-wide barrier: all CTAs must be co-resident
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeCooperative;
+        attr[nattr].val.cooperative = 1;
+        ++nattr;
     }
+    if (pl.scratch == 0) {
+        // programmatic dependent launch: this grid may be scheduled while the previous work on
+        // the stream drains; the kernels wait (griddepcontrol.wait) before touching global memory
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
     cudaError_t e;
     const bool fp8 = kv_format == SMLA_KV_FP8;
     if (h == 8)

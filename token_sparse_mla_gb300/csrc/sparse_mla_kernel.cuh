@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wtid = threadIdx.x - kSoftmaxThread0;
         if (wtid < HP) sM[wtid] = -CUDART_INF_F;
     }
+    // launched as a programmatic dependent: nothing above touched global memory
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();

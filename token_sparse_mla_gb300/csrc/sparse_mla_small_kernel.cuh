@@ -386,6 +386,9 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         ptx::fence_mbarrier_init();
     }
     if (threadIdx.x >= kSmCompute0 && threadIdx.x - kSmCompute0 < H) sM[threadIdx.x - kSmCompute0] = -CUDART_INF_F;
+    // launched as a programmatic dependent: nothing above touched global memory
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
     __syncthreads();
 
     if (warp < kProducerWarps) {
