@@ -204,7 +204,7 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms, 
         pl.splits = 0;
         pl.ctas = W < want ? W : want;
         auto whole_lists = [&](int64_t g) { return W % g == 0 && (W / g) % nblk == 0; };
-        const int64_t per_token = pl.ctas % T == 0 ? pl.ctas / T : 0;
+        const int64_t per_token = (T > 0 && pl.ctas % T == 0) ? pl.ctas / T : 0;
         const bool pow2 = per_token > 0 && (per_token & (per_token - 1)) == 0;
         if (pow2 && per_token >= 2 && per_token <= smla::kMaxSplits && nblk % per_token == 0) {
             // aligned parts, 2, 4 or 8 per list (so each CTA of the cluster owns 512 / parts
