@@ -35,6 +35,7 @@ namespace smla {
 
 constexpr int kSmRows = 32;                                          // KV rows per stage
 constexpr int kSmStagesBf16 = 5;                                     // bf16 cache: operand stages
+constexpr int kSmStagesBf16H8 = 6;                                   // (six fit at 8 heads)
 constexpr int kSmStagesFp8 = 3;                                      // fp8 cache: operand stages ...
 constexpr int kSmRawStages = 4;                                      // ... fed by a raw-row ring
 constexpr int kSmRawStageBytes = kSmRows * kFp8RowBytes;             // 20992
@@ -56,7 +57,7 @@ template <int H, int KVF>
 struct SmallLayout {
     static_assert(H == 8 || H == 16, "the small-head kernel runs 8 or 16 heads");
     static constexpr int kNT = H / 8;                                // n-tiles of 8 heads
-    static constexpr int kStages = KVF == 0 ? kSmStagesBf16 : kSmStagesFp8;
+    static constexpr int kStages = KVF == 1 ? kSmStagesFp8 : (H == 8 ? kSmStagesBf16H8 : kSmStagesBf16);
     static constexpr int kStageBytes = kSmStageBytes;
     static constexpr int kOffKV = 0;
     static constexpr int kOffRaw = kStages * kStageBytes;            // fp8: raw 656-byte rows
@@ -69,15 +70,15 @@ struct SmallLayout {
     static constexpr int kOffM = kOffHr + kSmComputeWarps * H * 4;   // running max (log2 units)
     static constexpr int kOffAlpha = kOffM + H * 4;                  // rescale factor / 1/L
     static constexpr int kOffML = kOffAlpha + H * 4;                 // segment m[H], L[H]
-    static constexpr int kOffOut = kOffML + 2 * H * 4;               // bf16 output staging [H][512]
-    static constexpr int kOffBar = kOffOut + H * kDV * 2;            // full[stages], empty[stages]
+    static constexpr int kOffBar = kOffML + 2 * H * 4;               // full[stages], empty[stages]
     static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;       // abort flag
     static constexpr int kOffMask = kOffMisc + 16;                   // valid-row mask per stage
     static constexpr int kOffMrg = kOffMask + 32;                    // merge: m, L, weight [16][H] each
     static constexpr int kBytes = kOffMrg + 3 * kMaxParts * H * 4;
     // scratch slot of one partial segment: m[H], L[H], then O^T unnormalised as [H][512] fp32
     static constexpr int kSlotFloats = 2 * H + H * kDV;
-    static_assert(kOffP % 16 == 0 && kOffOut % 16 == 0 && kOffRaw % 16 == 0, "16-byte aligned shared buffers");
+    static_assert(kOffP % 16 == 0 && kOffRaw % 16 == 0, "16-byte aligned shared buffers");
+    static_assert(H * kDV * 2 <= kStages * kStageBytes, "output staging fits the stages");
     static_assert(kStages * 4 <= 32, "stage masks fit their slot");
     static_assert(H * kDV * 4 + kMaxSplits * 2 * H * 4 <= kStages * kStageBytes, "cluster merge buffers fit the stages");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
@@ -610,8 +611,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         ptx::named_bar_sync(1, 128);
 
         if (seg_from_start && token_end) {
-            // ---- the whole list was here: O = O^T / L as bf16, staged as out[t] ([h][512])
-            uint16_t* so = reinterpret_cast<uint16_t*>(smem + L::kOffOut);
+            // ---- the whole list was here: O = O^T / L as bf16.  After the CTA's last block the
+            // stage memory is free: out[t] ([h][512]) is staged there and written with 16-byte
+            // stores; a list that ends earlier in the range is written straight from registers.
+            const bool last = b + 1 == nb;
+            uint16_t* so = last ? reinterpret_cast<uint16_t*>(smem + L::kOffKV)
+                                : reinterpret_cast<uint16_t*>(p.out + static_cast<int64_t>(t) * H * kDV);
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const int d = 128 * cw + 16 * mt + g;
@@ -624,10 +629,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
                     so[(h + 1) * kDV + d + 8] = bf16_bits(o[mt][nt][3] * sAlpha[h + 1]);
                 }
             }
-            ptx::named_bar_sync(1, 128);
-            const uint4* src = reinterpret_cast<const uint4*>(so);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * H * kDV);
-            for (int v = wtid; v < H * (kDV / 8); v += 128) dst[v] = src[v];
+            if (last) {
+                ptx::named_bar_sync(1, 128);
+                const uint4* src = reinterpret_cast<const uint4*>(so);
+                uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * H * kDV);
+                for (int v = wtid; v < H * (kDV / 8); v += 128) dst[v] = src[v];
+            }
             if (wtid < H) {
                 const float tot = sML[H + wtid];
                 p.lse[static_cast<int64_t>(t) * H + wtid] =
