@@ -329,6 +329,17 @@ def test_fp8_random(h, splits):
     check_case(q, kv, idx, 576 ** -0.5, splits, kv_format="fp8", what=f"fp8 h={h} splits={splits}")
 
 
+@pytest.mark.parametrize("h", [8, 16])
+@pytest.mark.parametrize("splits", [0, 2])
+def test_fp8_cluster_parts(h, splits):
+    # topk 1000 = 32 row blocks: the list is cut into 8 (default) or 2 aligned parts, one
+    # thread-block cluster per token, merged through distributed shared memory
+    q, kv, idx = _rand_fp8(400 + h, 5, h, 1000, 6000)
+    info = smla.launch_info(5, h, 1000, "fp8")
+    assert splits != 0 or info["splits"] == 8
+    check_case(q, kv, idx, 576 ** -0.5, splits, kv_format="fp8", what=f"fp8 clusters h={h} splits={splits}")
+
+
 def test_fp8_reduced_config():
     w = wl("fp8_mixed", n_seq=1, n_tokens=48)
     check_case(w.q, w.kv, w.indices, w.scale, 0, kv_format="fp8", what="fp8_mixed prefix")
