@@ -14,19 +14,22 @@
 //                                                V^T comes from the SAME shared-memory tile as K
 //                                                through ldmatrix.trans.
 //
-// Rows arrive in 32-row stages (five in flight) gathered by seven producer warps
-// (small_gather).  Each compute warp takes eight of the block's rows for the softmax: masking, a
-// running max per head in log2 units with conditional rescaling (only when the max grows by more
-// than 2^8), fp32 partial sums, P^T (bf16) to shared memory.
+// Rows arrive in 32-row stages (six in flight at 8 heads, five at 16; fp8 rows through a raw
+// ring, see small_gather) gathered by seven producer warps.  Each compute warp takes eight of the
+// block's rows for the softmax: masking, a running max per head in log2 units with conditional
+// rescaling (only when the max grows by more than 2^8), fp32 partial sums, P^T (bf16) to shared
+// memory.
 //
 // Work partition: the T * nblk row blocks (nblk = ceil(topk / 32) per token, token-major) are
-// cut into `grid` equal contiguous ranges, one per CTA (grid = the SM count by default), so every
-// SM gets the same number of rows whatever T is.  A CTA walks its range as consecutive token
-// segments; its producers stream straight across token boundaries.  A token whose whole list
-// lies in one CTA is normalised and stored directly; a token cut between CTAs leaves one partial
-// (m, L, unnormalised O) per CTA in a global scratch slot, and the last CTA to arrive on the
-// token's counter merges them (weights 2^(m_j - M) / sum_j L_j 2^(m_j - M), in CTA order, so
-// the result does not depend on which CTA merges).
+// cut into `grid` equal contiguous ranges, one per CTA.  A CTA walks its range as consecutive
+// token segments; its producers stream straight across token boundaries.  A token whose whole
+// list lies in one CTA is normalised and stored directly.  When every list falls into 2, 4 or 8
+// whole parts (the default below one CTA per SM) the parts of a token form a thread-block
+// cluster and merge through distributed shared memory; otherwise (cuts anywhere, explicit split
+// counts only) each part leaves (m, L, unnormalised O) in a global scratch slot and, after a
+// grid-wide barrier, every participant merges one slice of the output dims.  Both merges weigh
+// the parts by 2^(m_j - M) / sum_j L_j 2^(m_j - M) in a fixed order, so results repeat bit for
+// bit.
 #pragma once
 
 #include "sparse_mla_common.cuh"
@@ -450,13 +453,16 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         const bool valid = (ptx::ld_shared_u32(sbase + L::kOffMask + 4u * s) >> rr) & 1u;
 
         // ---- partial S^T over this warp's 144 dims, all 32 rows
-        float cs[2][NT][4];
+        // at 16 heads two accumulator sets (even and odd k-steps) halve the dependent MMA chains
+        // (measured: 94 -> 80 us on the h=16 sweep; at 8 heads it costs ~1 %, so one set)
+        constexpr bool kTwoSets = NT > 1;
+        float cs[2][NT][4], cs2[2][NT][4];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) cs[mt][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) cs[mt][nt][e] = cs2[mt][nt][e] = 0.f;
         if (ok) {
 #pragma unroll
             for (int kk = 0; kk < kSmKSteps; ++kk) {
@@ -468,8 +474,21 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
                     uint32_t a[4];
                     mma16816::ldsm_x4(a, stb + row * kSmRowStride + kchunk);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma16816::mma(cs[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kTwoSets && (kk & 1))
+                            mma16816::mma(cs2[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
+                        else
+                            mma16816::mma(cs[mt][nt], a, bq[kk][nt][0], bq[kk][nt][1]);
+                    }
                 }
+            }
+            if constexpr (kTwoSets) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) cs[mt][nt][e] += cs2[mt][nt][e];
             }
         }
 #pragma unroll
