@@ -127,3 +127,25 @@ def test_product_package_does_not_import_the_oracle():
     for f in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.cuh")):
         text = f.read_text()
         assert "oracle" not in text.replace("oracle-free", ""), f"{f} mentions the oracle"
+
+
+def test_launch_plans_over_many_shapes(lib):
+    # host-side plan (no device: 152 SMs assumed) for every head count and a spread of batch
+    # sizes and list lengths: whole lists, aligned cluster parts (2/4/8 CTAs per token, never
+    # more CTAs than SMs) or the tcgen05 kernel's clusters
+    for h in (8, 16, 32, 64):
+        for T in (1, 3, 19, 32, 76, 151, 152, 153, 1000):
+            for topk in (1, 33, 100, 2048, 2049, 4096):
+                nblk_small = (topk + 31) // 32
+                info = smla.launch_info(T, h, topk)
+                assert info["launches"] == 1 and info["smem_bytes"] <= 232448
+                s, ctas = info["splits"], info["ctas"]
+                if h <= 16:
+                    if s == 0:
+                        assert ctas == T  # whole lists, one CTA per token
+                    else:
+                        assert s in (2, 4, 8) and nblk_small % s == 0
+                        assert ctas == T * s and ctas <= 152
+                else:
+                    assert s in (1, 2, 4, 8) and ctas == T * s
+                    assert s == 1 or ctas <= 152
