@@ -59,10 +59,14 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 cudaError_t set_kernel_attrs() {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0>, smla::SmallLayout<8, 0>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1>, smla::SmallLayout<8, 1>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0>, smla::SmallLayout<16, 0>::kBytes);
-    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1>, smla::SmallLayout<16, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0, false>, smla::SmallLayout<8, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1, false>, smla::SmallLayout<8, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0, false>, smla::SmallLayout<16, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1, false>, smla::SmallLayout<16, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 0, true>, smla::SmallLayout<8, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1, true>, smla::SmallLayout<8, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0, true>, smla::SmallLayout<16, 0>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1, true>, smla::SmallLayout<16, 1>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 0>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 1>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 0>, smla::Layout<64>::kBytes);
@@ -391,12 +395,19 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     cfg.numAttrs = nattr;
     cudaError_t e;
     const bool fp8 = kv_format == SMLA_KV_FP8;
-    if (h == 8)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 1>, prm)
-                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 0>, prm);
+    const bool cl = pl.splits > 1;  // small-head kernels: the cluster-merge instantiation
+    if (h == 8 && cl)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 1, true>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 0, true>, prm);
+    else if (h == 8)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 1, false>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<8, 0, false>, prm);
+    else if (h == 16 && cl)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 1, true>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 0, true>, prm);
     else if (h == 16)
-        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 1>, prm)
-                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 0>, prm);
+        e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 1, false>, prm)
+                : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_small_kernel<16, 0, false>, prm);
     else if (h == 32)
         e = fp8 ? cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<32, 1>, tm_q, prm)
                 : cudaLaunchKernelEx(&cfg, smla::sparse_mla_fwd_tc_kernel<32, 0>, tm_q, prm);

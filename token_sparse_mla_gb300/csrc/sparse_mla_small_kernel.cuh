@@ -56,6 +56,10 @@ constexpr int kSmStageBytes = kSmRows * kSmRowStride;                 // 37376
 // batch, 0 to 20 bulk rows per stage run within 2 % of each other (the SM streams about
 // 44 GB/s either way) and 24 or more are slower; 14 keeps both engines in use.
 constexpr int kSmBulkRows = 14;
+// Cluster merge: a CTA's unnormalised O^T as [h][516] fp32 in its own stage memory.  516 = 512 + 4
+// puts the fragment stores of a warp (heads 2*tq (+1), dims g) on 32 distinct banks and keeps
+// every head row 16-byte aligned for the vector loads of the other CTAs.
+constexpr int kSmLocStride = kDV + 4;
 
 template <int H, int KVF>
 struct SmallLayout {
@@ -84,7 +88,7 @@ struct SmallLayout {
     static_assert(kOffP % 16 == 0 && kOffRaw % 16 == 0, "16-byte aligned shared buffers");
     static_assert(H * kDV * 2 <= kStages * kStageBytes, "output staging fits the stages");
     static_assert(kStages * 4 <= 32, "stage masks fit their slot");
-    static_assert(H * kDV * 4 + kMaxSplits * 2 * H * 4 <= kStages * kStageBytes, "cluster merge buffers fit the stages");
+    static_assert(H * kSmLocStride * 4 + 2 * H * 4 <= kStages * kStageBytes, "cluster merge buffers fit the stages");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
@@ -352,7 +356,85 @@ __device__ __forceinline__ void load_q_frags(const FwdParams& p, int t, int cw, 
     }
 }
 
-template <int H, int KVF>
+// Cluster merge of token t's list, cut into ns aligned parts, one per CTA of the cluster
+// (rank = part).  Every CTA has left its unnormalised O^T as [H][kSmLocStride] fp32 at `loc`
+// in its own shared memory, followed by (m, L) per head as [H][2]; the caller has passed a
+// cluster barrier since.  Each thread of CTA `rank` takes items (head, 8 output dims) of the
+// dims [rank*ds, (rank+1)*ds), ds = 512/ns: it loads that piece of every part and the parts'
+// (m, L) with vector loads from the other CTAs' shared memory (all in flight at once), weights
+// part j by 2^(m_j - M) / sum_i L_i 2^(m_i - M) (M the largest m_i), sums in part order and
+// stores eight bf16.  Rank 0 also stores the LSE.
+template <int H>
+__device__ __forceinline__ void cluster_pull_merge(const FwdParams& p, int t, uint32_t loc, int ns, int rank) {
+    const int ds = kDV / ns;
+    const int per_head = ds / 8;
+    for (int it = threadIdx.x; it < H * per_head; it += kSmThreads) {
+        const int hh = it / per_head;
+        const int dd = rank * ds + (it % per_head) * 8;
+        // (m, L) of every part, and the first four parts' pieces, in flight together
+        float2 ml[kMaxSplits];
+        float4 lo[4], hi[4];
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j)
+            if (j < ns)
+                ml[j] = ptx::ld_shared_cluster_v2(ptx::map_shared_rank(loc, j) +
+                                                  static_cast<uint32_t>((H * kSmLocStride + 2 * hh) * 4));
+        auto load4 = [&](int j0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j0 + u < ns) {
+                    const uint32_t base = ptx::map_shared_rank(loc, j0 + u);
+                    lo[u] = ptx::ld_shared_cluster_v4(base + static_cast<uint32_t>((hh * kSmLocStride + dd) * 4));
+                    hi[u] = ptx::ld_shared_cluster_v4(base + static_cast<uint32_t>((hh * kSmLocStride + dd + 4) * 4));
+                }
+            }
+        };
+        load4(0);
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j)
+            if (j < ns) M = fmaxf(M, ml[j].x);
+        float Lt = 0.f;
+        float w[kMaxSplits];
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j) {
+            w[j] = 0.f;
+            if (j < ns && ml[j].x != -CUDART_INF_F && ml[j].y > 0.f) {
+                w[j] = ptx::ex2_approx(ml[j].x - M);
+                Lt += ml[j].y * w[j];
+            }
+        }
+        const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j0 = 0; j0 < kMaxSplits; j0 += 4) {
+            if (j0 >= ns) break;
+            if (j0 > 0) load4(j0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j0 + u < ns) {
+                    const float wj = w[j0 + u] * inv;
+                    acc[0] += wj * lo[u].x; acc[1] += wj * lo[u].y; acc[2] += wj * lo[u].z; acc[3] += wj * lo[u].w;
+                    acc[4] += wj * hi[u].x; acc[5] += wj * hi[u].y; acc[6] += wj * hi[u].z; acc[7] += wj * hi[u].w;
+                }
+            }
+        }
+        uint4 packed;
+        packed.x = pack_bf16x2(acc[0], acc[1]);
+        packed.y = pack_bf16x2(acc[2], acc[3]);
+        packed.z = pack_bf16x2(acc[4], acc[5]);
+        packed.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * H + hh) * kDV + dd) = packed;
+        if (rank == 0 && dd == 0)
+            p.lse[static_cast<int64_t>(t) * H + hh] = Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+}
+
+// CL: the launch is a cluster launch (p.splits > 1, aligned parts merged in the cluster).  The
+// merge is compiled only into those kernels: at 16 heads the compute warps sit at the register
+// limit of 11 warps per SM (168), and the merge code alone moved their allocation into spills
+// (an 80 -> 83 us loss on a 16-head launch that never merges).
+template <int H, int KVF, bool CL>
 __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
     using L = SmallLayout<H, KVF>;
     constexpr int NT = L::kNT;
@@ -391,7 +473,18 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         ptx::fence_mbarrier_init();
     }
     if (threadIdx.x >= kSmCompute0 && threadIdx.x - kSmCompute0 < H) sM[threadIdx.x - kSmCompute0] = -CUDART_INF_F;
-    // launched as a programmatic dependent: nothing above touched global memory
+    // Launched as a programmatic dependent: nothing above reads global memory.  Warp 0 moves the
+    // list entries of the CTA's first eight blocks and its first token's q into L2 first: a
+    // prefetch returns no data and fills no L1, and L2 is where the previous launch's stores
+    // land, so the loads after the wait still see that launch's results.
+    if (warp == 0) {
+        const int64_t tp = x0 / p.nblk;
+        const int jp = static_cast<int>(x0 - tp * p.nblk) * kSmRows;
+        const int32_t* ib = p.indices + tp * p.topk + jp;
+        if (lane < 8 && jp + lane * 32 < p.topk) ptx::prefetch_l2(ib + lane * 32);
+        const char* qb = reinterpret_cast<const char*>(p.q + tp * H * kDQK);
+        for (int l = lane; l < H * kDQK * 2 / 128; l += 32) ptx::prefetch_l2(qb + l * 128);
+    }
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
     __syncthreads();
@@ -400,8 +493,11 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         // ================================================================ producers
         small_gather<KVF, NST>(p, x0, nb, warp, lane, sKV, sbase + L::kOffRaw, bar_full0, bar_empty0,
                                sbase + L::kOffMask, sAbort);
-        if (p.splits > 1) {  // the cluster merge below: every thread takes part in its barriers
+        if constexpr (CL) {  // the cluster merge: every thread takes part
             ptx::cluster_sync();
+            cluster_pull_merge<H>(p, static_cast<int>(x0 / p.nblk), sKV, p.splits,
+                                  static_cast<int>(blockIdx.x) % p.splits);
+            __syncwarp();
             ptx::cluster_sync();
         }
         return;
@@ -660,7 +756,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
                 p.lse[static_cast<int64_t>(t) * H + wtid] =
                     tot > 0.f ? (sML[wtid] + log2f(tot)) * 0.69314718055994531f : -CUDART_INF_F;
             }
-        } else if (p.splits > 1) {
+        } else if (CL) {
             // ---- an aligned part of a list (one per CTA of the cluster): (m, L) stay in sML and
             // O^T in registers for the cluster merge after the loop
         } else {
@@ -703,89 +799,36 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         load_q_frags<H>(p, t, cw, lane, bq);
     }
     if (failed) *sAbort = 1;  // producers still waiting for a free stage give up
-    if (p.splits > 1) {
+    if constexpr (CL) {
         // ================================================================ cluster merge
         // The list of token t is cut into p.splits aligned parts, one per CTA of a thread-block
-        // cluster (rank = part).  After every CTA has left its loop (so stage memory is free),
-        // each pushes its per-head (m, L) to all CTAs and its unnormalised O^T fragments for
-        // dims [k*ds, (k+1)*ds) to CTA k (ds = 512 / splits), into stage memory; after a second
-        // cluster barrier CTA k weights the parts by 2^(m_j - M) / sum_j L_j 2^(m_j - M) and
-        // stores its dims.  No CTA touches another's memory after that barrier.
-        const int ns = p.splits;  // 2, 4 or 8 (host plan): ds below is a multiple of 8
-        const int rank = static_cast<int>(blockIdx.x) % ns;
-        const int ds = kDV / ns;
-        const uint32_t recv = sKV;                            // [ns][H][ds] fp32
-        const uint32_t recv_ml = sKV + H * kDV * 4;           // [ns][2H] fp32
+        // cluster (rank = part).  Every warp is past the end-of-segment barriers, so no warp
+        // reads the stages any more: O^T and (m, L) go to this CTA's own stage memory, and after
+        // a cluster barrier every thread of the CTA pulls and merges its share of the output
+        // (cluster_pull_merge).  The second barrier keeps each CTA's memory alive until the
+        // other CTAs have read it.
         const bool have = nb > 0 && !failed;
-        ptx::cluster_sync();
+        float* loc = reinterpret_cast<float*>(smem + L::kOffKV);  // [H][kSmLocStride], then [H][2]
         if (wtid < H) {
-            const float m = have ? sML[wtid] : -CUDART_INF_F;
-            const float l = have ? sML[H + wtid] : 0.f;
-            for (int k = 0; k < ns; ++k) {
-                ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + wtid) * 4, k), m);
-                ptx::st_shared_cluster_f32(ptx::map_shared_rank(recv_ml + (rank * 2 * H + H + wtid) * 4, k), l);
-            }
+            loc[H * kSmLocStride + 2 * wtid] = have ? sML[wtid] : -CUDART_INF_F;
+            loc[H * kSmLocStride + 2 * wtid + 1] = have ? sML[H + wtid] : 0.f;
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
+            const int d = 128 * cw + 16 * mt + g;
 #pragma unroll
-            for (int hi = 0; hi < 2; ++hi) {
-                const int d = 128 * cw + 16 * mt + g + 8 * hi;
-                const int k = d / ds;
-                const int dd = d - k * ds;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int h = nt * 8 + 2 * tq + e;
-                        const uint32_t la = recv + static_cast<uint32_t>(((rank * H + h) * ds + dd) * 4);
-                        ptx::st_shared_cluster_f32(ptx::map_shared_rank(la, k), have ? o[mt][nt][2 * hi + e] : 0.f);
-                    }
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                const int h = nt * 8 + 2 * tq;
+                loc[h * kSmLocStride + d] = have ? o[mt][nt][0] : 0.f;
+                loc[(h + 1) * kSmLocStride + d] = have ? o[mt][nt][1] : 0.f;
+                loc[h * kSmLocStride + d + 8] = have ? o[mt][nt][2] : 0.f;
+                loc[(h + 1) * kSmLocStride + d + 8] = have ? o[mt][nt][3] : 0.f;
             }
         }
         ptx::cluster_sync();
-        const float* rml = reinterpret_cast<const float*>(smem + H * kDV * 4);
-        const float* rcv = reinterpret_cast<const float*>(smem);
-        float* mW = reinterpret_cast<float*>(smem + L::kOffMrg);
-        if (wtid < H) {
-            float M = -CUDART_INF_F;
-            for (int j = 0; j < ns; ++j) M = fmaxf(M, rml[j * 2 * H + wtid]);
-            float Lt = 0.f;
-            for (int j = 0; j < ns; ++j) {
-                const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
-                if (mj != -CUDART_INF_F && lj > 0.f) Lt += lj * ptx::ex2_approx(mj - M);
-            }
-            const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
-            for (int j = 0; j < ns; ++j) {
-                const float mj = rml[j * 2 * H + wtid], lj = rml[j * 2 * H + H + wtid];
-                mW[j * H + wtid] = (mj != -CUDART_INF_F && lj > 0.f) ? ptx::ex2_approx(mj - M) * inv : 0.f;
-            }
-            if (rank == 0)
-                p.lse[static_cast<int64_t>(t) * H + wtid] =
-                    Lt > 0.f ? (M + log2f(Lt)) * 0.69314718055994531f : -CUDART_INF_F;
-        }
-        ptx::named_bar_sync(1, 128);
-        // eight dims of one head per item, stored as one 16-byte vector
-        const int per_head = ds / 8;
-        for (int it = wtid; it < H * per_head; it += 128) {
-            const int hh = it / per_head;
-            const int dd = (it % per_head) * 8;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < ns; ++j) {
-                const float w = mW[j * H + hh];
-                const float4 lo = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd);
-                const float4 hv = *reinterpret_cast<const float4*>(rcv + (j * H + hh) * ds + dd + 4);
-                acc[0] += w * lo.x; acc[1] += w * lo.y; acc[2] += w * lo.z; acc[3] += w * lo.w;
-                acc[4] += w * hv.x; acc[5] += w * hv.y; acc[6] += w * hv.z; acc[7] += w * hv.w;
-            }
-            uint4 packed;
-            packed.x = pack_bf16x2(acc[0], acc[1]);
-            packed.y = pack_bf16x2(acc[2], acc[3]);
-            packed.z = pack_bf16x2(acc[4], acc[5]);
-            packed.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * H + hh) * kDV + rank * ds + dd) = packed;
-        }
+        cluster_pull_merge<H>(p, t, sKV, p.splits, static_cast<int>(blockIdx.x) % p.splits);
+        __syncwarp();
+        ptx::cluster_sync();
         return;
     }
     if (p.part == nullptr) return;  // every list lay within one CTA
