@@ -306,21 +306,27 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int
                 for (int i = 0; i < kPerWarp; ++i) {
                     const int r = pw + kWarps * i;
                     if (r < kSmRows) {
+                        // lane l converts dims [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8): each of the
+                        // two stores below then writes 512 contiguous bytes, without bank conflicts
+                        // (16 consecutive dims per lane made every store two-way conflicted: 256 of
+                        // ~1600 shared-memory wavefronts per block, measured with ncu)
                         const uint32_t rr = rs + r * kFp8RowBytes;
-                        const uint4 lat = ptx::ld_shared_v4(rr + 16 * lane);
-                        const float scl = ptx::ld_shared_f32(rr + 512 + 4 * (lane >> 3));
+                        const uint2 la = ptx::ld_shared_v2(rr + 8 * lane);
+                        const uint2 lb = ptx::ld_shared_v2(rr + 256 + 8 * lane);
+                        const float sa = ptx::ld_shared_f32(rr + 512 + 4 * (lane >> 4));
+                        const float sb = ptx::ld_shared_f32(rr + 512 + 4 * (2 + (lane >> 4)));
                         uint4 v0, v1;
-                        v0.x = ptx::e4m3x2_scaled_bf16x2(lat.x & 0xFFFFu, scl);
-                        v0.y = ptx::e4m3x2_scaled_bf16x2(lat.x >> 16, scl);
-                        v0.z = ptx::e4m3x2_scaled_bf16x2(lat.y & 0xFFFFu, scl);
-                        v0.w = ptx::e4m3x2_scaled_bf16x2(lat.y >> 16, scl);
-                        v1.x = ptx::e4m3x2_scaled_bf16x2(lat.z & 0xFFFFu, scl);
-                        v1.y = ptx::e4m3x2_scaled_bf16x2(lat.z >> 16, scl);
-                        v1.z = ptx::e4m3x2_scaled_bf16x2(lat.w & 0xFFFFu, scl);
-                        v1.w = ptx::e4m3x2_scaled_bf16x2(lat.w >> 16, scl);
+                        v0.x = ptx::e4m3x2_scaled_bf16x2(la.x & 0xFFFFu, sa);
+                        v0.y = ptx::e4m3x2_scaled_bf16x2(la.x >> 16, sa);
+                        v0.z = ptx::e4m3x2_scaled_bf16x2(la.y & 0xFFFFu, sa);
+                        v0.w = ptx::e4m3x2_scaled_bf16x2(la.y >> 16, sa);
+                        v1.x = ptx::e4m3x2_scaled_bf16x2(lb.x & 0xFFFFu, sb);
+                        v1.y = ptx::e4m3x2_scaled_bf16x2(lb.x >> 16, sb);
+                        v1.z = ptx::e4m3x2_scaled_bf16x2(lb.y & 0xFFFFu, sb);
+                        v1.w = ptx::e4m3x2_scaled_bf16x2(lb.y >> 16, sb);
                         const uint32_t rd = st + r * kSmRowStride;
-                        ptx::st_shared_v4(rd + (2 * lane) * 16, v0);      // dims 16 lane .. +7
-                        ptx::st_shared_v4(rd + (2 * lane + 1) * 16, v1);  // dims 16 lane + 8 .. +15
+                        ptx::st_shared_v4(rd + lane * 16, v0);         // dims 8 lane .. +7
+                        ptx::st_shared_v4(rd + (32 + lane) * 16, v1);  // dims 256 + 8 lane .. +7
                         if (lane < 8) ptx::st_shared_v4(rd + (64 + lane) * 16, ptx::ld_shared_v4(rr + 528 + 16 * lane));
                     }
                 }
