@@ -15,7 +15,7 @@
 //                                                through ldmatrix.trans.
 //
 // Rows arrive in 32-row stages (six in flight at 8 heads, five at 16; fp8 rows through a raw
-// ring, see small_gather) gathered by seven producer warps.  Each compute warp takes eight of the
+// ring, see small_gather) gathered by seven producer warps (eight for fp8).  Each compute warp takes eight of the
 // block's rows for the softmax: masking, a running max per head in log2 units with conditional
 // rescaling (only when the max grows by more than 2^8), fp32 partial sums, P^T (bf16) to shared
 // memory.
@@ -43,8 +43,17 @@ constexpr int kSmStagesFp8 = 3;                                      // fp8 cach
 constexpr int kSmRawStages = 4;                                      // ... fed by a raw-row ring
 constexpr int kSmRawStageBytes = kSmRows * kFp8RowBytes;             // 20992
 constexpr int kSmComputeWarps = 4;
-constexpr int kSmThreads = 32 * (kProducerWarps + kSmComputeWarps);  // 352
-constexpr int kSmCompute0 = 32 * kProducerWarps;                     // first compute thread
+// Warp roles: producer warps first, then the four compute warps.  The fp8 cache takes eight
+// producers (each dequantises four rows of a block; 384 threads), bf16 seven (352 threads).
+// Measured on the four-sequence fp8 batch: 4.48 -> 4.40 ms with the eighth warp; rows
+// assigned so each SM sub-partition (warp % 4) dequantises eight rows, with one warp taking
+// eight, ran at 6.15 ms: the warp with the most rows sets the pace.
+template <int KVF>
+struct SmRoles {
+    static constexpr int kProducers = KVF == 1 ? 8 : kProducerWarps;
+    static constexpr int kThreads = 32 * (kProducers + kSmComputeWarps);
+    static constexpr int kCompute0 = 32 * kProducers;  // first compute thread
+};
 constexpr int kSmKSteps = kDQK / 16 / kSmComputeWarps;               // 9 k-steps per warp
 // Stage layout: row r at r * 1168 bytes (1152 + 16).  Consecutive rows then start four banks
 // apart, so the eight row addresses of every ldmatrix hit disjoint banks without a swizzle, and
@@ -163,7 +172,7 @@ __device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t add
 // lane 0 (with the expected bytes); fp8 -> all seven warps (one per thread).
 template <int KVF>
 __host__ __device__ constexpr int small_full_count() {
-    return KVF == 0 ? 32 * (kProducerWarps - 1) + 1 : 32 * kProducerWarps;
+    return KVF == 0 ? 32 * (kProducerWarps - 1) + 1 : 32 * SmRoles<1>::kProducers;
 }
 
 // KV row gather of the small-head kernel (producer warp pw), into NST stages of kSmRows
@@ -173,7 +182,7 @@ __host__ __device__ constexpr int small_full_count() {
 // compute warps read validity from shared memory after their wait.
 //   bf16: warp 6 takes rows [0, kSmBulkRows), one row per lane, one cp.async.bulk of 1152 bytes
 //         each; warps 0-5 take rows kSmBulkRows + pw + 6 i with 16-byte cp.async.
-//   fp8:  warps 0-6 take rows pw + 7 i.  Raw 656-byte rows are copied with cp.async into a ring
+//   fp8:  warps 0-7 take rows pw + 8 i.  Raw 656-byte rows are copied with cp.async into a ring
 //         of kSmRawStages blocks, kSmRawStages - 1 blocks ahead of use (about 63 KB in flight);
 //         then each lane dequantises 16 latent bytes of a row with its tile scale (e4m3 -> f16
 //         exactly, x scale in fp32, -> bf16 round to nearest even) into the bf16 operand stage,
@@ -187,10 +196,10 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int
     // entry is first read kAhead blocks after its load was issued.
     constexpr int kAhead = 8;
     constexpr int kRow0 = KVF == 0 ? kSmBulkRows : 0;
-    constexpr int kWarps = KVF == 0 ? kProducerWarps - 1 : kProducerWarps;
+    constexpr int kWarps = KVF == 0 ? kProducerWarps - 1 : SmRoles<1>::kProducers;
     constexpr int kPerWarp = (kSmRows - kRow0 + kWarps - 1) / kWarps;
     constexpr uint32_t kBulkMask = kSmBulkRows >= 32 ? 0xffffffffu : ((1u << kSmBulkRows) - 1u);
-    const bool mask_warp = pw == kProducerWarps - 1;
+    const bool mask_warp = pw == SmRoles<KVF>::kProducers - 1;
     // fetch cursor: token ft, first list entry fj of the next block to fetch (blocks x0, x0+1, ...)
     const int kpad = p.nblk * kSmRows;
     int ft = static_cast<int>(x0 / p.nblk);
@@ -374,7 +383,7 @@ template <int H>
 __device__ __forceinline__ void cluster_pull_merge(const FwdParams& p, int t, uint32_t loc, int ns, int rank) {
     const int ds = kDV / ns;
     const int per_head = ds / 8;
-    for (int it = threadIdx.x; it < H * per_head; it += kSmThreads) {
+    for (int it = threadIdx.x; it < H * per_head; it += blockDim.x) {
         const int hh = it / per_head;
         const int dd = rank * ds + (it % per_head) * 8;
         // (m, L) of every part, and the first four parts' pieces, in flight together
@@ -441,7 +450,9 @@ __device__ __forceinline__ void cluster_pull_merge(const FwdParams& p, int t, ui
 // limit of 11 warps per SM (168), and the merge code alone moved their allocation into spills
 // (an 80 -> 83 us loss on a 16-head launch that never merges).
 template <int H, int KVF, bool CL>
-__global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(SmRoles<KVF>::kThreads, 1) sparse_mla_fwd_small_kernel(const FwdParams p) {
+    constexpr int kSmCompute0 = SmRoles<KVF>::kCompute0;
+    constexpr int kSmProducers = SmRoles<KVF>::kProducers;
     using L = SmallLayout<H, KVF>;
     constexpr int NT = L::kNT;
     constexpr int NST = L::kStages;
@@ -495,7 +506,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
     ptx::grid_launch_dependents();
     __syncthreads();
 
-    if (warp < kProducerWarps) {
+    if (warp < kSmProducers) {
         // ================================================================ producers
         small_gather<KVF, NST>(p, x0, nb, warp, lane, sKV, sbase + L::kOffRaw, bar_full0, bar_empty0,
                                sbase + L::kOffMask, sAbort);
@@ -509,7 +520,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sparse_mla_fwd_small_kernel(con
         return;
     }
     // ==================================================================== compute warps
-    const int cw = warp - kProducerWarps;   // 0..3
+    const int cw = warp - kSmProducers;   // 0..3
     const int wtid = threadIdx.x - kSmCompute0;
     const int g = lane >> 2;                // MMA fragment row group
     const int tq = lane & 3;                // MMA fragment column pair
