@@ -53,6 +53,9 @@ def _load():
         lib.oracle_decode_row.restype = None
         lib.oracle_decode_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                           ctypes.c_void_p]
+        lib.oracle_merge.restype = ctypes.c_int
+        lib.oracle_merge.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                     ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -139,3 +142,30 @@ def decode_row(kv, kv_format: str, slot: int) -> np.ndarray:
     _load().oracle_decode_row(kvn.ctypes.data, KV_FORMATS[kv_format], int(slot),
                               row.ctypes.data)
     return row
+
+
+def merge(o_parts, lse_parts) -> Tuple[np.ndarray, np.ndarray]:
+    """Exact merge of the partial results of a split list (the C file's oracle_merge), fp64.
+
+    o_parts    [n, ..., 512]: a torch bf16 tensor (or uint16 bf16 bit patterns), or fp64 values
+    lse_parts  [n, ...] natural-log LSE of each part (-inf = empty part), any float type
+    returns    out [..., 512] float64 and lse [...] float64
+    """
+    lib = _load()
+    ln = np.ascontiguousarray(_as_np(lse_parts).astype(np.float64))
+    n = ln.shape[0]
+    lead = ln.shape[1:]
+    rows = int(np.prod(lead)) if len(lead) else 1
+    on = _as_np(o_parts)
+    if on.dtype == np.uint16 or on.dtype == np.int16:
+        on, bf16 = np.ascontiguousarray(on.view(np.uint16)), 1
+    else:
+        on, bf16 = np.ascontiguousarray(on.astype(np.float64)), 0
+    assert on.shape == (n,) + tuple(lead) + (512,), (on.shape, ln.shape)
+    out = np.empty(tuple(lead) + (512,), dtype=np.float64)
+    lse = np.empty(lead, dtype=np.float64)
+    rc = lib.oracle_merge(on.ctypes.data, bf16, ln.ctypes.data, n, rows, out.ctypes.data,
+                          lse.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out, lse

@@ -200,3 +200,58 @@ int oracle_sparse_mla_fwd(const uint16_t *q, const void *kv, int kv_format,
     }
     return failed ? 2 : 0;
 }
+
+/*
+ * Merge of the partial results of one list split into parts: the "DCP merge"
+ * that consumes out and lse (vLLM PR #60220, Details: the output "is consumed
+ * by the v_up projection or the DCP merge"; vLLM PR #64510, Details: heads
+ * gathered by DCP).  The pages do not write the merge.  Read as the exact
+ * combination of softmax results over disjoint parts of one list, each part p
+ * given as its normalised O_p and natural-log LSE_p (what the forward returns):
+ *
+ *   M        = max_p LSE_p
+ *   LSE      = M + ln sum_p exp(LSE_p - M)
+ *   O[d]     = sum_p exp(LSE_p - LSE) * O_p[d]
+ *   a part with LSE_p = -inf is empty and weighs 0; no non-empty part: O = 0,
+ *   LSE = -inf.
+ *
+ * o_parts   [n][rows][512], fp64 (o_bf16 = 0) or bf16 bit patterns (o_bf16 = 1)
+ * lse_parts [n][rows] fp64
+ * out       [rows][512] fp64;  lse [rows] fp64
+ * Returns 0, or 1 for n < 1 or rows < 0.
+ */
+int oracle_merge(const void *o_parts, int o_bf16, const double *lse_parts, int n, int64_t rows,
+                 double *out, double *lse) {
+    if (n < 1 || rows < 0) return 1;
+    const double *of = (const double *)o_parts;
+    const uint16_t *ob = (const uint16_t *)o_parts;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int p = 0; p < n; ++p)
+            if (lse_parts[p * rows + r] > m) m = lse_parts[p * rows + r];
+        double *o = out + r * ORACLE_DV;
+        if (m == -INFINITY) {
+            for (int d = 0; d < ORACLE_DV; ++d) o[d] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int p = 0; p < n; ++p) {
+            double l = lse_parts[p * rows + r];
+            if (l != -INFINITY) sum += exp(l - m);
+        }
+        double total = m + log(sum);
+        for (int d = 0; d < ORACLE_DV; ++d) o[d] = 0.0;
+        for (int p = 0; p < n; ++p) {
+            double l = lse_parts[p * rows + r];
+            if (l == -INFINITY) continue;
+            double w = exp(l - total);
+            int64_t base = (p * rows + r) * ORACLE_DV;
+            for (int d = 0; d < ORACLE_DV; ++d)
+                o[d] += w * (o_bf16 ? bf16_bits_to_double(ob[base + d]) : of[base + d]);
+        }
+        lse[r] = total;
+    }
+    return 0;
+}

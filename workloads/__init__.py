@@ -1,7 +1,7 @@
 """Seeded synthetic workloads for the token-sparse MLA forward.
 
 This package only draws random inputs (queries, a paged latent KV cache, block
-tables and per-token top-k slot lists) and packs them into the layouts the
+tables, per-token top-k slot lists, and the parts of split lists) and packs them into the layouts the
 kernel and the oracle read.  It contains none of the attention arithmetic, so
 both sides of every parity check can take their inputs from here.
 """
@@ -10,9 +10,11 @@ from .configs import CONFIGS, WorkloadConfig, config_by_name
 from .generators import (
     Workload,
     gathered_bytes,
+    make_merge_parts,
     make_workload,
     pad_heads,
     quantize_fp8_rows,
+    split_lists,
 )
 
 __all__ = [
@@ -21,7 +23,9 @@ __all__ = [
     "config_by_name",
     "Workload",
     "gathered_bytes",
+    "make_merge_parts",
     "make_workload",
     "pad_heads",
     "quantize_fp8_rows",
+    "split_lists",
 ]

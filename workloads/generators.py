@@ -210,3 +210,35 @@ def gathered_bytes(indices: torch.Tensor, num_slots: int, row_bytes: int) -> int
     """Algorithmic gathered KV bytes: valid list entries x row bytes."""
     valid = (indices >= 0) & (indices < num_slots)
     return int(valid.sum().item()) * int(row_bytes)
+
+
+def split_lists(indices: torch.Tensor, n_parts: int) -> list:
+    """Split every token's list into n_parts contiguous column ranges (the parts a decode-
+    context-parallel split gives each rank): part p keeps columns [p*topk//n, (p+1)*topk//n)
+    and holds -1 everywhere else, so the parts' valid entries are disjoint and their union is
+    the list."""
+    topk = indices.shape[1]
+    parts = []
+    for p in range(n_parts):
+        a, b = p * topk // n_parts, (p + 1) * topk // n_parts
+        part = torch.full_like(indices, -1)
+        part[:, a:b] = indices[:, a:b]
+        parts.append(part)
+    return parts
+
+
+def make_merge_parts(n_parts: int, T: int, h: int, seed: int = 6000, p_empty: float = 0.05):
+    """Synthetic partial results of lists split into n_parts, in the layout the merge reads:
+    o_parts [n, T, h, 512] bf16 = bf16(N(0, 1) * 0.1) (an attention output is a convex mix of
+    value rows, smaller than the rows themselves) and lse_parts [n, T, h] fp32 = N(6, 1)
+    (about ln 2048 / n), each part empty (LSE = -inf, O = 0) with probability p_empty, and
+    the first row of every token empty in all parts."""
+    g = _gen(seed, 11)
+    o = (torch.randn(n_parts, T, h, 512, generator=g) * 0.1).to(torch.bfloat16)
+    lse = torch.randn(n_parts, T, h, generator=g) + 6.0
+    empty = torch.rand(n_parts, T, h, generator=g) < p_empty
+    if T > 0:
+        empty[:, :, 0] = True
+    lse[empty] = float("-inf")
+    o[empty] = 0
+    return o, lse.to(torch.float32)
