@@ -14,6 +14,8 @@ step never finds its rows in L2 from the previous steps.
 
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores on the
 same workload, a bounded number of tokens per step.
+--workload dcp_merge times sparse_mla_merge instead: the combine of 4 split-list
+partial results per row at the fp8 batch's shape (T = 32768, h = 8).
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path shards by query token with no exchange), weak scaling.
 """
@@ -34,7 +36,7 @@ sys.path.insert(0, str(ROOT))
 
 import torch  # noqa: E402
 
-from workloads import config_by_name, gathered_bytes, make_workload, pad_heads  # noqa: E402
+from workloads import config_by_name, gathered_bytes, make_merge_parts, make_workload, pad_heads  # noqa: E402
 
 METRIC = "query-tokens/s and gathered-KV HBM GB/s (fraction of roofline) at topk=2048"
 UNIT = "query-tokens/s"
@@ -388,6 +390,137 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+# ---- the DCP merge (combine of split-list partial results), on the fp8 batch's shape
+MERGE_SHAPE = {"n_parts": 4, "T": 32768, "h": 8}
+
+
+def merge_bytes(lse_parts: torch.Tensor) -> int:
+    """Algorithmic bytes of one merge: every LSE and the O (bf16) of every non-empty part read
+    (an empty part's O is never needed), O and LSE written."""
+    n = lse_parts.shape[0]
+    rows = lse_parts[0].numel()
+    nonempty = int((lse_parts != float("-inf")).sum().item())
+    return nonempty * 512 * 2 + n * rows * 4 + rows * (512 * 2 + 4)
+
+
+def merge_config(args, nbytes: int) -> dict:
+    return {"workload": "dcp_merge", **MERGE_SHAPE,
+            "parts": "synthetic partials: O ~ bf16(N(0, 0.1)), LSE ~ N(6, 1); each part empty with "
+                     "probability 0.05, and head 0 of every token empty in all parts",
+            "launch": "CUDA graph of consecutive steps" if args.launch == "graph" else "eager launches",
+            "l2": f"{nbytes / 1e9:.2f} GB read and written per step > 2 x L2"}
+
+
+def run_merge(args, rank, world, local_rank):
+    import token_sparse_mla_gb300 as smla
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    n, T, H = MERGE_SHAPE["n_parts"], MERGE_SHAPE["T"], MERGE_SHAPE["h"]
+    o_h, l_h = make_merge_parts(n, T, H, seed=6000 + 7919 * rank)
+    o_d, l_d = o_h.to(dev), l_h.to(dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        smla.sparse_mla_merge(o_d, l_d, out=out, lse=lse, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    smla.sync_status(stream)
+    glen = 16
+    graph = None
+    if args.launch == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(glen):
+                step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    steps = max(glen, (args.steps // glen) * glen) if graph is not None else args.steps
+
+    def timed():
+        if graph is not None:
+            for _ in range(steps // glen):
+                graph.replay()
+        else:
+            for _ in range(steps):
+                step()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        timed()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        timed()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.stop()
+    smla.sync_status(stream)
+    t_dev = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    per_launch = t_dev / steps
+    nbytes = merge_bytes(l_h)
+    achieved = nbytes / per_launch / 1e9
+    peaks = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        tok = 256
+        t0 = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t0 < args.cpu_seconds or k == 0:
+            oracle.merge(o_h[:, :tok], l_h[:, :tok])
+            k += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": k * tok / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"the first {tok} query tokens' rows, merged {k} times in {el:.1f} s"}
+    line = {
+        "metric": METRIC, "value": world * T * steps / t_dev, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_launch * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": merge_config(args, nbytes), "merged_gbps": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("dcp_merge", H, False),
+                     "peak_source": peaks["source"] + " (copy bandwidth)",
+                     "per_launch_algorithmic_bytes": nbytes, "kernel": "sparse_mla_merge_kernel"},
+        "cpu_baseline": cpu, "e2e": None, "clocks": clocks.summary(), "gpu_launches": steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_merge_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n, T, H = MERGE_SHAPE["n_parts"], MERGE_SHAPE["T"], MERGE_SHAPE["h"]
+    o_h, l_h = make_merge_parts(n, T, H, seed=6000)
+    tok = 256
+    for _ in range(args.warmup):
+        oracle.merge(o_h[:, :8], l_h[:, :8])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.merge(o_h[:, :tok], l_h[:, :tok])
+    el = time.perf_counter() - t0
+    value = tok * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": merge_config(args, merge_bytes(l_h)),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{tok} query tokens' rows per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +543,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_setup(args)
-    if args.impl == "reference":
+    if args.workload == "dcp_merge":
+        (run_merge_reference(args, rank, world) if args.impl == "reference"
+         else run_merge(args, rank, world, local_rank))
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)

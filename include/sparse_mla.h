@@ -138,6 +138,32 @@ smla_status sparse_mla_fwd_noalloc(const void* q, const void* kv_cache, const in
                                    int32_t splits, void* stream);
 
 /*
+ * sparse_mla_merge -- merge the partial results of token lists that were split
+ * into parts (the DCP merge: with decode context parallelism each rank runs the
+ * forward over its part of every list; vLLM PR #60220, Details: out and lse are
+ * "consumed by the v_up projection or the DCP merge"; vLLM PR #64510, Details:
+ * heads gathered by DCP).  The pages do not write the merge; it is the exact
+ * combination of softmax results over disjoint parts of one list.  Per row
+ * (token, head), with O_p and LSE_p what sparse_mla_fwd returns for part p:
+ *     M = max_p LSE_p,  LSE = M + ln sum_p exp(LSE_p - M),
+ *     O = sum_p exp(LSE_p - LSE) * O_p
+ * A part with LSE_p = -inf (an empty part) weighs nothing; a row whose parts
+ * are all empty gets O = 0, LSE = -inf.  fp32 arithmetic, O rounded to bf16.
+ *   o_parts    device, [n_parts, T, h, 512] bf16, contiguous, 16-byte aligned
+ *   lse_parts  device, [n_parts, T, h] fp32 natural-log LSE, 4-byte aligned
+ *   n_parts    1 .. 16
+ *   T, h       rows = T * h (any h >= 1); T = 0 is a no-op
+ *   out        device, [T, h, 512] bf16, caller-owned, 16-byte aligned; must
+ *              not overlap o_parts
+ *   lse        device, [T, h] fp32, caller-owned, 4-byte aligned
+ * Allocates nothing; asynchronous on `stream`.  Errors: SMLA_ERR_INVALID_ARG for
+ * a bad n_parts, T, h, null pointer or alignment (nothing is launched);
+ * SMLA_ERR_CUDA if the launch fails.
+ */
+smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_t n_parts, int32_t T,
+                             int32_t h, void* out, float* lse, void* stream);
+
+/*
  * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the
  * per-step inputs and outputs, for callers whose q/indices live in host memory.
  * It queues on `stream`: copies of q_host and indices_host into `workspace`,

@@ -1,4 +1,5 @@
-"""The merge of split-list partial results (the DCP merge): oracle pins on the CPU.
+"""The merge of split-list partial results (the DCP merge): oracle pins on the CPU, C-ABI
+validation, and GPU parity through sparse_mla_merge.
 
 A token's top-k list split into disjoint parts, each part's (O_p, LSE_p) as the forward
 returns them, merged: the result must be the forward of the whole list (vLLM PR #60220,
@@ -150,3 +151,93 @@ def test_merge_mutants_fail_a_pin(tmp_path, monkeypatch, name):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"no pin caught the mutant {name}"
+
+
+# ----------------------------------------------------------------------------- C ABI (no GPU)
+
+@pytest.fixture(scope="module")
+def lib():
+    import token_sparse_mla_gb300 as smla
+    return smla.library()
+
+
+@pytest.mark.parametrize("n,T,h,status", [(0, 4, 8, 1), (17, 4, 8, 1), (4, -1, 8, 1), (4, 4, 0, 1)])
+def test_merge_rejects_bad_arguments(lib, n, T, h, status):
+    buf = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    assert lib.sparse_mla_merge(buf, buf, n, T, h, buf, buf, None) == status
+
+
+def test_merge_rejects_null_and_misaligned(lib):
+    good = ctypes.c_void_p(4096)
+    assert lib.sparse_mla_merge(None, good, 2, 4, 8, good, good, None) == 1
+    assert lib.sparse_mla_merge(ctypes.c_void_p(4104), good, 2, 4, 8, good, good, None) == 1
+    assert lib.sparse_mla_merge(good, good, 2, 4, 8, ctypes.c_void_p(4100), good, None) == 1
+
+
+def test_merge_zero_tokens_is_a_noop(lib):
+    assert lib.sparse_mla_merge(None, None, 2, 0, 8, None, None, None) == 0
+
+
+# ----------------------------------------------------------------------------- GPU parity
+
+DEV = "cuda:0"
+
+
+def _gpu_merge(o, l):
+    import token_sparse_mla_gb300 as smla
+    out, lse = smla.sparse_mla_merge(o.to(DEV), l.to(DEV))
+    smla.sync_status()
+    return out.cpu(), lse.cpu()
+
+
+def _assert_merge_parity(out, lse, ref_out, ref_lse, what):
+    o = out.float().double().numpy()
+    l = lse.double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(l), ~fin), f"{what}: -inf pattern"
+    assert np.all(o[~fin] == 0.0), f"{what}: empty rows must be 0"
+    # fp32 weights and sums, one bf16 rounding of the result
+    err = np.abs(o - ref_out)
+    assert np.all(err <= 1e-5 + 2.0 ** -8 * np.abs(ref_out)), f"{what}: O max err {err.max()}"
+    assert np.all(np.abs(l[fin] - ref_lse[fin]) <= 1e-5 * np.maximum(1.0, np.abs(ref_lse[fin]))), what
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n,T,h", [(1, 5, 8), (2, 3, 16), (4, 37, 8), (8, 9, 64), (16, 4, 32),
+                                   (3, 1, 1), (5, 301, 8)])
+def test_gpu_merge_matches_oracle(n, T, h):
+    o, l = make_merge_parts(n, T, h, seed=100 + n * 7 + T)
+    out, lse = _gpu_merge(o, l)
+    ref_out, ref_lse = oracle.merge(o, l)
+    _assert_merge_parity(out, lse, ref_out, ref_lse, f"n={n} T={T} h={h}")
+
+
+@pytest.mark.gpu
+def test_gpu_merge_single_part_is_exact():
+    o, l = make_merge_parts(1, 7, 8, seed=5)
+    out, lse = _gpu_merge(o, l)
+    assert torch.equal(out, o[0]) and torch.equal(lse, l[0])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,kw,n", [("decode_bf16", {"n_seq": 4}, 4), ("sweep", {"h": 16, "n_seq": 3}, 2),
+                                        ("sweep", {"h": 64, "n_seq": 2}, 8), ("fp8_mixed", {"n_seq": 1, "n_tokens": 6}, 3)])
+def test_gpu_split_forward_then_merge_equals_whole_forward(name, kw, n):
+    """The forward on each part of the lists, merged on the GPU, against the forward of the
+    whole lists: the oracle's, and the GPU's own."""
+    import token_sparse_mla_gb300 as smla
+    from tests.parity import assert_parity
+    w = make_workload(name, **kw)
+    q, kv = w.q.to(DEV), w.kv.to(DEV)
+    o_parts, l_parts = [], []
+    for part in split_lists(w.indices, n):
+        o, l = smla.sparse_mla_fwd(q, kv, part.to(DEV), w.scale, kv_format=w.kv_format)
+        o_parts.append(o)
+        l_parts.append(l)
+    out, lse = smla.sparse_mla_merge(torch.stack(o_parts), torch.stack(l_parts))
+    full_out, full_lse = smla.sparse_mla_fwd(q, kv, w.indices.to(DEV), w.scale, kv_format=w.kv_format)
+    smla.sync_status()
+    ref_out, ref_lse = oracle.sparse_mla_fwd(w.q, w.kv, w.indices, w.scale, kv_format=w.kv_format)
+    assert_parity(out.cpu(), lse.cpu(), ref_out, ref_lse, f"{name} merged")
+    # against the unsplit GPU forward: both within the tolerance of the same reference
+    assert_parity(full_out.cpu(), full_lse.cpu(), ref_out, ref_lse, f"{name} whole")

@@ -47,6 +47,8 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_fwd_noalloc.restype = ctypes.c_int
     lib.sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_merge.restype = ctypes.c_int
+    lib.sparse_mla_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.sparse_mla_host_workspace_bytes.restype = sz
     lib.sparse_mla_host_workspace_bytes.argtypes = [i32, i32, i32]
     lib.sparse_mla_fwd_host.restype = ctypes.c_int
@@ -155,6 +157,38 @@ def sparse_mla_fwd_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: tor
         q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
         KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
         _stream_handle(stream)))
+
+
+def sparse_mla_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
+                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Merge the partial results of split token lists (the DCP merge; include/sparse_mla.h).
+
+    o_parts [n, T, h, 512] bf16 and lse_parts [n, T, h] fp32 are what sparse_mla_fwd returned
+    for each of the n parts (LSE -inf = empty part); returns out [T, h, 512] bf16 and
+    lse [T, h] fp32 of the whole lists.
+    """
+    if o_parts.dim() != 4 or o_parts.shape[-1] != D_V or o_parts.dtype != torch.bfloat16:
+        raise ValueError("o_parts must be [n, T, h, 512] bf16")
+    n, T, h = int(o_parts.shape[0]), int(o_parts.shape[1]), int(o_parts.shape[2])
+    if lse_parts.shape != (n, T, h) or lse_parts.dtype != torch.float32:
+        raise ValueError("lse_parts must be [n, T, h] fp32")
+    for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((T, h), dtype=torch.float32, device=o_parts.device)
+    if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
+    if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
+    _check(library().sparse_mla_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, T, h,
+                                      out.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
+    return out, lse
 
 
 def host_workspace_bytes(T: int, h: int, topk: int) -> int:

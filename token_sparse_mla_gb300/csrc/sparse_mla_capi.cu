@@ -14,6 +14,7 @@
 #include "sparse_mla.h"
 #include "sparse_mla_kernel.cuh"
 #include "sparse_mla_small_kernel.cuh"
+#include "sparse_mla_merge.cuh"
 
 namespace {
 
@@ -542,5 +543,55 @@ smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t k
 const char* sparse_mla_last_error(void) { return g_last_error; }
 
 int32_t sparse_mla_version(void) { return kVersion; }
+
+
+smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_t n_parts, int32_t T,
+                             int32_t h, void* out, float* lse, void* stream) {
+    if (n_parts < 1 || n_parts > smla::kMergeMaxParts)
+        return fail(SMLA_ERR_INVALID_ARG, "n_parts must be in [1, %d] (got %d)", smla::kMergeMaxParts, n_parts);
+    if (T < 0 || h < 1) return fail(SMLA_ERR_INVALID_ARG, "T must be >= 0 and h >= 1 (got %d, %d)", T, h);
+    if (T == 0) return SMLA_OK;
+    if (!o_parts || !lse_parts || !out || !lse) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(o_parts, 16) || !aligned(out, 16))
+        return fail(SMLA_ERR_INVALID_ARG, "o_parts and out must be 16-byte aligned");
+    if (!aligned(lse_parts, 4) || !aligned(lse, 4))
+        return fail(SMLA_ERR_INVALID_ARG, "lse_parts and lse must be 4-byte aligned");
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    smla_status st = device_state(&dev, &ds);
+    if (st != SMLA_OK) return st;
+    smla::MergeParams mp;
+    mp.o_parts = static_cast<const __nv_bfloat16*>(o_parts);
+    mp.lse_parts = lse_parts;
+    mp.out = static_cast<__nv_bfloat16*>(out);
+    mp.lse = lse;
+    mp.rows = static_cast<int64_t>(T) * h;
+    mp.n = n_parts;
+    // one warp per row, eight rows per CTA; a grid of the CTAs that fit on the device at once
+    // strides over the rows (their count is asked of the runtime once per device)
+    static int resident[kMaxDevices];
+    if (resident[dev] == 0) {
+        int per_sm = 0;
+        const cudaError_t oe =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, smla::sparse_mla_merge_kernel, smla::kMergeThreads, 0);
+        if (oe != cudaSuccess) return cuda_fail(oe, "occupancy of the merge kernel");
+        resident[dev] = per_sm > 0 ? per_sm : 1;
+    }
+    const int64_t want = (mp.rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(ds->num_sms) * resident[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
+    cfg.blockDim = dim3(smla::kMergeThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_merge_kernel, mp);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return SMLA_OK;
+}
 
 }  // extern "C"
