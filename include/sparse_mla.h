@@ -12,6 +12,8 @@
  *     LSE    = ln sum_j exp(s_j)                              (natural log, fp32)
  * An index list with no valid entry gives O = 0 and LSE = -inf.  Each list
  * entry is a separate softmax term (a slot listed twice counts twice).
+ * sparse_mla_merge combines the (O, LSE) of lists split into parts, e.g. over
+ * decode-context-parallel ranks, into the result of the whole lists.
  *
  * Sources (page title, section):
  *   vLLM PR #60220 "FlashMLA sparse: stage fp8 mixed-batch q/out in the
