@@ -56,6 +56,9 @@ def _load():
         lib.oracle_merge.restype = ctypes.c_int
         lib.oracle_merge.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_v_up.restype = ctypes.c_int
+        lib.oracle_v_up.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_void_p]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -169,3 +172,23 @@ def merge(o_parts, lse_parts) -> Tuple[np.ndarray, np.ndarray]:
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return out, lse
+
+
+def v_up(o, w) -> np.ndarray:
+    """The v_up projection (the C file's oracle_v_up), fp64.
+
+    o  [T, h, 512] bf16 (torch bf16 tensor or uint16 bit patterns)
+    w  [h, v, 512] bf16
+    returns y [T, h, v] float64
+    """
+    lib = _load()
+    on = _as_np(o, np.uint16)
+    wn = _as_np(w, np.uint16)
+    T, h, d = on.shape
+    hw, v, dw = wn.shape
+    assert d == 512 and dw == 512 and hw == h, (on.shape, wn.shape)
+    y = np.empty((T, h, v), dtype=np.float64)
+    rc = lib.oracle_v_up(on.ctypes.data, wn.ctypes.data, T, h, v, y.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return y

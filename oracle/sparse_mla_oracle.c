@@ -255,3 +255,34 @@ int oracle_merge(const void *o_parts, int o_bf16, const double *lse_parts, int n
     }
     return 0;
 }
+
+/*
+ * The v_up projection of the attention output (vLLM PR #60220, Details: the output "is
+ * consumed by the v_up projection or the DCP merge").  Shapes from the PR #55738 report,
+ * `_is_masked_mha_available` geometry table: kv_lora_rank 512 with v_head_dim 128
+ * (DeepSeek-V3.2) or 256 (GLM-5).  Per head h the 512-dim latent output goes through that
+ * head's value up-projection (512 -> v):
+ *
+ *   y[t, h, n] = sum_{k < 512} O[t, h, k] * W[h, n, k]        (n < v)
+ *
+ * O [T, h, 512] bf16, W [h, v, 512] bf16 (row n of head h: the 512 weights of output n; the
+ * pages give no layout, this one keeps each output's weights contiguous), y [T, h, v] fp64.
+ * Returns 0, or 1 for a bad size.
+ */
+int oracle_v_up(const uint16_t *o, const uint16_t *w, int64_t T, int h, int v, double *y) {
+    if (T < 0 || h < 1 || v < 1) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int hh = 0; hh < h; ++hh) {
+            const uint16_t *orow = o + (t * h + hh) * ORACLE_DV;
+            for (int n = 0; n < v; ++n) {
+                const uint16_t *wrow = w + ((int64_t)hh * v + n) * ORACLE_DV;
+                double acc = 0.0;
+                for (int k = 0; k < ORACLE_DV; ++k)
+                    acc += bf16_bits_to_double(orow[k]) * bf16_bits_to_double(wrow[k]);
+                y[(t * h + hh) * v + n] = acc;
+            }
+        }
+    }
+    return 0;
+}

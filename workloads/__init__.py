@@ -1,7 +1,7 @@
 """Seeded synthetic workloads for the token-sparse MLA forward.
 
 This package only draws random inputs (queries, a paged latent KV cache, block
-tables, per-token top-k slot lists, and the parts of split lists) and packs them into the layouts the
+tables, per-token top-k slot lists, the parts of split lists, value up-projection weights) and packs them into the layouts the
 kernel and the oracle read.  It contains none of the attention arithmetic, so
 both sides of every parity check can take their inputs from here.
 """
@@ -11,6 +11,7 @@ from .generators import (
     Workload,
     gathered_bytes,
     make_merge_parts,
+    make_v_up_weights,
     make_workload,
     pad_heads,
     quantize_fp8_rows,
@@ -24,6 +25,7 @@ __all__ = [
     "Workload",
     "gathered_bytes",
     "make_merge_parts",
+    "make_v_up_weights",
     "make_workload",
     "pad_heads",
     "quantize_fp8_rows",

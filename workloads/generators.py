@@ -242,3 +242,11 @@ def make_merge_parts(n_parts: int, T: int, h: int, seed: int = 6000, p_empty: fl
     lse[empty] = float("-inf")
     o[empty] = 0
     return o, lse.to(torch.float32)
+
+
+def make_v_up_weights(h: int, v: int, seed: int = 7000) -> torch.Tensor:
+    """Synthetic value up-projection weights, W [h, v, 512] bf16 = bf16(N(0, 1) / sqrt(512))
+    (row n of head h holds the 512 weights of output n), so the projected values keep about
+    the scale of the latent output."""
+    g = _gen(seed, 12)
+    return (torch.randn(h, v, 512, generator=g) * 512 ** -0.5).to(torch.bfloat16)
