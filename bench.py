@@ -15,7 +15,8 @@ step never finds its rows in L2 from the previous steps.
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores on the
 same workload, a bounded number of tokens per step.
 --workload dcp_merge times sparse_mla_merge instead: the combine of 4 split-list
-partial results per row at the fp8 batch's shape (T = 32768, h = 8).
+partial results per row at the fp8 batch's shape (T = 32768, h = 8); --workload
+v_up times sparse_mla_v_up (T = 32768, h = 8, v_head_dim 128).
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path shards by query token with no exchange), weak scaling.
 """
@@ -36,7 +37,8 @@ sys.path.insert(0, str(ROOT))
 
 import torch  # noqa: E402
 
-from workloads import config_by_name, gathered_bytes, make_merge_parts, make_workload, pad_heads  # noqa: E402
+from workloads import (config_by_name, gathered_bytes, make_merge_parts, make_v_up_weights,  # noqa: E402
+                       make_workload, pad_heads)
 
 METRIC = "query-tokens/s and gathered-KV HBM GB/s (fraction of roofline) at topk=2048"
 UNIT = "query-tokens/s"
@@ -521,6 +523,139 @@ def run_merge_reference(args, rank, world):
     }), flush=True)
 
 
+# ---- the v_up projection of the attention output (DeepSeek-V3.2 geometry, 8 heads)
+V_UP_SHAPE = {"T": 32768, "h": 8, "v": 128}
+
+
+def v_up_inputs(seed: int):
+    g = torch.Generator().manual_seed(seed)
+    o = (torch.randn(V_UP_SHAPE["T"], V_UP_SHAPE["h"], 512, generator=g) * 0.1).to(torch.bfloat16)
+    return o, make_v_up_weights(V_UP_SHAPE["h"], V_UP_SHAPE["v"], seed=seed)
+
+
+def v_up_bytes() -> int:
+    T, h, v = V_UP_SHAPE["T"], V_UP_SHAPE["h"], V_UP_SHAPE["v"]
+    return (T * h * 512 + h * v * 512 + T * h * v) * 2
+
+
+def v_up_config(args) -> dict:
+    return {"workload": "v_up", **V_UP_SHAPE,
+            "inputs": "O ~ bf16(N(0, 0.1)) [T, h, 512], W ~ bf16(N(0, 1) / sqrt(512)) [h, v, 512]",
+            "launch": "CUDA graph of consecutive steps" if args.launch == "graph" else "eager launches",
+            "l2": f"{v_up_bytes() / 1e6:.0f} MB read and written per step > 2 x L2"}
+
+
+def run_v_up(args, rank, world, local_rank):
+    import token_sparse_mla_gb300 as smla
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    T, H, V = V_UP_SHAPE["T"], V_UP_SHAPE["h"], V_UP_SHAPE["v"]
+    o_h, w_h = v_up_inputs(7100 + 7919 * rank)
+    o_d, w_d = o_h.to(dev), w_h.to(dev)
+    y = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        smla.sparse_mla_v_up(o_d, w_d, out=y, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    smla.sync_status(stream)
+    glen = 16
+    graph = None
+    if args.launch == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(glen):
+                step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    steps = max(glen, (args.steps // glen) * glen) if graph is not None else args.steps
+
+    def timed():
+        if graph is not None:
+            for _ in range(steps // glen):
+                graph.replay()
+        else:
+            for _ in range(steps):
+                step()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        timed()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        timed()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.stop()
+    smla.sync_status(stream)
+    t_dev = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    per_launch = t_dev / steps
+    nbytes = v_up_bytes()
+    achieved = nbytes / per_launch / 1e9
+    flops = 2.0 * T * H * 512 * V
+    peaks = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        tok = 512
+        t0 = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t0 < args.cpu_seconds or k == 0:
+            oracle.v_up(o_h[:tok], w_h)
+            k += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": k * tok / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"the first {tok} query tokens, projected {k} times in {el:.1f} s"}
+    line = {
+        "metric": METRIC, "value": world * T * steps / t_dev, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_launch * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": v_up_config(args), "tflops": flops / per_launch / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("v_up", H, False),
+                     "peak_source": peaks["source"] + " (copy bandwidth)",
+                     "per_launch_algorithmic_bytes": nbytes,
+                     "tensor_frac": flops / per_launch / 1e12 / peaks["bf16_tflops_sustained"],
+                     "kernel": "sparse_mla_v_up_kernel"},
+        "cpu_baseline": cpu, "e2e": None, "clocks": clocks.summary(), "gpu_launches": steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_v_up_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    o_h, w_h = v_up_inputs(7100)
+    tok = 512
+    for _ in range(args.warmup):
+        oracle.v_up(o_h[:8], w_h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.v_up(o_h[:tok], w_h)
+    el = time.perf_counter() - t0
+    value = tok * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": v_up_config(args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{tok} query tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -543,7 +678,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_setup(args)
-    if args.workload == "dcp_merge":
+    if args.workload == "v_up":
+        (run_v_up_reference(args, rank, world) if args.impl == "reference"
+         else run_v_up(args, rank, world, local_rank))
+    elif args.workload == "dcp_merge":
         (run_merge_reference(args, rank, world) if args.impl == "reference"
          else run_merge(args, rank, world, local_rank))
     elif args.impl == "reference":

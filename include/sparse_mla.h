@@ -13,7 +13,8 @@
  * An index list with no valid entry gives O = 0 and LSE = -inf.  Each list
  * entry is a separate softmax term (a slot listed twice counts twice).
  * sparse_mla_merge combines the (O, LSE) of lists split into parts, e.g. over
- * decode-context-parallel ranks, into the result of the whole lists.
+ * decode-context-parallel ranks, into the result of the whole lists, and
+ * sparse_mla_v_up applies the per-head value up-projection to O.
  *
  * Sources (page title, section):
  *   vLLM PR #60220 "FlashMLA sparse: stage fp8 mixed-batch q/out in the
@@ -164,6 +165,27 @@ smla_status sparse_mla_fwd_noalloc(const void* q, const void* kv_cache, const in
  */
 smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_t n_parts, int32_t T,
                              int32_t h, void* out, float* lse, void* stream);
+
+/*
+ * sparse_mla_v_up -- the v_up projection of the attention output: per head, the
+ * 512-dim latent output through that head's value up-projection (the output
+ * "is consumed by the v_up projection": vLLM PR #60220, Details; v_head_dim 128
+ * (DeepSeek-V3.2) or 256 (GLM-5) at kv_lora_rank 512: PR #55738 report, the
+ * `_is_masked_mha_available` geometry table):
+ *     y[t, h, n] = sum_{k < 512} o[t, h, k] * w[h, n, k]
+ * fp32 accumulation on the tcgen05 tensor cores, y rounded to bf16.
+ *   o     device, [T, h, 512] bf16 (what sparse_mla_fwd returns), 16-byte aligned
+ *   w     device, [h, v, 512] bf16: row n of head h holds the 512 weights of
+ *         output n (the pages give no layout); 16-byte aligned
+ *   v     128 or 256 (others: SMLA_ERR_UNSUPPORTED)
+ *   y     device, [T, h, v] bf16, caller-owned, 16-byte aligned
+ * T = 0 is a no-op.  Allocates nothing; asynchronous on `stream`.  Errors:
+ * SMLA_ERR_INVALID_ARG for a bad T or h, a null pointer or misalignment;
+ * SMLA_ERR_CUDA if a tensor map or the launch fails; a bounded wait that ran out
+ * is reported by sparse_mla_sync_status().
+ */
+smla_status sparse_mla_v_up(const void* o, const void* w, int32_t T, int32_t h, int32_t v, void* y,
+                            void* stream);
 
 /*
  * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the

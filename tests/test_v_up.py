@@ -102,3 +102,94 @@ def test_v_up_mutants_fail_a_pin(tmp_path, monkeypatch, name):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"no pin caught the mutant {name}"
+
+
+# ----------------------------------------------------------------------------- C ABI (no GPU)
+
+@pytest.fixture(scope="module")
+def lib():
+    import token_sparse_mla_gb300 as smla
+    return smla.library()
+
+
+@pytest.mark.parametrize("T,h,v,status", [(4, 8, 64, 2), (4, 8, 512, 2), (4, 0, 128, 1), (-1, 8, 128, 1)])
+def test_v_up_rejects_bad_arguments(lib, T, h, v, status):
+    buf = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    assert lib.sparse_mla_v_up(buf, buf, T, h, v, buf, None) == status
+
+
+def test_v_up_rejects_null_and_misaligned(lib):
+    good = ctypes.c_void_p(4096)
+    assert lib.sparse_mla_v_up(None, good, 4, 8, 128, good, None) == 1
+    assert lib.sparse_mla_v_up(good, ctypes.c_void_p(4104), 4, 8, 128, good, None) == 1
+    assert lib.sparse_mla_v_up(good, good, 4, 8, 128, ctypes.c_void_p(4098), None) == 1
+
+
+def test_v_up_zero_tokens_is_a_noop(lib):
+    assert lib.sparse_mla_v_up(None, None, 0, 8, 128, None, None) == 0
+
+
+# ----------------------------------------------------------------------------- GPU parity
+
+DEV = "cuda:0"
+
+
+def _gpu_v_up(o, w):
+    import token_sparse_mla_gb300 as smla
+    y = smla.sparse_mla_v_up(o.to(DEV), w.to(DEV))
+    smla.sync_status()
+    return y.cpu()
+
+
+def _assert_v_up_parity(y, ref, o, w, what):
+    """fp32 accumulation over 512 products, one bf16 rounding of the result."""
+    yv = y.float().double().numpy()
+    scale = np.einsum("thk,hnk->thn", np.abs(_dec(o)), np.abs(_dec(w)))
+    err = np.abs(yv - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * scale + 1e-30
+    assert np.all(np.isfinite(yv)), what
+    assert np.all(err <= bound), f"{what}: worst excess {(err - bound).max()}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,h,v", [(1, 1, 128), (5, 8, 128), (128, 2, 128), (129, 3, 256), (300, 8, 128),
+                                   (1000, 1, 256), (4096, 16, 128)])
+def test_gpu_v_up_matches_oracle(T, h, v):
+    o = _rand_o(T, h, seed=T + 7 * h)
+    w = make_v_up_weights(h, v, seed=T + v)
+    y = _gpu_v_up(o, w)
+    ref = oracle.v_up(o, w)
+    _assert_v_up_parity(y, ref, o, w, f"T={T} h={h} v={v}")
+
+
+@pytest.mark.gpu
+def test_gpu_v_up_identity_weights_are_exact():
+    T, h, v = 257, 4, 256
+    o = _rand_o(T, h, seed=9)
+    w = torch.zeros(h, v, 512, dtype=torch.bfloat16)
+    for n in range(v):
+        w[:, n, n] = 1.0
+    y = _gpu_v_up(o, w)
+    assert torch.equal(y, o[:, :, :v])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,kw", [("decode_bf16", {"n_seq": 8}), ("sweep", {"h": 64, "n_seq": 3})])
+def test_gpu_forward_then_v_up(name, kw):
+    """The forward on the GPU, then v_up on the GPU: against the oracle v_up of the same
+    output, and against the oracle chain within the forward's tolerance carried through W."""
+    import token_sparse_mla_gb300 as smla
+    from tests.parity import O_ATOL, O_RTOL
+    from workloads import make_workload
+    w_ = make_workload(name, **kw)
+    out, _ = smla.sparse_mla_fwd(w_.q.to(DEV), w_.kv.to(DEV), w_.indices.to(DEV), w_.scale)
+    W = make_v_up_weights(w_.h, 128, seed=3)
+    y = smla.sparse_mla_v_up(out, W.to(DEV))
+    smla.sync_status()
+    o_gpu = out.cpu()
+    _assert_v_up_parity(y.cpu(), oracle.v_up(o_gpu, W), o_gpu, W, f"{name} same input")
+    ref_o, _ = oracle.sparse_mla_fwd(w_.q, w_.kv, w_.indices, w_.scale)
+    ref_y = np.einsum("thk,hnk->thn", ref_o, _dec(W))
+    carried = np.einsum("thk,hnk->thn", O_ATOL + O_RTOL * np.abs(ref_o), np.abs(_dec(W)))
+    err = np.abs(y.cpu().float().double().numpy() - ref_y)
+    assert np.all(err <= carried + 2.0 ** -8 * np.abs(ref_y) + 1e-6), f"{name} chain"

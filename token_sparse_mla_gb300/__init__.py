@@ -10,7 +10,8 @@ device, the calls raise.
 q [T, h, 576] bf16, kv_cache [num_slots, 576] bf16 (or [num_slots, 656] uint8
 fp8 rows), indices [T, topk] int32 (-1 = invalid), h in {8, 16, 32, 64};
 returns out [T, h, 512] bf16 and lse [T, h] fp32.  sparse_mla_merge combines
-the (out, lse) of lists split into parts (the DCP merge).
+the (out, lse) of lists split into parts (the DCP merge); sparse_mla_v_up applies the
+per-head value up-projection to out on the tensor cores.
 """
 
 from ._binding import (  # noqa: F401
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     sparse_mla_fwd_host,
     sparse_mla_fwd_noalloc,
     sparse_mla_merge,
+    sparse_mla_v_up,
     sync_status,
     version,
 )
@@ -39,6 +41,7 @@ __all__ = [
     "sparse_mla_fwd_host",
     "sparse_mla_fwd_noalloc",
     "sparse_mla_merge",
+    "sparse_mla_v_up",
     "sync_status",
     "version",
 ]

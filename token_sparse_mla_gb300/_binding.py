@@ -47,6 +47,8 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_fwd_noalloc.restype = ctypes.c_int
     lib.sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_v_up.restype = ctypes.c_int
+    lib.sparse_mla_v_up.argtypes = [vp, vp, i32, i32, i32, vp, vp]
     lib.sparse_mla_merge.restype = ctypes.c_int
     lib.sparse_mla_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.sparse_mla_host_workspace_bytes.restype = sz
@@ -189,6 +191,31 @@ def sparse_mla_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
     _check(library().sparse_mla_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, T, h,
                                       out.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
     return out, lse
+
+
+def sparse_mla_v_up(o: torch.Tensor, w: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """The v_up projection of the attention output on the tensor cores (include/sparse_mla.h):
+    y[t, h, n] = sum_k o[t, h, k] * w[h, n, k], o [T, h, 512] bf16, w [h, v, 512] bf16
+    (v = 128 or 256); returns y [T, h, v] bf16."""
+    if o.dim() != 3 or o.shape[-1] != D_V or o.dtype != torch.bfloat16:
+        raise ValueError("o must be [T, h, 512] bf16")
+    T, h = int(o.shape[0]), int(o.shape[1])
+    if w.dim() != 3 or w.shape[0] != h or w.shape[2] != D_V or w.dtype != torch.bfloat16:
+        raise ValueError("w must be [h, v, 512] bf16")
+    v = int(w.shape[1])
+    for name, t in (("o", o), ("w", w)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, h, v), dtype=torch.bfloat16, device=o.device)
+    if out.shape != (T, h, v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, h, v] bf16 tensor")
+    _check(library().sparse_mla_v_up(o.data_ptr(), w.data_ptr(), T, h, v, out.data_ptr(),
+                                     _stream_handle(stream)))
+    return out
 
 
 def host_workspace_bytes(T: int, h: int, topk: int) -> int:

@@ -15,6 +15,7 @@
 #include "sparse_mla_kernel.cuh"
 #include "sparse_mla_small_kernel.cuh"
 #include "sparse_mla_merge.cuh"
+#include "sparse_mla_v_up.cuh"
 
 namespace {
 
@@ -68,6 +69,7 @@ cudaError_t set_kernel_attrs() {
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<8, 1, true>, smla::SmallLayout<8, 1>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 0, true>, smla::SmallLayout<16, 0>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_small_kernel<16, 1, true>, smla::SmallLayout<16, 1>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_v_up_kernel, smla::VupLayout::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 0>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 1>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 0>, smla::Layout<64>::kBytes);
@@ -591,6 +593,79 @@ smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_merge_kernel, mp);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return SMLA_OK;
+}
+
+
+smla_status sparse_mla_v_up(const void* o, const void* w, int32_t T, int32_t h, int32_t v, void* y,
+                            void* stream) {
+    if (T < 0 || h < 1) return fail(SMLA_ERR_INVALID_ARG, "T must be >= 0 and h >= 1 (got %d, %d)", T, h);
+    if (!(v == 128 || v == 256)) return fail(SMLA_ERR_UNSUPPORTED, "v must be 128 or 256 (got %d)", v);
+    if (T == 0) return SMLA_OK;
+    if (!o || !w || !y) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(o, 16) || !aligned(w, 16) || !aligned(y, 16))
+        return fail(SMLA_ERR_INVALID_ARG, "o, w and y must be 16-byte aligned");
+    if (static_cast<int64_t>(h) * v > 0x7fffffffLL || static_cast<int64_t>(T) * h > 0x7fffffffLL)
+        return fail(SMLA_ERR_INVALID_ARG, "T * h or h * v too large (%d, %d, %d)", T, h, v);
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    smla_status st = device_state(&dev, &ds);
+    if (st != SMLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    if ((st = encode_fn(&enc)) != SMLA_OK) return st;
+    // O [T, h, 512]: boxes of 128 tokens x 64 dims of one head; W [h, v, 512]: 128 outputs x 64 dims
+    alignas(64) CUtensorMap tm_o;
+    alignas(64) CUtensorMap tm_w;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(smla::kDV), static_cast<cuuint64_t>(h),
+                                    static_cast<cuuint64_t>(T)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(smla::kDV) * 2,
+                                       static_cast<cuuint64_t>(smla::kDV) * 2 * h};
+        const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(smla::kVupRows)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&tm_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(o), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor map for o failed (%d)", (int)r);
+    }
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(smla::kDV), static_cast<cuuint64_t>(v),
+                                    static_cast<cuuint64_t>(h)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(smla::kDV) * 2,
+                                       static_cast<cuuint64_t>(smla::kDV) * 2 * v};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(smla::kVupN), 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor map for w failed (%d)", (int)r);
+    }
+    smla::VupParams vp;
+    vp.y = static_cast<__nv_bfloat16*>(y);
+    vp.T = T;
+    vp.h = h;
+    vp.v = v;
+    vp.mtiles = (T + smla::kVupRows - 1) / smla::kVupRows;
+    // one CTA per SM: the (head, 128-output) slices share the SMs, each slice's token tiles
+    // split evenly over its CTAs (at least one tile each)
+    const int64_t slices = static_cast<int64_t>(h) * (v / smla::kVupN);
+    int64_t cpg = slices >= ds->num_sms ? 1 : ds->num_sms / slices;
+    if (cpg > vp.mtiles) cpg = vp.mtiles;
+    vp.cpg = static_cast<int32_t>(cpg);
+    const int64_t grid = slices * cpg;
+    if (grid > 0x7fffffffLL) return fail(SMLA_ERR_INVALID_ARG, "grid too large");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(smla::kVupThreads, 1, 1);
+    cfg.dynamicSmemBytes = smla::VupLayout::kBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_v_up_kernel, tm_o, tm_w, vp);
+    if (e != cudaSuccess) return cuda_fail(e, "v_up kernel launch");
     return SMLA_OK;
 }
 
