@@ -11,7 +11,7 @@
 // GEMM per head on the tensor cores: M = 128 tokens, N = 128 outputs, K = 512 in eight
 // 64-wide SW128 panels.  Each CTA owns one (head, 128-output slice) and a contiguous run of
 // 128-token tiles: its W slice (128 KB) is loaded once and stays in shared memory, the O
-// panels stream through a four-stage TMA ring, and the fp32 accumulator lives in TMEM, double
+// panels stream through a six-stage TMA ring, and the fp32 accumulator lives in TMEM, double
 // buffered so the epilogue of one tile overlaps the MMAs of the next.
 //
 // Roles (192 threads):
@@ -30,14 +30,14 @@ namespace smla {
 constexpr int kVupRows = 128;                      // tokens per tile (MMA M)
 constexpr int kVupN = 128;                         // outputs per CTA (MMA N)
 constexpr int kVupPanels = kDV / 64;               // K = 512 in 64-wide panels
-constexpr int kVupStages = 4;
+constexpr int kVupStages = 6;                      // 96 KB of O in flight (four stages: 60.3 us, six: 55.5 us)
 constexpr int kVupPanelBytes = 128 * 128;          // 128 rows x 64 bf16, SW128
 constexpr int kVupThreads = 192;
 constexpr int kVupTmemCols = 2 * kVupN;            // two accumulators
 
 struct VupLayout {
     static constexpr int kOffW = 0;                                          // [8 panels][128 n][64 k]
-    static constexpr int kOffA = kOffW + kVupPanels * kVupPanelBytes;        // [4 stages][128 t][64 k]
+    static constexpr int kOffA = kOffW + kVupPanels * kVupPanelBytes;        // [6 stages][128 t][64 k]
     static constexpr int kOffBar = kOffA + kVupStages * kVupPanelBytes;
     static constexpr int kNumBars = 1 + 2 * kVupStages + 4 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;                  // tmem base, abort flag
