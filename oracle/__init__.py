@@ -59,6 +59,9 @@ def _load():
         lib.oracle_v_up.restype = ctypes.c_int
         lib.oracle_v_up.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_void_p]
+        lib.oracle_topk.restype = ctypes.c_int
+        lib.oracle_topk.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                    ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -192,3 +195,24 @@ def v_up(o, w) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return y
+
+
+def topk(scores, lengths, k: int, block_table=None) -> np.ndarray:
+    """Top-k index lists from scores (the C file's oracle_topk).
+
+    scores [T, S] fp32, lengths [T] int32 (the causal history of each row), block_table
+    optional [ceil(S / 64)] int32; returns [T, k] int32: selected slots (positions when no
+    table) in ascending position order, -1 padding.
+    """
+    lib = _load()
+    sn = np.ascontiguousarray(_as_np(scores).astype(np.float32))
+    ln = np.ascontiguousarray(_as_np(lengths).astype(np.int32))
+    T, S = sn.shape
+    assert ln.shape == (T,)
+    bt = None if block_table is None else np.ascontiguousarray(_as_np(block_table).astype(np.int32))
+    out = np.empty((T, k), dtype=np.int32)
+    rc = lib.oracle_topk(sn.ctypes.data, T, S, ln.ctypes.data, int(k),
+                         None if bt is None else bt.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out

@@ -286,3 +286,70 @@ int oracle_v_up(const uint16_t *o, const uint16_t *w, int64_t T, int h, int v, d
     }
     return 0;
 }
+
+/*
+ * Top-k selection of a token's index list from per-position scores: the step before the
+ * sparse attention (vLLM PR #54951, Summary: the indexer's "MQA logits and top-k" produce the
+ * fixed-width int32 lists; Additional checks: the top-k order is not deterministic, only the
+ * set matters).  The pages do not give the indexer's scoring; this takes the scores as input.
+ * Row t keeps the `topk` positions with the largest scores among its causal history
+ * [0, len[t]) -- ties broken towards the lower position -- lists them in ascending position
+ * order, maps position p to slot block_table[p / 64] * 64 + p % 64 (block_table may be NULL:
+ * slot = p), and pads with -1 when len[t] < topk.
+ * scores [T, S] fp32, len [T] int32 (0 <= len <= S), out [T, topk] int32.
+ * Returns 0, or 1 for bad sizes.
+ */
+typedef struct {
+    float score;
+    int32_t pos;
+} oracle_scored;
+
+static int oracle_by_score_desc(const void *a, const void *b) {
+    const oracle_scored *x = (const oracle_scored *)a, *y = (const oracle_scored *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static int oracle_by_pos(const void *a, const void *b) {
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+int oracle_topk(const float *scores, int64_t T, int64_t S, const int32_t *len, int topk,
+                const int32_t *block_table, int32_t *out) {
+    if (T < 0 || S < 0 || topk < 1) return 1;
+    for (int64_t t = 0; t < T; ++t)
+        if (len[t] < 0 || len[t] > S) return 1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        oracle_scored *row = (oracle_scored *)malloc(sizeof(oracle_scored) * (size_t)(S > 0 ? S : 1));
+        int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk);
+        if (!row || !sel) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!row || !sel) continue;
+            const int64_t n = len[t];
+            for (int64_t p = 0; p < n; ++p) {
+                row[p].score = scores[t * S + p];
+                row[p].pos = (int32_t)p;
+            }
+            qsort(row, (size_t)n, sizeof(oracle_scored), oracle_by_score_desc);
+            const int k = n < topk ? (int)n : topk;
+            for (int i = 0; i < k; ++i) sel[i] = row[i].pos;
+            qsort(sel, (size_t)k, sizeof(int32_t), oracle_by_pos);
+            for (int i = 0; i < topk; ++i) {
+                int32_t v = -1;
+                if (i < k) v = block_table ? block_table[sel[i] / 64] * 64 + sel[i] % 64 : sel[i];
+                out[t * topk + i] = v;
+            }
+        }
+        free(row);
+        free(sel);
+    }
+    return failed ? 2 : 0;
+}

@@ -1,0 +1,107 @@
+"""Top-k selection of the index lists from per-position scores (the step before the sparse
+attention): oracle pins on the CPU.
+
+Row t keeps the topk positions with the largest scores among its causal history [0, len[t]),
+ties to the lower position, in ascending position order, mapped to slots through a block table
+of 64-slot blocks, -1 padded (vLLM PR #54951, Summary and Additional checks: int32 lists of
+fixed width, only the set of selected rows matters).  Pins of the oracle, from outside it:
+
+* set equality with torch.topk on distinct scores, rows in ascending position order;
+* closed forms: a history shorter than topk selects all of it and pads with -1; equal scores
+  select the lowest positions; a block table maps position p to table[p / 64] * 64 + p % 64;
+* mutation: mutated copies (bottom-k, the history length ignored, ties to the higher
+  position) each fail one of these.
+"""
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _scores(T, S, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(T, S, generator=g, dtype=torch.float32)
+
+
+# ----------------------------------------------------------------------------- oracle pins
+
+@pytest.mark.parametrize("T,S,k", [(4, 300, 16), (3, 5000, 2048), (2, 64, 64), (5, 1000, 1)])
+def test_matches_torch_topk_as_sets(T, S, k):
+    s = _scores(T, S, seed=S + k)
+    g = torch.Generator().manual_seed(k)
+    lens = torch.randint(k, S + 1, (T,), generator=g).to(torch.int32)
+    out = oracle.topk(s, lens, k)
+    for t in range(T):
+        n = int(lens[t])
+        ref = torch.topk(s[t, :n], k).indices.numpy()
+        assert set(out[t].tolist()) == set(ref.tolist())
+        assert np.all(np.diff(out[t]) > 0)
+
+
+def test_short_history_selects_all_and_pads():
+    s = _scores(3, 100, seed=1)
+    out = oracle.topk(s, np.array([0, 7, 100], dtype=np.int32), 16)
+    assert np.all(out[0] == -1)
+    assert out[1].tolist() == list(range(7)) + [-1] * 9
+    assert len(set(out[2].tolist())) == 16 and -1 not in out[2]
+
+
+def test_ties_go_to_the_lower_positions():
+    s = torch.zeros(2, 500)
+    s[1, 300:] = 1.0  # 200 top scores tied, topk 50: the 50 lowest of them
+    out = oracle.topk(s, np.array([500, 500], dtype=np.int32), 50)
+    assert out[0].tolist() == list(range(50))
+    assert out[1].tolist() == list(range(300, 350))
+
+
+def test_block_table_maps_positions_to_slots():
+    s = _scores(2, 640, seed=2)
+    table = torch.randperm(10, generator=torch.Generator().manual_seed(3)).to(torch.int32) + 5
+    pos = oracle.topk(s, np.array([640, 333], dtype=np.int32), 32)
+    slots = oracle.topk(s, np.array([640, 333], dtype=np.int32), 32, block_table=table)
+    tb = table.numpy()
+    assert np.array_equal(slots, tb[pos // 64] * 64 + pos % 64)
+
+
+_MUTANTS = {
+    "bottom_k": (r"if \(x->score > y->score\) return -1;\n    if \(x->score < y->score\) return 1;",
+                 "if (x->score < y->score) return -1;\n    if (x->score > y->score) return 1;"),
+    "history_ignored": (r"const int64_t n = len\[t\];", "const int64_t n = S;"),
+    "ties_to_higher_position": (r"return \(x->pos > y->pos\) - \(x->pos < y->pos\);\n\}\n\nstatic int oracle_by_pos",
+                                "return (x->pos < y->pos) - (x->pos > y->pos);\n}\n\nstatic int oracle_by_pos"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_MUTANTS))
+def test_topk_mutants_fail_a_pin(tmp_path, monkeypatch, name):
+    src = Path(oracle.__file__).with_name("sparse_mla_oracle.c").read_text()
+    pat, rep = _MUTANTS[name]
+    mutated, k = re.subn(pat, rep, src)
+    assert k == 1, f"mutation {name} did not apply"
+    c = tmp_path / f"{name}.c"
+    c.write_text(mutated)
+    so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", str(so),
+                    str(c), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    good = oracle._load()
+    for fn in ("oracle_topk", "oracle_max_threads"):
+        getattr(lib, fn).restype = getattr(good, fn).restype
+        getattr(lib, fn).argtypes = getattr(good, fn).argtypes
+    monkeypatch.setattr(oracle, "_lib", lib)
+    pins = [lambda: test_matches_torch_topk_as_sets(4, 300, 16), test_short_history_selects_all_and_pads,
+            test_ties_go_to_the_lower_positions, test_block_table_maps_positions_to_slots]
+    failures = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"no pin caught the mutant {name}"
