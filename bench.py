@@ -16,7 +16,8 @@ step never finds its rows in L2 from the previous steps.
 same workload, a bounded number of tokens per step.
 --workload dcp_merge times sparse_mla_merge instead: the combine of 4 split-list
 partial results per row at the fp8 batch's shape (T = 32768, h = 8); --workload
-v_up times sparse_mla_v_up (T = 32768, h = 8, v_head_dim 128).
+v_up times sparse_mla_v_up (T = 32768, h = 8, v_head_dim 128); --workload topk times
+sparse_mla_topk (the prefill chunk's 16384 causal rows over 32768 positions, k = 2048).
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path shards by query token with no exchange), weak scaling.
 """
@@ -656,6 +657,140 @@ def run_v_up_reference(args, rank, world):
     }), flush=True)
 
 
+# ---- top-k selection of the index lists (the prefill chunk's shape: causal rows)
+TOPK_SHAPE = {"T": 16384, "S": 32768, "topk": 2048}
+
+
+def topk_inputs(seed: int):
+    T, S = TOPK_SHAPE["T"], TOPK_SHAPE["S"]
+    g = torch.Generator().manual_seed(seed)
+    scores = torch.randn(T, S, generator=g)
+    lens = torch.arange(S - T + 1, S + 1, dtype=torch.int32)  # query positions S-T .. S-1
+    table = torch.randperm(S // 64, generator=g).to(torch.int32)
+    return scores, lens, table
+
+
+def topk_bytes(lens) -> int:
+    """Scores read once over each row's history, the lengths, the lists written."""
+    T = lens.numel()
+    return int(lens.sum().item()) * 4 + T * 4 + T * TOPK_SHAPE["topk"] * 4
+
+
+def topk_config(args, nbytes: int) -> dict:
+    return {"workload": "topk", **TOPK_SHAPE,
+            "inputs": "scores ~ N(0, 1) fp32 [T, S], causal histories S - T + 1 .. S, a random block table",
+            "launch": "CUDA graph of consecutive steps" if args.launch == "graph" else "eager launches",
+            "l2": f"{nbytes / 1e9:.2f} GB read and written per step > 2 x L2"}
+
+
+def run_topk(args, rank, world, local_rank):
+    import token_sparse_mla_gb300 as smla
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    T, S, K = TOPK_SHAPE["T"], TOPK_SHAPE["S"], TOPK_SHAPE["topk"]
+    s_h, l_h, t_h = topk_inputs(7200 + 7919 * rank)
+    s_d, l_d, t_d = s_h.to(dev), l_h.to(dev), t_h.to(dev)
+    out = torch.empty((T, K), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        smla.sparse_mla_topk(s_d, l_d, K, block_table=t_d, out=out, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    smla.sync_status(stream)
+    glen = 4
+    graph = None
+    if args.launch == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(glen):
+                step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    steps = max(glen, (args.steps // glen) * glen) if graph is not None else args.steps
+
+    def timed():
+        if graph is not None:
+            for _ in range(steps // glen):
+                graph.replay()
+        else:
+            for _ in range(steps):
+                step()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        timed()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        timed()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.stop()
+    smla.sync_status(stream)
+    t_dev = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    per_launch = t_dev / steps
+    nbytes = topk_bytes(l_h)
+    achieved = nbytes / per_launch / 1e9
+    peaks = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rows = 64
+        t0 = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t0 < args.cpu_seconds or k == 0:
+            oracle.topk(s_h[:rows], l_h[:rows], K, block_table=t_h)
+            k += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": k * rows / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"the first {rows} rows, selected {k} times in {el:.1f} s"}
+    line = {
+        "metric": METRIC, "value": world * T * steps / t_dev, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_launch * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": topk_config(args, nbytes),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("topk", 0, False),
+                     "peak_source": peaks["source"] + " (copy bandwidth)",
+                     "per_launch_algorithmic_bytes": nbytes, "kernel": "sparse_mla_topk_kernel"},
+        "cpu_baseline": cpu, "e2e": None, "clocks": clocks.summary(), "gpu_launches": steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_topk_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    s_h, l_h, t_h = topk_inputs(7200)
+    rows = 64
+    for _ in range(args.warmup):
+        oracle.topk(s_h[:2], l_h[:2], TOPK_SHAPE["topk"], block_table=t_h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.topk(s_h[:rows], l_h[:rows], TOPK_SHAPE["topk"], block_table=t_h)
+    el = time.perf_counter() - t0
+    value = rows * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": topk_config(args, topk_bytes(l_h)),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -678,7 +813,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_setup(args)
-    if args.workload == "v_up":
+    if args.workload == "topk":
+        (run_topk_reference(args, rank, world) if args.impl == "reference"
+         else run_topk(args, rank, world, local_rank))
+    elif args.workload == "v_up":
         (run_v_up_reference(args, rank, world) if args.impl == "reference"
          else run_v_up(args, rank, world, local_rank))
     elif args.workload == "dcp_merge":

@@ -13,8 +13,9 @@
  * An index list with no valid entry gives O = 0 and LSE = -inf.  Each list
  * entry is a separate softmax term (a slot listed twice counts twice).
  * sparse_mla_merge combines the (O, LSE) of lists split into parts, e.g. over
- * decode-context-parallel ranks, into the result of the whole lists, and
- * sparse_mla_v_up applies the per-head value up-projection to O.
+ * decode-context-parallel ranks, into the result of the whole lists,
+ * sparse_mla_v_up applies the per-head value up-projection to O, and
+ * sparse_mla_topk builds the index lists from per-position scores.
  *
  * Sources (page title, section):
  *   vLLM PR #60220 "FlashMLA sparse: stage fp8 mixed-batch q/out in the
@@ -186,6 +187,28 @@ smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_
  */
 smla_status sparse_mla_v_up(const void* o, const void* w, int32_t T, int32_t h, int32_t v, void* y,
                             void* stream);
+
+/*
+ * sparse_mla_topk -- the index lists from per-position scores: the step before
+ * the attention.  The indexer scores every position of a token's causal history
+ * and keeps the top k as a fixed-width int32 list in which only the set matters
+ * (vLLM PR #54951, Summary and Additional checks); the pages do not give the
+ * scoring, so the scores are the input.  Row t keeps the topk positions with the
+ * largest scores among [0, lengths[t]) (ties to the lower position), in
+ * ascending position order, each mapped to its cache slot
+ * block_table[p / 64] * 64 + p % 64 (block_table NULL: the position itself),
+ * and pads with -1 when lengths[t] < topk.  Exact (a radix select), so results
+ * are reproducible bit for bit.
+ *   scores       device, [T, S] fp32 (no NaN), row-major, 4-byte aligned
+ *   lengths      device, [T] int32; values outside [0, S] are clamped
+ *   block_table  device, [ceil(S / 64)] int32 of one sequence, or NULL
+ *   indices      device, [T, topk] int32, caller-owned: sparse_mla_fwd's input
+ * T = 0 is a no-op.  Allocates nothing; asynchronous on `stream`.  Errors:
+ * SMLA_ERR_INVALID_ARG for bad sizes (S < 1, topk outside [1, 2^20]), a null
+ * pointer or misalignment; SMLA_ERR_CUDA if the launch fails.
+ */
+smla_status sparse_mla_topk(const float* scores, int32_t T, int64_t S, const int32_t* lengths, int32_t topk,
+                            const int32_t* block_table, int32_t* indices, void* stream);
 
 /*
  * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the

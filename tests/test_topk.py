@@ -105,3 +105,81 @@ def test_topk_mutants_fail_a_pin(tmp_path, monkeypatch, name):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"no pin caught the mutant {name}"
+
+
+# ----------------------------------------------------------------------------- C ABI (no GPU)
+
+@pytest.fixture(scope="module")
+def lib():
+    import token_sparse_mla_gb300 as smla
+    return smla.library()
+
+
+@pytest.mark.parametrize("T,S,k", [(-1, 100, 8), (4, 0, 8), (4, 100, 0), (4, 100, (1 << 20) + 1)])
+def test_topk_rejects_bad_sizes(lib, T, S, k):
+    buf = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    assert lib.sparse_mla_topk(buf, T, S, buf, k, None, buf, None) == 1
+
+
+def test_topk_rejects_null_and_misaligned(lib):
+    good = ctypes.c_void_p(4096)
+    assert lib.sparse_mla_topk(None, 4, 100, good, 8, None, good, None) == 1
+    assert lib.sparse_mla_topk(ctypes.c_void_p(4098), 4, 100, good, 8, None, good, None) == 1
+    assert lib.sparse_mla_topk(good, 4, 100, good, 8, ctypes.c_void_p(4097), good, None) == 1
+
+
+def test_topk_zero_rows_is_a_noop(lib):
+    assert lib.sparse_mla_topk(None, 0, 100, None, 8, None, None, None) == 0
+
+
+# ----------------------------------------------------------------------------- GPU parity
+
+DEV = "cuda:0"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,S,k,mode", [(4, 300, 16, "rand"), (3, 5000, 2048, "rand"), (6, 2047, 2048, "rand"),
+                                        (5, 4096, 2048, "ties"), (2, 70000, 2048, "rand"), (8, 1000, 1, "rand"),
+                                        (3, 3000, 777, "quant"), (16, 33000, 2048, "rand")])
+def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
+    import token_sparse_mla_gb300 as smla
+    s = _scores(T, S, seed=S + k)
+    if mode == "ties":
+        s = torch.zeros(T, S)
+        s[:, ::3] = 1.0  # many equal scores at the threshold
+    elif mode == "quant":
+        s = torch.round(s * 4) / 4  # few distinct values: ties everywhere
+    g = torch.Generator().manual_seed(T + k)
+    lens = torch.randint(0, S + 1, (T,), generator=g).to(torch.int32)
+    lens[0] = S
+    if T > 1:
+        lens[1] = min(S, k - 1)  # a short history
+    table = (torch.randperm((S + 63) // 64, generator=g).to(torch.int32) + 3)
+    for bt in (None, table):
+        out = smla.sparse_mla_topk(s.to(DEV), lens.to(DEV), k, block_table=None if bt is None else bt.to(DEV))
+        smla.sync_status()
+        ref = oracle.topk(s, lens, k, block_table=bt)
+        assert np.array_equal(out.cpu().numpy(), ref), f"T={T} S={S} k={k} {mode} table={bt is not None}"
+
+
+@pytest.mark.gpu
+def test_gpu_topk_feeds_the_forward():
+    """Scores -> GPU top-k (slots through the block table) -> GPU forward, against the oracle
+    forward on the oracle's lists: the lists must be identical and the outputs within the
+    forward's tolerance."""
+    import token_sparse_mla_gb300 as smla
+    from tests.parity import assert_parity
+    from workloads import make_workload
+    w = make_workload("prefill", n_tokens=8)
+    S = w.num_slots  # one sequence: positions 0 .. 32767
+    g = torch.Generator().manual_seed(77)
+    scores = torch.randn(w.T, S, generator=g)
+    lens = torch.arange(S - w.T + 1, S + 1, dtype=torch.int32)[: w.T]  # causal histories
+    table = torch.randperm(S // 64, generator=g).to(torch.int32)
+    idx_gpu = smla.sparse_mla_topk(scores.to(DEV), lens.to(DEV), w.topk, block_table=table.to(DEV))
+    out, lse = smla.sparse_mla_fwd(w.q.to(DEV), w.kv.to(DEV), idx_gpu, w.scale)
+    smla.sync_status()
+    idx_ref = oracle.topk(scores, lens, w.topk, block_table=table)
+    assert np.array_equal(idx_gpu.cpu().numpy(), idx_ref)
+    ref_o, ref_l = oracle.sparse_mla_fwd(w.q, w.kv, torch.from_numpy(idx_ref), w.scale)
+    assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, "topk -> forward")

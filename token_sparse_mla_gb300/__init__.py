@@ -11,7 +11,8 @@ q [T, h, 576] bf16, kv_cache [num_slots, 576] bf16 (or [num_slots, 656] uint8
 fp8 rows), indices [T, topk] int32 (-1 = invalid), h in {8, 16, 32, 64};
 returns out [T, h, 512] bf16 and lse [T, h] fp32.  sparse_mla_merge combines
 the (out, lse) of lists split into parts (the DCP merge); sparse_mla_v_up applies the
-per-head value up-projection to out on the tensor cores.
+per-head value up-projection to out on the tensor cores; sparse_mla_topk builds the
+index lists from per-position scores.
 """
 
 from ._binding import (  # noqa: F401
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     sparse_mla_fwd_host,
     sparse_mla_fwd_noalloc,
     sparse_mla_merge,
+    sparse_mla_topk,
     sparse_mla_v_up,
     sync_status,
     version,
@@ -41,6 +43,7 @@ __all__ = [
     "sparse_mla_fwd_host",
     "sparse_mla_fwd_noalloc",
     "sparse_mla_merge",
+    "sparse_mla_topk",
     "sparse_mla_v_up",
     "sync_status",
     "version",

@@ -47,6 +47,8 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_fwd_noalloc.restype = ctypes.c_int
     lib.sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_topk.restype = ctypes.c_int
+    lib.sparse_mla_topk.argtypes = [vp, i32, i64, vp, i32, vp, vp, vp]
     lib.sparse_mla_v_up.restype = ctypes.c_int
     lib.sparse_mla_v_up.argtypes = [vp, vp, i32, i32, i32, vp, vp]
     lib.sparse_mla_merge.restype = ctypes.c_int
@@ -215,6 +217,37 @@ def sparse_mla_v_up(o: torch.Tensor, w: torch.Tensor, *, out: Optional[torch.Ten
         raise ValueError("out must be a contiguous [T, h, v] bf16 tensor")
     _check(library().sparse_mla_v_up(o.data_ptr(), w.data_ptr(), T, h, v, out.data_ptr(),
                                      _stream_handle(stream)))
+    return out
+
+
+def sparse_mla_topk(scores: torch.Tensor, lengths: torch.Tensor, topk: int, *,
+                    block_table: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """Index lists from per-position scores (include/sparse_mla.h): the top `topk` positions of
+    scores[t, :lengths[t]] (ties to the lower position), ascending, mapped through block_table
+    (64-slot blocks) when given, -1 padded.  scores [T, S] fp32, lengths [T] int32."""
+    if scores.dim() != 2 or scores.dtype != torch.float32:
+        raise ValueError("scores must be [T, S] fp32")
+    T, S = int(scores.shape[0]), int(scores.shape[1])
+    if lengths.shape != (T,) or lengths.dtype != torch.int32:
+        raise ValueError("lengths must be [T] int32")
+    tensors = [("scores", scores), ("lengths", lengths)]
+    if block_table is not None:
+        if block_table.dim() != 1 or block_table.dtype != torch.int32 or block_table.numel() * 64 < S:
+            raise ValueError("block_table must be [ceil(S / 64)] int32")
+        tensors.append(("block_table", block_table))
+    for name, t in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, topk), dtype=torch.int32, device=scores.device)
+    if out.shape != (T, topk) or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, topk] int32 tensor")
+    _check(library().sparse_mla_topk(scores.data_ptr(), T, S, lengths.data_ptr(), int(topk),
+                                     None if block_table is None else block_table.data_ptr(),
+                                     out.data_ptr(), _stream_handle(stream)))
     return out
 
 

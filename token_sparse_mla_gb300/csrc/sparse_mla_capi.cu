@@ -16,6 +16,7 @@
 #include "sparse_mla_small_kernel.cuh"
 #include "sparse_mla_merge.cuh"
 #include "sparse_mla_v_up.cuh"
+#include "sparse_mla_topk.cuh"
 
 namespace {
 
@@ -666,6 +667,42 @@ smla_status sparse_mla_v_up(const void* o, const void* w, int32_t T, int32_t h, 
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_v_up_kernel, tm_o, tm_w, vp);
     if (e != cudaSuccess) return cuda_fail(e, "v_up kernel launch");
+    return SMLA_OK;
+}
+
+
+smla_status sparse_mla_topk(const float* scores, int32_t T, int64_t S, const int32_t* lengths, int32_t topk,
+                            const int32_t* block_table, int32_t* indices, void* stream) {
+    if (T < 0 || S < 1 || topk < 1 || topk > (1 << 20) || S > 0x7fffffffLL)
+        return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d S=%lld topk=%d", T, static_cast<long long>(S), topk);
+    if (T == 0) return SMLA_OK;
+    if (!scores || !lengths || !indices) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(scores, 4) || !aligned(lengths, 4) || !aligned(indices, 4) || !aligned(block_table, 4))
+        return fail(SMLA_ERR_INVALID_ARG, "scores, lengths, block_table and indices must be 4-byte aligned");
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    smla_status st = device_state(&dev, &ds);
+    if (st != SMLA_OK) return st;
+    smla::TopkParams tp;
+    tp.scores = scores;
+    tp.len = lengths;
+    tp.block_table = block_table;
+    tp.out = indices;
+    tp.S = S;
+    tp.T = T;
+    tp.topk = topk;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(T), 1, 1);
+    cfg.blockDim = dim3(smla::kTopkThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_topk_kernel, tp);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
     return SMLA_OK;
 }
 
