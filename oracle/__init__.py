@@ -62,6 +62,14 @@ def _load():
         lib.oracle_topk.restype = ctypes.c_int
         lib.oracle_topk.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_scatter_mask.restype = ctypes.c_int
+        lib.oracle_scatter_mask.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                            ctypes.c_int64, ctypes.c_void_p]
+        lib.oracle_masked_mha.restype = ctypes.c_int
+        lib.oracle_masked_mha.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -216,3 +224,56 @@ def topk(scores, lengths, k: int, block_table=None) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return out
+
+
+def _as_f64(x) -> np.ndarray:
+    """torch tensor (any float dtype, bf16 included) or float array -> C-contiguous float64."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().cpu().double().numpy())  # exact widening
+    except ImportError:
+        pass
+    a = np.asarray(x)
+    assert a.dtype.kind == "f", a.dtype
+    return np.ascontiguousarray(a.astype(np.float64))
+
+
+def scatter_mask(indices, S: int) -> np.ndarray:
+    """The lists scattered to a bit mask (the C file's oracle_scatter_mask).
+
+    indices [T, topk] int32 positions in [0, S) (-1 and other values outside it set nothing);
+    returns [T, ceil(S / 32)] uint32: bit s % 32 of word s // 32 is set iff s is listed.
+    """
+    lib = _load()
+    idn = np.ascontiguousarray(_as_np(indices).astype(np.int32))
+    T, k = idn.shape
+    mask = np.empty((T, (int(S) + 31) // 32), dtype=np.uint32)
+    rc = lib.oracle_scatter_mask(idn.ctypes.data, T, k, int(S), mask.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return mask
+
+
+def masked_mha(q, k, v, mask, scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Masked dense MHA over per-head K and V (the C file's oracle_masked_mha), fp64.
+
+    q [T, h, dqk], k [S, h, dqk], v [S, h, dv]: torch tensors (bf16 included) or float arrays;
+    mask [T, ceil(S / 32)] uint32 bits as scatter_mask returns them.
+    returns out [T, h, dv] float64 and lse [T, h] float64 (natural log; -inf for an empty row)
+    """
+    lib = _load()
+    qn, kn, vn = _as_f64(q), _as_f64(k), _as_f64(v)
+    T, h, dqk = qn.shape
+    S = kn.shape[0]
+    dv = vn.shape[2]
+    assert kn.shape == (S, h, dqk) and vn.shape == (S, h, dv), (qn.shape, kn.shape, vn.shape)
+    mn = np.ascontiguousarray(np.asarray(mask, dtype=np.uint32))
+    assert mn.shape == (T, (S + 31) // 32), mn.shape
+    out = np.empty((T, h, dv), dtype=np.float64)
+    lse = np.empty((T, h), dtype=np.float64)
+    rc = lib.oracle_masked_mha(qn.ctypes.data, kn.ctypes.data, vn.ctypes.data, mn.ctypes.data,
+                               T, S, h, dqk, dv, float(scale), out.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out, lse

@@ -353,3 +353,102 @@ int oracle_topk(const float *scores, int64_t T, int64_t S, const int32_t *len, i
     }
     return failed ? 2 : 0;
 }
+
+/*
+ * The masked dense route for short prefill (PR #55738 report, 实现拆解 items 2 and 5 and the
+ * key-files list: the top-k lists are scattered into a dense mask and a masked MHA runs over
+ * the request's decompressed per-head K and V, instead of the per-token sparse kernel).  The
+ * pages name the steps (a scatter kernel, a `mask_mod` attention) but give neither the mask's
+ * layout nor the arithmetic.  Read as:
+ *
+ *   scatter:  mask[t, s] = 1  <=>  some j has idx[t, j] == s, 0 <= s < S
+ *             (-1 and every other value outside [0, S) set nothing; a position listed twice
+ *             sets its bit once).  Stored as bits: bit (s % 32) of word s / 32 of row t,
+ *             W = ceil(S / 32) uint32 words a row, the bits past S zero.
+ *   masked MHA, per token t and head h, over the positions s with mask[t, s] = 1:
+ *             s_ts    = scale * sum_{d < dqk} q[t, h, d] * k[s, h, d]
+ *             O[t, h] = sum_s softmax(s_t.)_s * v[s, h, 0:dv]
+ *             LSE     = natural log of sum_s exp(s_ts);  no position: O = 0, LSE = -inf.
+ *
+ * The mask alone decides which positions attend: lists drawn over a token's causal history
+ * are causal by construction.  Since the mask holds a set, this equals the sparse forward
+ * over the same lists exactly when no list repeats a position.
+ */
+int oracle_scatter_mask(const int32_t *idx, int64_t T, int topk, int64_t S, uint32_t *mask) {
+    if (T < 0 || topk < 1 || S < 1) return 1;
+    const int64_t W = (S + 31) / 32;
+    for (int64_t i = 0; i < T * W; ++i) mask[i] = 0u;
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < topk; ++j) {
+            const int64_t s = idx[t * topk + j];
+            if (s < 0 || s >= S) continue;
+            mask[t * W + s / 32] |= 1u << (s % 32);
+        }
+    return 0;
+}
+
+/*
+ * q [T, h, dqk], k [S, h, dqk], v [S, h, dv] fp64 values (the caller decodes bf16 exactly);
+ * mask [T, ceil(S / 32)] bits as oracle_scatter_mask writes them;
+ * out [T, h, dv] fp64;  lse [T, h] fp64.
+ * Returns 0, 1 for a bad size, 2 if memory ran out.
+ */
+int oracle_masked_mha(const double *q, const double *k, const double *v, const uint32_t *mask,
+                      int64_t T, int64_t S, int h, int dqk, int dv, double scale, double *out,
+                      double *lse) {
+    if (T < 0 || S < 1 || h < 1 || dqk < 1 || dv < 1) return 1;
+    const int64_t W = (S + 31) / 32;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)S);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!sc || !acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t p = 0; p < T * (int64_t)h; ++p) {
+            if (!sc || !acc) continue;
+            const int64_t t = p / h;
+            const int hh = (int)(p % h);
+            const double *qr = q + p * dqk;
+            const uint32_t *mrow = mask + t * W;
+            double *o = out + p * dv;
+
+            /* pass 1: scaled logits of the masked-in positions and their maximum */
+            double m = -INFINITY;
+            int64_t n_in = 0;
+            for (int64_t s = 0; s < S; ++s) {
+                if (!((mrow[s / 32] >> (s % 32)) & 1u)) continue;
+                const double *kr = k + (s * h + hh) * (int64_t)dqk;
+                double dot = 0.0;
+                for (int d = 0; d < dqk; ++d) dot += qr[d] * kr[d];
+                sc[s] = scale * dot;
+                if (sc[s] > m) m = sc[s];
+                ++n_in;
+            }
+            if (n_in == 0) {
+                for (int d = 0; d < dv; ++d) o[d] = 0.0;
+                lse[p] = -INFINITY;
+                continue;
+            }
+
+            /* pass 2: softmax weights and the weighted sum of the value rows */
+            double l = 0.0;
+            for (int d = 0; d < dv; ++d) acc[d] = 0.0;
+            for (int64_t s = 0; s < S; ++s) {
+                if (!((mrow[s / 32] >> (s % 32)) & 1u)) continue;
+                const double *vr = v + (s * h + hh) * (int64_t)dv;
+                const double w = exp(sc[s] - m);
+                l += w;
+                for (int d = 0; d < dv; ++d) acc[d] += w * vr[d];
+            }
+            for (int d = 0; d < dv; ++d) o[d] = acc[d] / l;
+            lse[p] = m + log(l);
+        }
+        free(sc);
+        free(acc);
+    }
+    return failed ? 2 : 0;
+}

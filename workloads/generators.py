@@ -250,3 +250,40 @@ def make_v_up_weights(h: int, v: int, seed: int = 7000) -> torch.Tensor:
     the scale of the latent output."""
     g = _gen(seed, 12)
     return (torch.randn(h, v, 512, generator=g) * 512 ** -0.5).to(torch.bfloat16)
+
+
+def causal_position_lists(T: int, S: int, topk: int, seed: int = 8000,
+                          p_empty: float = 0.0) -> torch.Tensor:
+    """Position lists of a prefill chunk, [T, topk] int32: the chunk's T query tokens are the
+    last T positions of an S-position request, so token t sees the causal history
+    [0, S - T + 1 + t).  Its list holds min(topk, history) distinct positions of that history,
+    the top-k of i.i.d. uniform keys (so in random order), -1 padded; a token's list is all -1
+    with probability p_empty.  A topk at least S gives every token its full history: the
+    short-prefill case."""
+    assert 1 <= T <= S and topk >= 1
+    g = _gen(seed, 13)
+    out = torch.full((T, topk), -1, dtype=torch.int32)
+    k = min(topk, S)
+    pos = torch.arange(S)
+    for t0 in range(0, T, _TOKEN_BATCH):
+        t1 = min(T, t0 + _TOKEN_BATCH)
+        hist = S - T + 1 + torch.arange(t0, t1)
+        keys = torch.rand(t1 - t0, S, generator=g)
+        keys[pos[None, :] >= hist[:, None]] = -1.0
+        vals, sel = keys.topk(k, dim=1)
+        sel = sel.to(torch.int32)
+        sel[vals < 0] = -1
+        out[t0:t1, :k] = sel
+    if p_empty > 0:
+        out[torch.rand(T, generator=g) < p_empty] = -1
+    return out
+
+
+def make_masked_dense_inputs(T: int, S: int, h: int, dqk: int, dv: int, seed: int = 9000):
+    """Decompressed per-head inputs of the masked dense route: q [T, h, dqk], k [S, h, dqk]
+    and v [S, h, dv], each bf16(N(0, 1) * 0.5) like the latent query and cache."""
+    g = _gen(seed, 14)
+    q = (torch.randn(T, h, dqk, generator=g) * 0.5).to(torch.bfloat16)
+    k = (torch.randn(S, h, dqk, generator=g) * 0.5).to(torch.bfloat16)
+    v = (torch.randn(S, h, dv, generator=g) * 0.5).to(torch.bfloat16)
+    return q, k, v
