@@ -75,11 +75,28 @@ def _check(status: int) -> None:
         raise SparseMLAError(status, msg)
 
 
-def _stream_handle(stream) -> Optional[int]:
+def _device_of(tensors) -> torch.device:
+    """The one CUDA device that all (name, tensor) pairs live on; raises if there is none."""
+    dev = None
+    for name, t in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+    return dev
+
+
+def _stream_handle(stream, device: Optional[torch.device] = None) -> Optional[int]:
+    """Raw handle of `stream` (default: the current stream of `device`, else of the current
+    device).  A stream object must belong to `device`; a raw int handle is passed as is."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     if isinstance(stream, int):
         return stream
+    if device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return stream.cuda_stream
 
 
@@ -121,23 +138,23 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
     list.  Runs asynchronously on `stream` (default: torch's current stream).
     """
     T, h, topk, num_slots = _dims(q, kv_cache, indices, kv_format)
-    for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices)):
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    dev = _device_of((("q", q), ("kv_cache", kv_cache), ("indices", indices)))
     if scale is None:
         scale = D_QK ** -0.5
     if out is None:
-        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=dev)
     if lse is None:
-        lse = torch.empty((T, h), dtype=torch.float32, device=q.device)
+        lse = torch.empty((T, h), dtype=torch.float32, device=dev)
     if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
-    st = library().sparse_mla_fwd_ex(
-        q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
-        KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
-        _stream_handle(stream))
+    _device_of((("q", q), ("out", out), ("lse", lse)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_fwd_ex(
+            q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
+            KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
+            _stream_handle(stream, dev))
     _check(st)
     return out, lse
 
@@ -148,19 +165,20 @@ def sparse_mla_fwd_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: tor
     """sparse_mla_fwd with the library's static merge scratch: nothing is allocated, so out and
     lse are required (see include/sparse_mla.h for the rules on first call and streams)."""
     T, h, topk, num_slots = _dims(q, kv_cache, indices, kv_format)
-    for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices), ("out", out), ("lse", lse)):
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    dev = _device_of((("q", q), ("kv_cache", kv_cache), ("indices", indices), ("out", out),
+                      ("lse", lse)))
     if scale is None:
         scale = D_QK ** -0.5
     if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
-    _check(library().sparse_mla_fwd_noalloc(
-        q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
-        KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
-        _stream_handle(stream)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_fwd_noalloc(
+            q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
+            KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
+            _stream_handle(stream, dev))
+    _check(st)
 
 
 def sparse_mla_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
@@ -177,21 +195,23 @@ def sparse_mla_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
     n, T, h = int(o_parts.shape[0]), int(o_parts.shape[1]), int(o_parts.shape[2])
     if lse_parts.shape != (n, T, h) or lse_parts.dtype != torch.float32:
         raise ValueError("lse_parts must be [n, T, h] fp32")
+    dev = _device_of((("o_parts", o_parts), ("lse_parts", lse_parts)))
     for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if out is None:
-        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=o_parts.device)
+        out = torch.empty((T, h, D_V), dtype=torch.bfloat16, device=dev)
     if lse is None:
-        lse = torch.empty((T, h), dtype=torch.float32, device=o_parts.device)
+        lse = torch.empty((T, h), dtype=torch.float32, device=dev)
     if out.shape != (T, h, D_V) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
-    _check(library().sparse_mla_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, T, h,
-                                      out.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
+    _device_of((("o_parts", o_parts), ("out", out), ("lse", lse)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, T, h,
+                                        out.data_ptr(), lse.data_ptr(), _stream_handle(stream, dev))
+    _check(st)
     return out, lse
 
 
@@ -206,17 +226,19 @@ def sparse_mla_v_up(o: torch.Tensor, w: torch.Tensor, *, out: Optional[torch.Ten
     if w.dim() != 3 or w.shape[0] != h or w.shape[2] != D_V or w.dtype != torch.bfloat16:
         raise ValueError("w must be [h, v, 512] bf16")
     v = int(w.shape[1])
+    dev = _device_of((("o", o), ("w", w)))
     for name, t in (("o", o), ("w", w)):
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if out is None:
-        out = torch.empty((T, h, v), dtype=torch.bfloat16, device=o.device)
+        out = torch.empty((T, h, v), dtype=torch.bfloat16, device=dev)
     if out.shape != (T, h, v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, h, v] bf16 tensor")
-    _check(library().sparse_mla_v_up(o.data_ptr(), w.data_ptr(), T, h, v, out.data_ptr(),
-                                     _stream_handle(stream)))
+    _device_of((("o", o), ("out", out)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_v_up(o.data_ptr(), w.data_ptr(), T, h, v, out.data_ptr(),
+                                       _stream_handle(stream, dev))
+    _check(st)
     return out
 
 
@@ -236,18 +258,20 @@ def sparse_mla_topk(scores: torch.Tensor, lengths: torch.Tensor, topk: int, *,
         if block_table.dim() != 1 or block_table.dtype != torch.int32 or block_table.numel() * 64 < S:
             raise ValueError("block_table must be [ceil(S / 64)] int32")
         tensors.append(("block_table", block_table))
+    dev = _device_of(tensors)
     for name, t in tensors:
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if out is None:
-        out = torch.empty((T, topk), dtype=torch.int32, device=scores.device)
+        out = torch.empty((T, topk), dtype=torch.int32, device=dev)
     if out.shape != (T, topk) or out.dtype != torch.int32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, topk] int32 tensor")
-    _check(library().sparse_mla_topk(scores.data_ptr(), T, S, lengths.data_ptr(), int(topk),
-                                     None if block_table is None else block_table.data_ptr(),
-                                     out.data_ptr(), _stream_handle(stream)))
+    _device_of((("scores", scores), ("out", out)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_topk(scores.data_ptr(), T, S, lengths.data_ptr(), int(topk),
+                                       None if block_table is None else block_table.data_ptr(),
+                                       out.data_ptr(), _stream_handle(stream, dev))
+    _check(st)
     return out
 
 
@@ -263,12 +287,13 @@ def sparse_mla_fwd_host(q_host: torch.Tensor, kv_cache: torch.Tensor, indices_ho
     T, h, topk, num_slots = _dims(q_host, kv_cache, indices_host, kv_format)
     if q_host.is_cuda or indices_host.is_cuda or out_host.is_cuda or lse_host.is_cuda:
         raise ValueError("q, indices, out and lse must be host tensors here")
-    if not kv_cache.is_cuda or not workspace.is_cuda:
-        raise ValueError("kv_cache and workspace must be CUDA tensors")
-    st = library().sparse_mla_fwd_host(
-        q_host.data_ptr(), kv_cache.data_ptr(), indices_host.data_ptr(), T, h, topk, num_slots,
-        KV_FORMATS[kv_format], float(scale), out_host.data_ptr(), lse_host.data_ptr(),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    dev = _device_of((("kv_cache", kv_cache), ("workspace", workspace)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_fwd_host(
+            q_host.data_ptr(), kv_cache.data_ptr(), indices_host.data_ptr(), T, h, topk,
+            num_slots, KV_FORMATS[kv_format], float(scale), out_host.data_ptr(),
+            lse_host.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream, dev))
     _check(st)
 
 
