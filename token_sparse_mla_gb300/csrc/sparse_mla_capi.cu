@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -571,17 +572,20 @@ smla_status sparse_mla_merge(const void* o_parts, const float* lse_parts, int32_
     mp.rows = static_cast<int64_t>(T) * h;
     mp.n = n_parts;
     // one warp per row, eight rows per CTA; a grid of the CTAs that fit on the device at once
-    // strides over the rows (their count is asked of the runtime once per device)
-    static int resident[kMaxDevices];
-    if (resident[dev] == 0) {
+    // strides over the rows (their count is asked of the runtime once per device; threads
+    // that race here ask twice and store the same value)
+    static std::atomic<int> resident[kMaxDevices];
+    int per_dev = resident[dev].load(std::memory_order_relaxed);
+    if (per_dev == 0) {
         int per_sm = 0;
         const cudaError_t oe =
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, smla::sparse_mla_merge_kernel, smla::kMergeThreads, 0);
         if (oe != cudaSuccess) return cuda_fail(oe, "occupancy of the merge kernel");
-        resident[dev] = per_sm > 0 ? per_sm : 1;
+        per_dev = per_sm > 0 ? per_sm : 1;
+        resident[dev].store(per_dev, std::memory_order_relaxed);
     }
     const int64_t want = (mp.rows + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(ds->num_sms) * resident[dev];
+    const int64_t cap = static_cast<int64_t>(ds->num_sms) * per_dev;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
     cfg.blockDim = dim3(smla::kMergeThreads, 1, 1);
