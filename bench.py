@@ -227,6 +227,115 @@ def workload_config(w, args, splits, rot, ctas=None):
                   f"{rot} x gathered bytes >= 2 x L2"}
 
 
+def gpu_busy_wait(stream, us: float = 200.0):
+    """Keep the GPU busy for about `us` microseconds on `stream` (torch's spin kernel), so the
+    launches queued behind it by the host start back to back when it ends: a timed window that
+    opens right after it measures the device, not the host's launch latency."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2000))
+
+
+def median_of_windows(replay, steps_per_replay: int, stream, n_windows: int = 10, min_window_ms: float = 1.0):
+    """Median over n_windows CUDA-event windows of the time per step; each window replays
+    enough graphs to last at least min_window_ms.  Returns (ms per step, replays per window)."""
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_busy_wait(stream)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    est = max(ev0.elapsed_time(ev1), 1e-3)
+    k = max(1, math.ceil(min_window_ms / est))
+    times = []
+    for _ in range(n_windows):
+        gpu_busy_wait(stream, min(2000.0, 200.0 + 20.0 * k))
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(k):
+                replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    return statistics.median(times) / (k * steps_per_replay), k
+
+
+def forward_graph(q, kv, idx, scale, out, lse, kv_format, stream, n_steps):
+    """A CUDA graph of n_steps forward calls on the same buffers."""
+    import token_sparse_mla_gb300 as smla
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            smla.sparse_mla_fwd(q, kv, idx, scale, out=out, lse=lse, kv_format=kv_format, stream=stream)
+    smla.sync_status(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n_steps):
+            smla.sparse_mla_fwd(q, kv, idx, scale, out=out, lse=lse, kv_format=kv_format, stream=stream)
+    return g
+
+
+def roofline_fields(h: int, gbytes: float, row_bytes: int, ms: float, peaks: dict) -> dict:
+    """Bound, achieved figure and fraction of one launch: 64 heads fill the MMA tile, so the
+    tensor roofline bounds them; fewer heads are bound by the gathered HBM bytes."""
+    gbps = gbytes / (ms * 1e-3) / 1e9
+    if h >= 64:
+        tfl = gbytes / row_bytes * flops_per_entry(h) / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": tfl, "unit": "TFLOP/s", "peak": peaks["bf16_tflops_sustained"],
+                "frac": tfl / peaks["bf16_tflops_sustained"], "gathered_gbps": gbps,
+                "hbm_frac": gbps / peaks["hbm_gbs"]}
+    return {"bound": "hbm", "achieved": gbps, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "frac": gbps / peaks["hbm_gbs"], "gathered_gbps": gbps}
+
+
+def per_config_runs(args, dev, stream, peaks: dict, main_entry: dict) -> dict:
+    """Every single-GPU configuration beside the headline one, timed in the same run as the
+    median of >= 10 CUDA-event windows of >= 1 ms (graphs of consecutive steps): the head-count
+    sweep native and padded to 64 heads, the prefill chunk, and the fp8 batch native and padded."""
+    res = {"decode_bf16": main_entry}
+
+    def run(key, name, q, kv, idx, scale, row_bytes, kv_format, h_real):
+        T, H = int(q.shape[0]), int(q.shape[1])
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        gb = gathered_bytes(idx, int(kv.shape[0]), row_bytes)
+        qd, kvd, idd = q.to(dev), kv.to(dev), idx.to(dev)
+        g1 = forward_graph(qd, kvd, idd, scale, out, lse, kv_format, stream, 1)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            g1.replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        n = max(1, min(32, math.ceil(1.0 / max(ev0.elapsed_time(ev1), 1e-3))))
+        g = forward_graph(qd, kvd, idd, scale, out, lse, kv_format, stream, n) if n > 1 else g1
+        ms, k = median_of_windows(g.replay, n, stream)
+        import token_sparse_mla_gb300 as smla
+        smla.sync_status(stream)
+        e = {"workload": name, "T": T, "h": H, "h_real": h_real, "padded_to_64": H != h_real,
+             "kv_format": kv_format, "ms": ms, "query_tokens_per_s": T / (ms * 1e-3),
+             "windows": 10, "steps_per_window": k * n, "gathered_bytes": gb,
+             "kernel": kernel_name(H), **roofline_fields(H, gb, row_bytes, ms, peaks)}
+        res[key] = e
+        del qd, kvd, idd, out, lse, g, g1
+        torch.cuda.synchronize(dev)
+
+    sw = make_workload("sweep", h=64)
+    for h in (8, 16, 32, 64):
+        qh = sw.q[:, :h].contiguous()
+        run(f"sweep_h{h}", "sweep", qh, sw.kv, sw.indices, sw.scale, 1152, "bf16", h)
+        if h < 64:
+            run(f"sweep_h{h}_pad64", "sweep", pad_heads(qh, 64), sw.kv, sw.indices, sw.scale, 1152, "bf16", h)
+    del sw
+    pf = make_workload("prefill")
+    run("prefill", "prefill", pf.q, pf.kv, pf.indices, pf.scale, 1152, "bf16", 64)
+    del pf
+    f8 = make_workload("fp8_mixed")
+    run("fp8_mixed", "fp8_mixed", f8.q, f8.kv, f8.indices, f8.scale, 656, "fp8", 8)
+    run("fp8_mixed_pad64", "fp8_mixed", pad_heads(f8.q, 64), f8.kv, f8.indices, f8.scale, 656, "fp8", 8)
+    del f8
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import token_sparse_mla_gb300 as smla
     dev = torch.device(f"cuda:{local_rank}")
@@ -307,6 +416,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_busy_wait(stream)  # the K steps below are queued while this runs
     ev0.record(stream)
     with torch.cuda.stream(stream):
         timed_steps(args.steps)
@@ -323,37 +433,58 @@ def run_ours(args, rank, world, local_rank):
     achieved = avg_gb / per_launch / 1e9
     traffic = ncu_traffic(name, base.h, args.pad)
 
-    # ---- end to end through the host-buffer entry point: H2D inputs, kernel, D2H outputs
+    # the same workload as the median of >= 10 windows of >= 1 ms each
+    win = None
+    if args.launch == "graph":
+        ms_w, k_w = median_of_windows(graphs[0].replay, glen, stream)
+        win = {"ms_per_step": ms_w, "query_tokens_per_s": T / (ms_w * 1e-3), "windows": 10,
+               "steps_per_window": k_w * glen,
+               **roofline_fields(H, avg_gb, cfg.row_bytes, ms_w, peaks)}
+
+    # ---- end to end through the packed host-buffer entry point: one H2D copy of the step's
+    # inputs, the kernel and one D2H copy of its outputs per step; steps alternate between two
+    # streams with their own workspaces, so one step's copies overlap its neighbour's kernel
     e2e = None
     if not args.no_e2e:
-        qh = [w.q.contiguous().pin_memory() for w in sets]
-        ih = [w.indices.contiguous().pin_memory() for w in sets]
-        oh = [torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory() for _ in sets]
-        lh = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in sets]
-        ws = torch.empty(smla.host_workspace_bytes(T, H, topk), dtype=torch.uint8, device=dev)
+        lay = smla.host_io_layout(T, H, topk)
+        ins = []
+        for w in sets:
+            b = torch.empty(lay["in_bytes"], dtype=torch.uint8).pin_memory()
+            qv, iv, _, _ = smla.host_io_views(b, torch.empty(lay["out_bytes"], dtype=torch.uint8), T, H, topk)
+            qv.copy_(w.q)
+            iv.copy_(w.indices)
+            ins.append(b)
+        ss = [stream, torch.cuda.Stream(dev)]
+        obs = [torch.empty(lay["out_bytes"], dtype=torch.uint8).pin_memory() for _ in ss]
+        wss = [torch.empty(smla.host_workspace_bytes(T, H, topk), dtype=torch.uint8, device=dev) for _ in ss]
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
         def estep(i):
-            k = i % rot
-            smla.sparse_mla_fwd_host(qh[k], kvs[k], ih[k], sets[k].scale, oh[k], lh[k], ws,
-                                     kv_format=cfg.kv_format, stream=stream)
-        for i in range(max(3, args.warmup // 10)):
+            j, k = i % 2, i % rot
+            smla.sparse_mla_fwd_host_packed(ins[k], kvs[k], T, H, topk, sets[k].scale, obs[j], wss[j],
+                                            kv_format=cfg.kv_format, stream=ss[j])
+        for i in range(max(4, args.warmup // 10)):
             estep(i)
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0, e1, eb = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                      torch.cuda.Event())
+        gpu_busy_wait(ss[0])
+        e0.record(ss[0])
+        ss[1].wait_event(e0)
         for i in range(e2e_steps):
             estep(i)
-        e1.record(stream)
+        eb.record(ss[1])
+        ss[0].wait_event(eb)
+        e1.record(ss[0])
         barrier()
         t_e2e = e0.elapsed_time(e1) / 1e3
-        smla.sync_status(stream)
+        smla.sync_status(ss[0])
+        smla.sync_status(ss[1])
         t_e2e = max_over_ranks(t_e2e, world, dev)
-        h2d = qh[0].numel() * 2 + ih[0].numel() * 4
-        d2h = oh[0].numel() * 2 + lh[0].numel() * 4
-        e2e = {"value": world * T * e2e_steps / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "path": "sparse_mla_fwd_host (pinned host q/indices in, out/lse back; cache resident)"}
+        e2e = {"value": world * T * e2e_steps / t_e2e, "unit": UNIT, "h2d_bytes_per_step": lay["in_bytes"],
+               "d2h_bytes_per_step": lay["out_bytes"], "steps": e2e_steps,
+               "path": "sparse_mla_fwd_host_packed (pinned host [q | indices] in, [out | lse] back, one "
+                       "copy each way per step; two streams alternate; cache resident)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -362,15 +493,14 @@ def run_ours(args, rank, world, local_rank):
                "sample": f"{ntok} query tokens (the workload's first {min(base.T, 32)} tokens, "
                          f"repeated) in {el:.1f} s"}
 
+    rf = roofline_fields(H, avg_gb, cfg.row_bytes, per_launch * 1e3, peaks)
     if H >= 64:
         # 64 heads fill the MMA tile: the tensor roofline bounds the kernel (the gathered
         # bytes are reported beside it)
-        avg_entries = avg_gb / cfg.row_bytes
-        tflops = avg_entries * flops_per_entry(H) / per_launch / 1e12
-        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops_sustained"],
+        roof = {"bound": "tensor", "achieved": rf["achieved"], "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": rf["frac"],
                 "traffic": traffic, "peak_source": peaks["source"] + " (bf16 sustained)",
-                "per_launch_algorithmic_flops": avg_entries * flops_per_entry(H),
+                "per_launch_algorithmic_flops": avg_gb / cfg.row_bytes * flops_per_entry(H),
                 "hbm_frac": achieved / peaks["hbm_gbs"], "kernel": kernel_name(H)}
     else:
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
@@ -388,7 +518,26 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "clocks": clocks.summary(),
         "gpu_launches": info["launches"] * args.steps,
+        "median_of_windows": win,
     }
+    if (name == "decode_bf16" and not args.pad and args.h is None and not args.no_per_config
+            and args.launch == "graph"):
+        entry = dict(win or {})
+        entry.update({"workload": name, "T": T, "h": H, "h_real": H, "kv_format": cfg.kv_format})
+        pc = per_config_runs(args, dev, stream, peaks, entry)
+        line["per_config"] = pc
+
+        def ratio(nat, pad):
+            if nat in pc and pad in pc:
+                return pc[pad]["ms"] / pc[nat]["ms"]
+            return None
+        line["native_over_padded"] = {
+            "meaning": "time per token of the padded-to-64 arm / time per token of the native arm "
+                       "(> 1: the native path is faster)",
+            "sweep_h8": ratio("sweep_h8", "sweep_h8_pad64"),
+            "sweep_h16": ratio("sweep_h16", "sweep_h16_pad64"),
+            "sweep_h32": ratio("sweep_h32", "sweep_h32_pad64"),
+            "fp8_mixed_h8": ratio("fp8_mixed", "fp8_mixed_pad64")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -805,6 +954,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other configurations (timed beside the decode batch by default)")
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
                     help="replay the timed steps from CUDA graphs, or launch each step eagerly")
     ap.add_argument("--prerun", type=float, default=0.3,

@@ -43,8 +43,12 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).
  *   - A non-OK return means nothing was launched.  Device-side failures (a
- *     bounded wait inside the kernel that ran out) are recorded in a device
- *     error word and reported by sparse_mla_sync_status().
+ *     bounded wait inside the kernel that ran out; in checked mode, list
+ *     entries out of range) are recorded in a device error word and reported
+ *     by sparse_mla_sync_status().  After a launch that timed out, call
+ *     sparse_mla_sync_status() before any further call on the device: a
+ *     launch that gave up part-way may leave merge-scratch barrier words
+ *     mid-count, and sparse_mla_sync_status() is what clears them.
  *   - sparse_mla_last_error() gives a message for the last non-OK return of
  *     the calling host thread.
  */
@@ -68,7 +72,9 @@ typedef enum smla_status {
     SMLA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or scale */
     SMLA_ERR_UNSUPPORTED = 2,  /* head count or KV format this build does not run */
     SMLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
-    SMLA_ERR_TIMEOUT = 4       /* a bounded wait inside a kernel gave up */
+    SMLA_ERR_TIMEOUT = 4,      /* a bounded wait inside a kernel gave up */
+    SMLA_ERR_INDEX_RANGE = 5   /* checked mode: a list entry other than -1 was outside
+                                  [0, num_slots) (it was masked) */
 } smla_status;
 
 typedef enum smla_kv_format {
@@ -118,6 +124,24 @@ smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t
                               int32_t T, int32_t h, int32_t topk, int64_t num_slots,
                               int32_t kv_format, float scale, void* out, float* lse,
                               int32_t splits, void* stream);
+
+/*
+ * sparse_mla_fwd_checked -- sparse_mla_fwd_ex in checked mode.  Every list entry
+ * outside [0, num_slots) is masked exactly as in sparse_mla_fwd_ex (outputs are
+ * identical byte for byte); in addition, an entry other than -1 that is out of
+ * range (>= num_slots, or negative and not -1) sets a bit in the device error
+ * word, which the next sparse_mla_sync_status() returns as SMLA_ERR_INDEX_RANGE
+ * and clears.  -1 is the list padding and never counts.  No trap and no fault:
+ * the check is a vote over the entries the producer warps already hold, one
+ * atomic per warp that met a bad entry.  The index lists are fixed-width int32
+ * (vLLM PR #54951, Summary) with -1 for an unused entry; the checked mode is
+ * the device-side range check that stands in for a memory checker.  Arguments
+ * as sparse_mla_fwd_ex.
+ */
+smla_status sparse_mla_fwd_checked(const void* q, const void* kv_cache, const int32_t* indices,
+                                   int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                                   int32_t kv_format, float scale, void* out, float* lse,
+                                   int32_t splits, void* stream);
 
 /*
  * sparse_mla_fwd_noalloc -- sparse_mla_fwd_ex with the merge scratch taken from
@@ -203,6 +227,9 @@ smla_status sparse_mla_v_up(const void* o, const void* w, int32_t T, int32_t h, 
  *   lengths      device, [T] int32; values outside [0, S] are clamped
  *   block_table  device, [ceil(S / 64)] int32 of one sequence, or NULL
  *   indices      device, [T, topk] int32, caller-owned: sparse_mla_fwd's input
+ * One call serves the rows of one sequence (one block table): a mixed batch of
+ * several sequences takes one call per sequence, each on that sequence's rows
+ * of scores, lengths and indices.
  * T = 0 is a no-op.  Allocates nothing; asynchronous on `stream`.  Errors:
  * SMLA_ERR_INVALID_ARG for bad sizes (S < 1, topk outside [1, 2^20]), a null
  * pointer or misalignment; SMLA_ERR_CUDA if the launch fails.
@@ -229,11 +256,37 @@ smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_cache,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sparse_mla_fwd_host_packed -- sparse_mla_fwd_host with the per-step inputs in
+ * one host buffer and the outputs in another, so each call queues exactly one
+ * host-to-device copy, the kernel and one device-to-host copy on `stream`.
+ *   in_host    host, in_bytes: q ([T, h, 576] bf16) at offset 0, indices
+ *              ([T, topk] int32) at indices_offset
+ *   out_host   host, out_bytes: out ([T, h, 512] bf16) at offset 0, lse ([T, h]
+ *              fp32) at lse_offset
+ *   workspace  device, at least sparse_mla_host_workspace_bytes(T, h, topk)
+ *              bytes, 256-byte aligned, caller-owned
+ * sparse_mla_host_io_layout gives the sizes and offsets (the gaps are padding to
+ * 256 bytes, never read or written by the kernel).  Pinned host buffers make the
+ * copies asynchronous; the results are in out_host once `stream` has been
+ * synchronised.  Calls on different streams with their own workspaces may
+ * overlap one step's copies with another's kernel.
+ */
+smla_status sparse_mla_host_io_layout(int32_t T, int32_t h, int32_t topk, size_t* in_bytes,
+                                      size_t* indices_offset, size_t* out_bytes, size_t* lse_offset);
+smla_status sparse_mla_fwd_host_packed(const void* in_host, const void* kv_cache, int32_t T, int32_t h,
+                                       int32_t topk, int64_t num_slots, int32_t kv_format, float scale,
+                                       void* out_host, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
+/*
  * sparse_mla_sync_status -- synchronise `stream`, then read and clear the
  * device error word of the current device.  Returns SMLA_ERR_TIMEOUT if a
  * kernel gave up on a bounded wait since the last call (the device is then
  * synchronised and the barrier words of every merge scratch on it cleared),
- * SMLA_ERR_CUDA if the synchronisation failed, SMLA_OK otherwise.  Not for the
+ * else SMLA_ERR_INDEX_RANGE if a sparse_mla_fwd_checked launch met a list
+ * entry other than -1 outside [0, num_slots), SMLA_ERR_CUDA if the
+ * synchronisation failed, SMLA_OK otherwise.  The word is per device, so a
+ * report covers every launch on the device since the last read.  Not for the
  * hot path.
  */
 smla_status sparse_mla_sync_status(void* stream);
@@ -247,7 +300,9 @@ smla_status sparse_mla_launch_info(int32_t T, int32_t h, int32_t topk, int32_t k
                                    int32_t* splits, int32_t* ctas, int32_t* smem_bytes,
                                    int32_t* launches);
 
-/* Message for the calling thread's last non-OK return ("" if none). */
+/* Message for the calling thread's last non-OK return ("" if none).  The
+ * pointer is to a thread-local buffer owned by the library: valid until the
+ * next non-OK return on the same thread; the caller copies it if it keeps it. */
 const char* sparse_mla_last_error(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

@@ -86,6 +86,15 @@ def test_forward(fake):
     assert fake.entered == [CUDA0]
 
 
+def test_forward_checked(fake):
+    q, kv, idx, out, lse = _fwd_args()
+    smla.sparse_mla_fwd(q, kv, idx, 0.1, out=out, lse=lse, splits=4, checked=True)
+    assert fake.lib.calls == [("sparse_mla_fwd_checked", (q.data_ptr(), kv.data_ptr(), idx.data_ptr(), 3,
+                                                          8, 64, 100, 0, 0.1, out.data_ptr(), lse.data_ptr(),
+                                                          4, STREAM))]
+    assert fake.entered == [CUDA0]
+
+
 def test_forward_fp8_and_default_scale(fake):
     q, _, idx, out, lse = _fwd_args()
     kv = _d((100, 656), torch.uint8)
@@ -116,6 +125,24 @@ def test_forward_host(fake):
                                                        topk, 50, 0, 0.3, out.data_ptr(), lse.data_ptr(),
                                                        ws.data_ptr(), 4096, STREAM))]
     assert fake.entered == [CUDA0]
+
+
+def test_forward_host_packed(fake, monkeypatch):
+    T, h, topk = 4, 8, 64
+    monkeypatch.setattr(_binding, "host_io_layout",
+                        lambda T_, h_, k_: {"in_bytes": 100, "indices_offset": 64, "out_bytes": 80,
+                                           "lse_offset": 48})
+    inb = torch.zeros(100, dtype=torch.uint8)
+    outb = torch.zeros(80, dtype=torch.uint8)
+    kv = _d((50, 576), torch.bfloat16)
+    ws = _d((4096,), torch.uint8)
+    smla.sparse_mla_fwd_host_packed(inb, kv, T, h, topk, 0.3, outb, ws)
+    assert fake.lib.calls == [("sparse_mla_fwd_host_packed", (inb.data_ptr(), kv.data_ptr(), T, h, topk, 50, 0,
+                                                              0.3, outb.data_ptr(), ws.data_ptr(), 4096,
+                                                              STREAM))]
+    assert fake.entered == [CUDA0]
+    with pytest.raises(ValueError):
+        smla.sparse_mla_fwd_host_packed(torch.zeros(99, dtype=torch.uint8), kv, T, h, topk, 0.3, outb, ws)
 
 
 def test_merge(fake):

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_version(lib):
-    assert smla.version() == 10000
+    assert smla.version() == 10100
 
 
 def test_workspace_bytes(lib):
@@ -50,6 +50,26 @@ def test_workspace_bytes(lib):
     raw = T * h * 576 * 2 + T * topk * 4 + T * h * 512 * 2 + T * h * 4
     assert raw <= need <= raw + 4 * 256
     assert smla.host_workspace_bytes(0, 8, 2048) == 0
+
+
+def test_host_io_layout(lib):
+    T, h, topk = 32, 8, 2048
+    lay = smla.host_io_layout(T, h, topk)
+    q, i, o, l = T * h * 576 * 2, T * topk * 4, T * h * 512 * 2, T * h * 4
+    assert lay["indices_offset"] >= q and lay["indices_offset"] % 256 == 0
+    assert lay["in_bytes"] == lay["indices_offset"] + i
+    assert lay["lse_offset"] >= o and lay["lse_offset"] % 256 == 0
+    assert lay["out_bytes"] == lay["lse_offset"] + l
+    # the device workspace holds both packed regions back to back
+    assert lay["in_bytes"] + lay["out_bytes"] <= smla.host_workspace_bytes(T, h, topk)
+    inb = torch.zeros(lay["in_bytes"], dtype=torch.uint8)
+    outb = torch.zeros(lay["out_bytes"], dtype=torch.uint8)
+    qv, iv, ov, lv = smla.host_io_views(inb, outb, T, h, topk)
+    iv.fill_(-1)
+    assert int(inb[lay["indices_offset"]:].sum()) == 255 * i and int(inb[:q].sum()) == 0
+    lv.fill_(1.0)
+    assert qv.shape == (T, h, 576) and ov.shape == (T, h, 512) and lv.shape == (T, h)
+    assert outb[lay["lse_offset"]:].view(torch.float32).eq(1.0).all()
 
 
 def _call(lib, **kw):

@@ -145,6 +145,36 @@ def test_out_of_range_and_negative_indices_are_masked():
     check_case(q, kv, idx, 0.05, 4, what="masking split")
 
 
+@pytest.mark.parametrize("h,kv_format", [(8, "bf16"), (16, "bf16"), (32, "bf16"), (64, "bf16"),
+                                         (8, "fp8"), (64, "fp8")])
+def test_checked_mode_reports_out_of_range_entries(h, kv_format):
+    # checked mode masks exactly what the default mode masks (same bytes out) and, for entries
+    # other than -1 outside [0, num_slots), makes sync_status report SMLA_ERR_INDEX_RANGE once
+    if kv_format == "fp8":
+        q, kv, idx = _rand_fp8(17 + h, 4, h, 200, 1000, p_invalid=0.2)
+    else:
+        q, kv, idx = _rand(17 + h, 4, h, 200, 1000, p_invalid=0.2)
+    clean = idx.clone()
+    idx[0, 3] = 1000          # == num_slots
+    idx[1, 5] = 2_000_000_000
+    idx[2, 199] = -5          # last entry of a list
+    qd, kvd, idd, cld = q.to(DEV), kv.to(DEV), idx.to(DEV), clean.to(DEV)
+    for splits in (0, 1, 4):
+        ref_o, ref_l = smla.sparse_mla_fwd(qd, kvd, idd, 0.05, splits=splits, kv_format=kv_format)
+        smla.sync_status()  # the default mode masks silently
+        o, l = smla.sparse_mla_fwd(qd, kvd, idd, 0.05, splits=splits, kv_format=kv_format, checked=True)
+        with pytest.raises(smla.SparseMLAError) as e:
+            smla.sync_status()
+        assert e.value.status == 5
+        smla.sync_status()  # read once, then cleared
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+        # -1 padding and in-range entries never count
+        smla.sparse_mla_fwd(qd, kvd, cld, 0.05, splits=splits, kv_format=kv_format, checked=True)
+        smla.sync_status()
+    ref_o, ref_l = oracle.sparse_mla_fwd(q, kv, idx, 0.05, kv_format=kv_format)
+    assert_parity(o.cpu(), l.cpu(), ref_o, ref_l, what=f"checked h={h} {kv_format}")
+
+
 def test_all_invalid_lists():
     q, kv, idx = _rand(8, 6, 32, 300, 500)
     idx[:] = -1
@@ -268,6 +298,24 @@ def test_host_entry_point_matches_device_path():
     smla.sparse_mla_fwd_host(qh, kv, ih, w.scale, oh, lh, ws)
     smla.sync_status()
     assert torch.equal(oh, out_d.cpu()) and torch.equal(lh, lse_d.cpu())
+
+
+def test_packed_host_entry_point_matches_device_path():
+    w = wl("decode_bf16", n_seq=5)
+    kv = w.kv.to(DEV)
+    out_d, lse_d = smla.sparse_mla_fwd(w.q.to(DEV), kv, w.indices.to(DEV), w.scale)
+    lay = smla.host_io_layout(w.T, w.h, w.topk)
+    inb = torch.full((lay["in_bytes"],), 0xAB, dtype=torch.uint8).pin_memory()
+    outb = torch.full((lay["out_bytes"],), 0xCD, dtype=torch.uint8).pin_memory()
+    qv, iv, ov, lv = smla.host_io_views(inb, outb, w.T, w.h, w.topk)
+    qv.copy_(w.q)
+    iv.copy_(w.indices)
+    ws = torch.empty(smla.host_workspace_bytes(w.T, w.h, w.topk), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        smla.sparse_mla_fwd_host_packed(inb, kv, w.T, w.h, w.topk, w.scale, outb, ws, stream=s)
+        smla.sync_status(s)
+        assert torch.equal(ov, out_d.cpu()) and torch.equal(lv, lse_d.cpu())
 
 
 def test_padded_matches_native():

@@ -18,12 +18,15 @@ index lists from per-position scores.
 from ._binding import (  # noqa: F401
     KV_FORMATS,
     SparseMLAError,
+    host_io_layout,
+    host_io_views,
     host_workspace_bytes,
     launch_info,
     lib_path,
     library,
     sparse_mla_fwd,
     sparse_mla_fwd_host,
+    sparse_mla_fwd_host_packed,
     sparse_mla_fwd_noalloc,
     sparse_mla_merge,
     sparse_mla_topk,
@@ -35,12 +38,15 @@ from ._binding import (  # noqa: F401
 __all__ = [
     "KV_FORMATS",
     "SparseMLAError",
+    "host_io_layout",
+    "host_io_views",
     "host_workspace_bytes",
     "launch_info",
     "lib_path",
     "library",
     "sparse_mla_fwd",
     "sparse_mla_fwd_host",
+    "sparse_mla_fwd_host_packed",
     "sparse_mla_fwd_noalloc",
     "sparse_mla_merge",
     "sparse_mla_topk",

@@ -13,10 +13,13 @@ KV_FORMATS = {"bf16": 0, "fp8": 1}
 D_QK, D_V, FP8_ROW_BYTES = 576, 512, 656
 
 _STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED",
-           3: "SMLA_ERR_CUDA", 4: "SMLA_ERR_TIMEOUT"}
+           3: "SMLA_ERR_CUDA", 4: "SMLA_ERR_TIMEOUT", 5: "SMLA_ERR_INDEX_RANGE"}
+SMLA_ERR_INDEX_RANGE = 5
 
-EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_ex", "sparse_mla_fwd_host",
-            "sparse_mla_host_workspace_bytes", "sparse_mla_sync_status",
+EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_ex", "sparse_mla_fwd_checked", "sparse_mla_fwd_noalloc",
+            "sparse_mla_fwd_host", "sparse_mla_fwd_host_packed", "sparse_mla_host_io_layout",
+            "sparse_mla_host_workspace_bytes", "sparse_mla_merge",
+            "sparse_mla_v_up", "sparse_mla_topk", "sparse_mla_sync_status",
             "sparse_mla_launch_info", "sparse_mla_last_error", "sparse_mla_version")
 
 
@@ -45,6 +48,8 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp]
     lib.sparse_mla_fwd_ex.restype = ctypes.c_int
     lib.sparse_mla_fwd_ex.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
+    lib.sparse_mla_fwd_checked.restype = ctypes.c_int
+    lib.sparse_mla_fwd_checked.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_fwd_noalloc.restype = ctypes.c_int
     lib.sparse_mla_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, i32, vp]
     lib.sparse_mla_topk.restype = ctypes.c_int
@@ -57,6 +62,10 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_host_workspace_bytes.argtypes = [i32, i32, i32]
     lib.sparse_mla_fwd_host.restype = ctypes.c_int
     lib.sparse_mla_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp, sz, vp]
+    lib.sparse_mla_host_io_layout.restype = ctypes.c_int
+    lib.sparse_mla_host_io_layout.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.sparse_mla_fwd_host_packed.restype = ctypes.c_int
+    lib.sparse_mla_fwd_host_packed.argtypes = [vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, sz, vp]
     lib.sparse_mla_sync_status.restype = ctypes.c_int
     lib.sparse_mla_sync_status.argtypes = [vp]
     lib.sparse_mla_launch_info.restype = ctypes.c_int
@@ -129,13 +138,17 @@ def _dims(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor, kv_for
 def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
                    scale: Optional[float] = None, *, out: Optional[torch.Tensor] = None,
                    lse: Optional[torch.Tensor] = None, kv_format: str = "bf16",
-                   splits: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   splits: int = 0, checked: bool = False,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Token-sparse MLA forward on the GPU (see include/sparse_mla.h).
 
     scale defaults to 576 ** -0.5.  out / lse may be passed in (caller-owned
     buffers, [T, h, 512] bf16 and [T, h] fp32); otherwise they are allocated
     here.  splits = 0 lets the library choose how many CTAs share a token's
-    list.  Runs asynchronously on `stream` (default: torch's current stream).
+    list.  checked = True runs sparse_mla_fwd_checked: the same outputs, and list
+    entries other than -1 outside [0, num_slots) make the next sync_status()
+    raise SMLA_ERR_INDEX_RANGE.  Runs asynchronously on `stream` (default:
+    torch's current stream).
     """
     T, h, topk, num_slots = _dims(q, kv_cache, indices, kv_format)
     dev = _device_of((("q", q), ("kv_cache", kv_cache), ("indices", indices)))
@@ -151,7 +164,9 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
     _device_of((("q", q), ("out", out), ("lse", lse)))
     with torch.cuda.device(dev):
-        st = library().sparse_mla_fwd_ex(
+        lib = library()
+        fn = lib.sparse_mla_fwd_checked if checked else lib.sparse_mla_fwd_ex
+        st = fn(
             q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
             KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
             _stream_handle(stream, dev))
@@ -294,6 +309,54 @@ def sparse_mla_fwd_host(q_host: torch.Tensor, kv_cache: torch.Tensor, indices_ho
             num_slots, KV_FORMATS[kv_format], float(scale), out_host.data_ptr(),
             lse_host.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             _stream_handle(stream, dev))
+    _check(st)
+
+
+def host_io_layout(T: int, h: int, topk: int) -> dict:
+    """Sizes and offsets of the packed host buffers of sparse_mla_fwd_host_packed."""
+    a, b, c, d = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(library().sparse_mla_host_io_layout(T, h, topk, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                               ctypes.byref(d)))
+    return {"in_bytes": a.value, "indices_offset": b.value, "out_bytes": c.value, "lse_offset": d.value}
+
+
+def host_io_views(in_host: torch.Tensor, out_host: torch.Tensor, T: int, h: int, topk: int):
+    """Views of q / indices inside a packed input buffer and of out / lse inside a packed output
+    buffer (uint8 host tensors of the sizes host_io_layout gives)."""
+    lay = host_io_layout(T, h, topk)
+    if in_host.dtype != torch.uint8 or in_host.numel() < lay["in_bytes"]:
+        raise ValueError(f"in_host must be a uint8 tensor of at least {lay['in_bytes']} bytes")
+    if out_host.dtype != torch.uint8 or out_host.numel() < lay["out_bytes"]:
+        raise ValueError(f"out_host must be a uint8 tensor of at least {lay['out_bytes']} bytes")
+    i0, l0 = lay["indices_offset"], lay["lse_offset"]
+    q = in_host[: T * h * D_QK * 2].view(torch.bfloat16).view(T, h, D_QK)
+    idx = in_host[i0: i0 + T * topk * 4].view(torch.int32).view(T, topk)
+    out = out_host[: T * h * D_V * 2].view(torch.bfloat16).view(T, h, D_V)
+    lse = out_host[l0: l0 + T * h * 4].view(torch.float32).view(T, h)
+    return q, idx, out, lse
+
+
+def sparse_mla_fwd_host_packed(in_host: torch.Tensor, kv_cache: torch.Tensor, T: int, h: int, topk: int,
+                               scale: float, out_host: torch.Tensor, workspace: torch.Tensor, *,
+                               kv_format: str = "bf16", stream=None) -> None:
+    """Forward pass from one packed host input buffer into one packed host output buffer
+    (include/sparse_mla.h): one H2D copy, the kernel and one D2H copy queued on `stream`."""
+    if in_host.is_cuda or out_host.is_cuda:
+        raise ValueError("in_host and out_host must be host tensors")
+    for name, t in (("in_host", in_host), ("out_host", out_host)):
+        if t.dtype != torch.uint8 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 tensor")
+    if kv_format not in KV_FORMATS:
+        raise ValueError(f"kv_format must be one of {sorted(KV_FORMATS)}")
+    lay = host_io_layout(T, h, topk)
+    if in_host.numel() < lay["in_bytes"] or out_host.numel() < lay["out_bytes"]:
+        raise ValueError("in_host / out_host smaller than host_io_layout says")
+    dev = _device_of((("kv_cache", kv_cache), ("workspace", workspace)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_fwd_host_packed(
+            in_host.data_ptr(), kv_cache.data_ptr(), T, h, topk, int(kv_cache.shape[0]),
+            KV_FORMATS[kv_format], float(scale), out_host.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _check(st)
 
 

@@ -21,7 +21,7 @@
 
 namespace {
 
-constexpr int32_t kVersion = 10000;  // 1.0.0
+constexpr int32_t kVersion = 10100;  // 1.1.0: checked mode, packed host buffers
 constexpr int kMaxDevices = 64;
 
 thread_local char g_last_error[512] = "";
@@ -316,7 +316,7 @@ enum class ScratchSource { kStream, kStatic };
 smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T, int32_t h,
                    int32_t topk, int64_t num_slots, int32_t kv_format, float scale, void* out,
                    float* lse, int32_t splits, cudaStream_t stream,
-                   ScratchSource source = ScratchSource::kStream) {
+                   ScratchSource source = ScratchSource::kStream, bool checked = false) {
     smla_status st = check_args(q, kv, idx, T, h, topk, num_slots, kv_format, scale, out, lse, splits);
     if (st != SMLA_OK || T == 0) return st;
     int dev = 0;
@@ -356,6 +356,7 @@ smla_status launch(const void* q, const void* kv, const int32_t* idx, int32_t T,
     prm.nblk = pl.nblk;
     prm.part = nullptr;
     prm.gbar = nullptr;
+    prm.checked = checked ? 1 : 0;
     if (pl.scratch > 0) {
         void* sp = nullptr;
         if (source == ScratchSource::kStatic) {
@@ -442,6 +443,14 @@ smla_status sparse_mla_fwd_ex(const void* q, const void* kv_cache, const int32_t
                   static_cast<cudaStream_t>(stream));
 }
 
+smla_status sparse_mla_fwd_checked(const void* q, const void* kv_cache, const int32_t* indices,
+                                   int32_t T, int32_t h, int32_t topk, int64_t num_slots,
+                                   int32_t kv_format, float scale, void* out, float* lse,
+                                   int32_t splits, void* stream) {
+    return launch(q, kv_cache, indices, T, h, topk, num_slots, kv_format, scale, out, lse, splits,
+                  static_cast<cudaStream_t>(stream), ScratchSource::kStream, true);
+}
+
 smla_status sparse_mla_fwd_noalloc(const void* q, const void* kv_cache, const int32_t* indices,
                                    int32_t T, int32_t h, int32_t topk, int64_t num_slots,
                                    int32_t kv_format, float scale, void* out, float* lse,
@@ -495,6 +504,54 @@ smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_cache, const 
     return SMLA_OK;
 }
 
+smla_status sparse_mla_host_io_layout(int32_t T, int32_t h, int32_t topk, size_t* in_bytes,
+                                      size_t* indices_offset, size_t* out_bytes, size_t* lse_offset) {
+    if (T < 0 || h <= 0 || topk <= 0)
+        return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d h=%d topk=%d", T, h, topk);
+    const size_t t = static_cast<size_t>(T);
+    const size_t q_bytes = t * h * smla::kDQK * 2, i_bytes = t * topk * 4;
+    const size_t o_bytes = t * h * smla::kDV * 2, l_bytes = t * h * 4;
+    if (in_bytes) *in_bytes = T == 0 ? 0 : align256(q_bytes) + i_bytes;
+    if (indices_offset) *indices_offset = align256(q_bytes);
+    if (out_bytes) *out_bytes = T == 0 ? 0 : align256(o_bytes) + l_bytes;
+    if (lse_offset) *lse_offset = align256(o_bytes);
+    return SMLA_OK;
+}
+
+smla_status sparse_mla_fwd_host_packed(const void* in_host, const void* kv_cache, int32_t T, int32_t h,
+                                       int32_t topk, int64_t num_slots, int32_t kv_format, float scale,
+                                       void* out_host, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (T < 0 || h <= 0 || topk <= 0)
+        return check_args(in_host, kv_cache, static_cast<const int32_t*>(in_host), T, h, topk, num_slots,
+                          kv_format, scale, out_host, static_cast<const float*>(out_host), 0);
+    if (T == 0)
+        return check_args(nullptr, kv_cache, nullptr, 0, h, topk, num_slots, kv_format, scale, nullptr,
+                          nullptr, 0);
+    if (!in_host || !out_host || !workspace) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(workspace, 256)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = sparse_mla_host_workspace_bytes(T, h, topk);
+    if (workspace_bytes < need)
+        return fail(SMLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, need);
+    size_t in_bytes = 0, i_off = 0, out_bytes = 0, l_off = 0;
+    sparse_mla_host_io_layout(T, h, topk, &in_bytes, &i_off, &out_bytes, &l_off);
+    const size_t t = static_cast<size_t>(T);
+    const size_t o_off = i_off + align256(t * topk * 4);  // device: [q | idx | out | lse]
+    char* w = static_cast<char*>(workspace);
+    const int32_t* i_dev = reinterpret_cast<const int32_t*>(w + i_off);
+    float* l_dev = reinterpret_cast<float*>(w + o_off + l_off);
+    smla_status st = check_args(w, kv_cache, i_dev, T, h, topk, num_slots, kv_format, scale, w + o_off, l_dev, 0);
+    if (st != SMLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(w, in_host, in_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    st = launch(w, kv_cache, i_dev, T, h, topk, num_slots, kv_format, scale, w + o_off, l_dev, 0, s);
+    if (st != SMLA_OK) return st;
+    e = cudaMemcpyAsync(out_host, w + o_off, out_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return SMLA_OK;
+}
+
 smla_status sparse_mla_sync_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
@@ -517,9 +574,13 @@ smla_status sparse_mla_sync_status(void* stream) {
                 if (dev >= 0 && dev < kMaxDevices && g_dev[dev].static_ptr)
                     cudaMemset(g_dev[dev].static_ptr, 0, kScratchHead);
             }
-            return fail(SMLA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (error word 0x%x)", word);
+            return fail(SMLA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (error word 0x%x%s)", word,
+                        (word & smla::kErrIndexRange) ? "; a checked launch also met out-of-range list entries" : "");
         }
-        return fail(SMLA_ERR_CUDA, "kernel reported an error (error word 0x%x)", word);
+        if (word & smla::kErrLayout)
+            return fail(SMLA_ERR_CUDA, "kernel reported an error (error word 0x%x)", word);
+        return fail(SMLA_ERR_INDEX_RANGE,
+                    "a checked launch met list entries other than -1 outside [0, num_slots); they were masked");
     }
     return SMLA_OK;
 }

@@ -26,6 +26,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;    // draining in-flight work a
 // device error word bits (read by sparse_mla_sync_status)
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrLayout = 2u;
+constexpr unsigned int kErrIndexRange = 4u;         // checked mode: an entry other than -1 was invalid
 
 struct FwdParams {
     const __nv_bfloat16* q;   // [T, h, 576]
@@ -43,9 +44,19 @@ struct FwdParams {
     int32_t grid, nblk;
     float* part;
     unsigned int* gbar;
+    // checked mode: list entries other than -1 outside [0, num_slots) are still masked, and the
+    // producers also set kErrIndexRange in the device error word
+    int32_t checked;
 };
 
 __device__ unsigned int g_smla_error;
+
+// Checked mode: one warp-wide vote over the raw entries this warp's lanes hold (-1 never
+// counts), and one atomic per warp that found an out-of-range entry.
+__device__ __forceinline__ void flag_out_of_range(int raw, int slot) {
+    const bool bad = raw != -1 && slot < 0;
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&g_smla_error, kErrIndexRange);
+}
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -55,7 +66,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return static_cast<uint32_t>(bf16_bits(lo)) | (static_cast<uint32_t>(bf16_bits(hi)) << 16);
 }
 
-// Slot of list entry j, or -1 when j is past this CTA's range or the index is invalid.
 // Raw list entry j of a row (-1 when j is past the CTA's range or pred is false).  The load is
 // not checked here: the check reads the value, and a read right after the load would wait for
 // it.  Callers hold raw entries in a ring and check them with valid_slot when they are used.
@@ -114,6 +124,7 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
             if (b >= nb) break;
             const int s = b % NST;
             const int my_slot = valid_slot(ring[u], p.num_slots);
+            if (p.checked) flag_out_of_range(ring[u], my_slot);
             ring[u] = fetch_entry(idx_row, j0 + (b + kAhead) * kRows + my_row, j1, row_owner && b + kAhead < nb);
             if constexpr (KVF == 0) {
                 if (b >= NST) {

@@ -251,6 +251,7 @@ __device__ __forceinline__ void small_gather(const FwdParams& p, int64_t x0, int
             const int s = b % NST;
             const uint32_t full = bar_full0 + 8u * s;
             const int my_slot = valid_slot(ring[u], p.num_slots);  // slot of row `lane`
+            if (p.checked && mask_warp) flag_out_of_range(ring[u], my_slot);
             if constexpr (KVF == 1) {
                 // raw rows of block b + kSmRawStages - 1 (their entries sit in the ring already)
                 const int ahead = valid_slot(ring[(u + kSmRawStages - 1) % kAhead], p.num_slots);
