@@ -17,7 +17,9 @@ same workload, a bounded number of tokens per step.
 --workload dcp_merge times sparse_mla_merge instead: the combine of 4 split-list
 partial results per row at the fp8 batch's shape (T = 32768, h = 8); --workload
 v_up times sparse_mla_v_up (T = 32768, h = 8, v_head_dim 128); --workload topk times
-sparse_mla_topk (the prefill chunk's 16384 causal rows over 32768 positions, k = 2048).
+sparse_mla_topk (the prefill chunk's 16384 causal rows over 32768 positions, k = 2048);
+--workload masked_dense times the masked dense route (scatter of the lists into a bit mask,
+then masked MHA) on a 4096-token GLM-5 prefill chunk that is the whole request.
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path shards by query token with no exchange), weak scaling.
 """
@@ -940,6 +942,161 @@ def run_topk_reference(args, rank, world):
     }), flush=True)
 
 
+# ---- the masked dense route: a GLM-5 prefill chunk that is the whole request
+MASKED_SHAPE = {"T": 4096, "S": 4096, "h": 64, "dqk": 256, "dv": 256, "topk": 2048}
+
+
+def masked_inputs(seed: int):
+    from workloads import causal_position_lists, make_masked_dense_inputs
+    m = MASKED_SHAPE
+    q, k, v = make_masked_dense_inputs(m["T"], m["S"], m["h"], m["dqk"], m["dv"], seed=seed)
+    lists = causal_position_lists(m["T"], m["S"], m["topk"], seed=seed + 1)
+    return q, k, v, lists
+
+
+def masked_tile_work(mask_words: torch.Tensor) -> dict:
+    """Dense work of the route: per 128-query tile, the 64-key tiles any of its rows attends to,
+    each a 128 x 64 block of QK^T and PV; beside it the masked-in (token, position) pairs."""
+    m = MASKED_SHAPE
+    T, W = mask_words.shape
+    nz = (mask_words != 0)
+    if W % 2:
+        nz = torch.cat([nz, torch.zeros(T, 1, dtype=torch.bool)], dim=1)
+    key_tiles = nz.view(T, -1, 2).any(dim=2)                      # [T, key tiles]
+    nq = (T + 127) // 128
+    pad = nq * 128 - T
+    if pad:
+        key_tiles = torch.cat([key_tiles, torch.zeros(pad, key_tiles.shape[1], dtype=torch.bool)])
+    active = int(key_tiles.view(nq, 128, -1).any(dim=1).sum().item())
+    import numpy as np
+    pairs = int(np.unpackbits(np.ascontiguousarray(mask_words.numpy()).view(np.uint8)).sum())
+    per_pair = 2 * m["h"] * (m["dqk"] + m["dv"])
+    return {"active_tiles": active, "tile_flops": active * 128 * 64 * per_pair,
+            "pairs": pairs, "pair_flops": pairs * per_pair}
+
+
+def masked_config(args) -> dict:
+    return {"workload": "masked_dense", **MASKED_SHAPE,
+            "geometry": "GLM-5: 64 heads, q/k 192 nope + 64 rope, v 256",
+            "inputs": "q, k, v ~ bf16(N(0, 1) * 0.5); lists = top-2048 of uniform keys over each causal history",
+            "launch": "CUDA graph of consecutive steps" if args.launch == "graph" else "eager launches",
+            "step": "sparse_mla_scatter_mask + sparse_mla_masked_mha"}
+
+
+def run_masked(args, rank, world, local_rank):
+    import numpy as np
+    import token_sparse_mla_gb300 as smla
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    m = MASKED_SHAPE
+    q_h, k_h, v_h, l_h = masked_inputs(9400 + 7919 * rank)
+    q_d, k_d, v_d, l_d = q_h.to(dev), k_h.to(dev), v_h.to(dev), l_h.to(dev)
+    W = (m["S"] + 31) // 32
+    mask = torch.empty((m["T"], W), dtype=torch.int32, device=dev)
+    out = torch.empty((m["T"], m["h"], m["dv"]), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((m["T"], m["h"]), dtype=torch.float32, device=dev)
+    scale = m["dqk"] ** -0.5
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        smla.sparse_mla_scatter_mask(l_d, m["S"], out=mask, stream=stream)
+        smla.sparse_mla_masked_mha(q_d, k_d, v_d, mask, scale, out=out, lse=lse, stream=stream)
+
+    def mha_only():
+        smla.sparse_mla_masked_mha(q_d, k_d, v_d, mask, scale, out=out, lse=lse, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    smla.sync_status(stream)
+    work = masked_tile_work(mask.cpu())
+    glen = 4
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(glen):
+                fn()
+        return g
+    g_step, g_mha = graph_of(step), graph_of(mha_only)
+    steps = max(glen, (args.steps // glen) * glen)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_busy_wait(stream)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps // glen):
+            g_step.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.stop()
+    t_dev = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    per_step = t_dev / steps
+    ms_mha, _ = median_of_windows(g_mha.replay, glen, stream)
+    smla.sync_status(stream)
+    peaks = measured_peaks()
+    tfl = work["tile_flops"] / (ms_mha * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        toks = [0, 1000, 2047, 3000, 4095]
+        mk = oracle.scatter_mask(l_h[toks], m["S"])
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < args.cpu_seconds or n == 0:
+            oracle.masked_mha(q_h[toks], k_h, v_h, mk, scale)
+            n += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": n * len(toks) / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"{len(toks)} query tokens (all 64 heads) attended {n} times in {el:.1f} s"}
+    line = {
+        "metric": METRIC, "value": world * m["T"] * steps / t_dev, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": masked_config(args),
+        "roofline": {"bound": "tensor", "achieved": tfl, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": tfl / peaks["bf16_tflops_sustained"], "traffic": ncu_traffic("masked_dense", m["h"], False),
+                     "peak_source": peaks["source"] + " (bf16 sustained)", "kernel": "sparse_mla_masked_mha_kernel",
+                     "per_launch_algorithmic_flops": work["tile_flops"], "kernel_ms": ms_mha,
+                     "flops_basis": "dense 128 x 64 tiles that hold a masked-in position",
+                     "masked_in_pair_flops": work["pair_flops"], "active_tiles": work["active_tiles"]},
+        "cpu_baseline": cpu, "e2e": None, "clocks": clocks.summary(), "gpu_launches": 2 * steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_masked_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    m = MASKED_SHAPE
+    q_h, k_h, v_h, l_h = masked_inputs(9400)
+    toks = [0, 2047, 4095]
+    scale = m["dqk"] ** -0.5
+    for _ in range(args.warmup):
+        oracle.masked_mha(q_h[toks[:1]], k_h, v_h, oracle.scatter_mask(l_h[toks[:1]], m["S"]), scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.masked_mha(q_h[toks], k_h, v_h, oracle.scatter_mask(l_h[toks], m["S"]), scale)
+    el = time.perf_counter() - t0
+    value = len(toks) * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": masked_config(args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{len(toks)} query tokens (all heads) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -964,7 +1121,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_setup(args)
-    if args.workload == "topk":
+    if args.workload == "masked_dense":
+        (run_masked_reference(args, rank, world) if args.impl == "reference"
+         else run_masked(args, rank, world, local_rank))
+    elif args.workload == "topk":
         (run_topk_reference(args, rank, world) if args.impl == "reference"
          else run_topk(args, rank, world, local_rank))
     elif args.workload == "v_up":

@@ -238,6 +238,56 @@ smla_status sparse_mla_topk(const float* scores, int32_t T, int64_t S, const int
                             const int32_t* block_table, int32_t* indices, void* stream);
 
 /*
+ * sparse_mla_scatter_mask -- the masked dense route's first step: the index
+ * lists of one request scattered into a bit mask.  PR #55738 report, 实现拆解
+ * (implementation breakdown) items 2 and 5: short prefills run a scatter of the
+ * top-k lists (_scatter_topk_single_req) and a dense attention with a mask
+ * instead of the per-token gather.  The report gives no layout; here row t of
+ * the mask has W = ceil(S / 32) uint32 words and bit s % 32 of word s / 32 is
+ * set iff position s appears in indices[t, :].  Entries outside [0, S) (-1 by
+ * convention) set nothing; a repeated position sets its bit once (the mask
+ * holds a set, where sparse_mla_fwd weighs every list entry).
+ *   indices   device, [T, topk] int32 positions of the request, 4-byte aligned
+ *   S         positions in the request, 1 .. 2^20
+ *   mask      device, [T, W] uint32, caller-owned, 16-byte aligned; every word
+ *             is written
+ * T = 0 is a no-op.  Allocates nothing; asynchronous on `stream`.  Errors:
+ * SMLA_ERR_INVALID_ARG for bad sizes, a null pointer or misalignment;
+ * SMLA_ERR_CUDA if the launch fails.
+ */
+smla_status sparse_mla_scatter_mask(const int32_t* indices, int32_t T, int32_t topk, int64_t S, uint32_t* mask,
+                                    void* stream);
+
+/*
+ * sparse_mla_masked_mha -- the masked dense route's attention: multi-head
+ * attention of T query tokens over the request's S positions with per-head
+ * K and V, in which the mask alone decides which positions each token attends
+ * to (the FA4 mask_mod attention of the same report).  Per token t and head h:
+ *     s_j = scale * <q[t,h,:], k[j,h,:]>   for the positions j set in mask[t]
+ *     O[t,h] = softmax(s) . v[:,h,:],   LSE[t,h] = ln sum_j exp(s_j)
+ * A row with no bit set gives O = 0 and LSE = -inf.  Head dims follow the
+ * report's `_is_masked_mha_available` geometry table: q/k 192 (128 nope + 64
+ * rope, DeepSeek-V3.2) or 256 (192 + 64, GLM-5; 256 + 0, the NoPE layout),
+ * v 128 or 256.  bf16 in, fp32 softmax and accumulation on the tcgen05 tensor
+ * cores, O rounded to bf16.
+ *   q      device, [T, h, dqk] bf16, 16-byte aligned
+ *   k      device, [S, h, dqk] bf16, 16-byte aligned
+ *   v      device, [S, h, dv] bf16, 16-byte aligned
+ *   mask   device, [T, ceil(S / 32)] uint32 as sparse_mla_scatter_mask writes
+ *          it, 4-byte aligned
+ *   S      1 .. 65536;  h >= 1;  dqk 192 or 256;  dv 128 or 256
+ *   out    device, [T, h, dv] bf16, caller-owned;  lse  device, [T, h] fp32
+ * T = 0 is a no-op.  Allocates nothing; asynchronous on `stream`.  Errors:
+ * SMLA_ERR_UNSUPPORTED for other head dims, SMLA_ERR_INVALID_ARG for bad sizes,
+ * scale, a null pointer or misalignment; SMLA_ERR_CUDA if a tensor map or the
+ * launch fails; a bounded wait that ran out is reported by
+ * sparse_mla_sync_status().
+ */
+smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, const uint32_t* mask, int32_t T,
+                                  int64_t S, int32_t h, int32_t dqk, int32_t dv, float scale, void* out, float* lse,
+                                  void* stream);
+
+/*
  * sparse_mla_fwd_host -- the same forward pass taking HOST buffers for the
  * per-step inputs and outputs, for callers whose q/indices live in host memory.
  * It queues on `stream`: copies of q_host and indices_host into `workspace`,

@@ -12,7 +12,9 @@ fp8 rows), indices [T, topk] int32 (-1 = invalid), h in {8, 16, 32, 64};
 returns out [T, h, 512] bf16 and lse [T, h] fp32.  sparse_mla_merge combines
 the (out, lse) of lists split into parts (the DCP merge); sparse_mla_v_up applies the
 per-head value up-projection to out on the tensor cores; sparse_mla_topk builds the
-index lists from per-position scores.
+index lists from per-position scores; sparse_mla_scatter_mask and sparse_mla_masked_mha are
+the masked dense route for short prefills (the lists as a bit mask, then dense MHA over per-head
+K and V under that mask).
 """
 
 from ._binding import (  # noqa: F401
@@ -28,7 +30,9 @@ from ._binding import (  # noqa: F401
     sparse_mla_fwd_host,
     sparse_mla_fwd_host_packed,
     sparse_mla_fwd_noalloc,
+    sparse_mla_masked_mha,
     sparse_mla_merge,
+    sparse_mla_scatter_mask,
     sparse_mla_topk,
     sparse_mla_v_up,
     sync_status,
@@ -48,7 +52,9 @@ __all__ = [
     "sparse_mla_fwd_host",
     "sparse_mla_fwd_host_packed",
     "sparse_mla_fwd_noalloc",
+    "sparse_mla_masked_mha",
     "sparse_mla_merge",
+    "sparse_mla_scatter_mask",
     "sparse_mla_topk",
     "sparse_mla_v_up",
     "sync_status",

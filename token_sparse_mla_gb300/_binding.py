@@ -19,7 +19,8 @@ SMLA_ERR_INDEX_RANGE = 5
 EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_ex", "sparse_mla_fwd_checked", "sparse_mla_fwd_noalloc",
             "sparse_mla_fwd_host", "sparse_mla_fwd_host_packed", "sparse_mla_host_io_layout",
             "sparse_mla_host_workspace_bytes", "sparse_mla_merge",
-            "sparse_mla_v_up", "sparse_mla_topk", "sparse_mla_sync_status",
+            "sparse_mla_v_up", "sparse_mla_topk", "sparse_mla_scatter_mask", "sparse_mla_masked_mha",
+            "sparse_mla_sync_status",
             "sparse_mla_launch_info", "sparse_mla_last_error", "sparse_mla_version")
 
 
@@ -62,6 +63,10 @@ def library() -> ctypes.CDLL:
     lib.sparse_mla_host_workspace_bytes.argtypes = [i32, i32, i32]
     lib.sparse_mla_fwd_host.restype = ctypes.c_int
     lib.sparse_mla_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i64, i32, f32, vp, vp, vp, sz, vp]
+    lib.sparse_mla_scatter_mask.restype = ctypes.c_int
+    lib.sparse_mla_scatter_mask.argtypes = [vp, i32, i32, i64, vp, vp]
+    lib.sparse_mla_masked_mha.restype = ctypes.c_int
+    lib.sparse_mla_masked_mha.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, f32, vp, vp, vp]
     lib.sparse_mla_host_io_layout.restype = ctypes.c_int
     lib.sparse_mla_host_io_layout.argtypes = [i32, i32, i32, vp, vp, vp, vp]
     lib.sparse_mla_fwd_host_packed.restype = ctypes.c_int
@@ -288,6 +293,70 @@ def sparse_mla_topk(scores: torch.Tensor, lengths: torch.Tensor, topk: int, *,
                                        out.data_ptr(), _stream_handle(stream, dev))
     _check(st)
     return out
+
+
+def sparse_mla_scatter_mask(indices: torch.Tensor, S: int, *, out: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """The lists of one request as a bit mask (include/sparse_mla.h): indices [T, topk] int32
+    positions; returns mask [T, ceil(S / 32)] int32 whose bit s % 32 of word s / 32 is set iff s
+    is listed (the words are uint32 bit patterns, held in an int32 tensor)."""
+    if indices.dim() != 2 or indices.dtype != torch.int32:
+        raise ValueError("indices must be [T, topk] int32")
+    T, topk = int(indices.shape[0]), int(indices.shape[1])
+    W = (int(S) + 31) // 32
+    dev = _device_of((("indices", indices),))
+    if not indices.is_contiguous():
+        raise ValueError("indices must be contiguous")
+    if out is None:
+        out = torch.empty((T, W), dtype=torch.int32, device=dev)
+    if out.shape != (T, W) or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [T, {W}] int32 tensor")
+    _device_of((("indices", indices), ("out", out)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_scatter_mask(indices.data_ptr(), T, topk, int(S), out.data_ptr(),
+                                               _stream_handle(stream, dev))
+    _check(st)
+    return out
+
+
+def sparse_mla_masked_mha(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor,
+                          scale: float, *, out: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Masked dense MHA (include/sparse_mla.h): q [T, h, dqk], k [S, h, dqk], v [S, h, dv] bf16,
+    mask [T, ceil(S / 32)] int32 bit words; returns out [T, h, dv] bf16 and lse [T, h] fp32."""
+    if q.dim() != 3 or q.dtype != torch.bfloat16:
+        raise ValueError("q must be [T, h, dqk] bf16")
+    T, h, dqk = (int(x) for x in q.shape)
+    if k.dim() != 3 or k.dtype != torch.bfloat16 or k.shape[1] != h or k.shape[2] != dqk:
+        raise ValueError("k must be [S, h, dqk] bf16")
+    S = int(k.shape[0])
+    if v.dim() != 3 or v.dtype != torch.bfloat16 or v.shape[0] != S or v.shape[1] != h:
+        raise ValueError("v must be [S, h, dv] bf16")
+    dv = int(v.shape[2])
+    W = (S + 31) // 32
+    if mask.shape != (T, W) or mask.dtype != torch.int32:
+        raise ValueError(f"mask must be [T, {W}] int32")
+    tensors = (("q", q), ("k", k), ("v", v), ("mask", mask))
+    dev = _device_of(tensors)
+    for name, t in tensors:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((T, h, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, h), dtype=torch.float32, device=dev)
+    if out.shape != (T, h, dv) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [T, h, {dv}] bf16 tensor")
+    if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
+    _device_of((("q", q), ("out", out), ("lse", lse)))
+    with torch.cuda.device(dev):
+        st = library().sparse_mla_masked_mha(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), T, S, h,
+                                             dqk, dv, float(scale), out.data_ptr(), lse.data_ptr(),
+                                             _stream_handle(stream, dev))
+    _check(st)
+    return out, lse
 
 
 def host_workspace_bytes(T: int, h: int, topk: int) -> int:

@@ -18,6 +18,7 @@
 #include "sparse_mla_merge.cuh"
 #include "sparse_mla_v_up.cuh"
 #include "sparse_mla_topk.cuh"
+#include "sparse_mla_masked.cuh"
 
 namespace {
 
@@ -76,6 +77,11 @@ cudaError_t set_kernel_attrs() {
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<32, 1>, smla::Layout<32>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 0>, smla::Layout<64>::kBytes);
     if (e == cudaSuccess) e = set_smem(smla::sparse_mla_fwd_tc_kernel<64, 1>, smla::Layout<64>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_masked_mha_kernel<192, 128>, smla::MmLayout<192, 128>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_masked_mha_kernel<192, 256>, smla::MmLayout<192, 256>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_masked_mha_kernel<256, 128>, smla::MmLayout<256, 128>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_masked_mha_kernel<256, 256>, smla::MmLayout<256, 256>::kBytes);
+    if (e == cudaSuccess) e = set_smem(smla::sparse_mla_scatter_mask_kernel, smla::kScatterMaxS / 32 * 4);
     return e;
 }
 
@@ -768,6 +774,120 @@ smla_status sparse_mla_topk(const float* scores, int32_t T, int64_t S, const int
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_topk_kernel, tp);
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
+    return SMLA_OK;
+}
+
+
+smla_status sparse_mla_scatter_mask(const int32_t* indices, int32_t T, int32_t topk, int64_t S, uint32_t* mask,
+                                    void* stream) {
+    if (T < 0 || topk < 1 || S < 1 || S > smla::kScatterMaxS)
+        return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d topk=%d S=%lld (S <= %d)", T, topk,
+                    static_cast<long long>(S), smla::kScatterMaxS);
+    if (T == 0) return SMLA_OK;
+    if (!indices || !mask) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(indices, 4) || !aligned(mask, 16))
+        return fail(SMLA_ERR_INVALID_ARG, "indices must be 4-byte and mask 16-byte aligned");
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    smla_status st = device_state(&dev, &ds);
+    if (st != SMLA_OK) return st;
+    smla::ScatterParams sp;
+    sp.idx = indices;
+    sp.mask = mask;
+    sp.S = S;
+    sp.T = T;
+    sp.topk = topk;
+    sp.W = static_cast<int32_t>((S + 31) / 32);
+    const int64_t cap = static_cast<int64_t>(ds->num_sms) * 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(T < cap ? T : cap), 1, 1);
+    cfg.blockDim = dim3(smla::kScatterThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(sp.W) * 4;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_scatter_mask_kernel, sp);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter kernel launch");
+    return SMLA_OK;
+}
+
+smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, const uint32_t* mask, int32_t T,
+                                  int64_t S, int32_t h, int32_t dqk, int32_t dv, float scale, void* out, float* lse,
+                                  void* stream) {
+    if (T < 0 || S < 1 || S > smla::kMmMaxS || h < 1)
+        return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d S=%lld h=%d (1 <= S <= %d)", T, static_cast<long long>(S), h,
+                    smla::kMmMaxS);
+    if (!((dqk == 192 || dqk == 256) && (dv == 128 || dv == 256)))
+        return fail(SMLA_ERR_UNSUPPORTED, "head dims (q/k %d, v %d): q/k must be 192 or 256 and v 128 or 256", dqk, dv);
+    if (!std::isfinite(scale)) return fail(SMLA_ERR_INVALID_ARG, "scale must be finite");
+    if (T == 0) return SMLA_OK;
+    if (!q || !k || !v || !mask || !out || !lse) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return fail(SMLA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (!aligned(mask, 4) || !aligned(lse, 4)) return fail(SMLA_ERR_INVALID_ARG, "mask and lse must be 4-byte aligned");
+    const int64_t nq = (static_cast<int64_t>(T) + smla::kMmBM - 1) / smla::kMmBM;
+    if (nq * h > 0x7fffffffLL || static_cast<int64_t>(T) * h > 0x7fffffffLL)
+        return fail(SMLA_ERR_INVALID_ARG, "T * h too large (%d, %d)", T, h);
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    smla_status st = device_state(&dev, &ds);
+    if (st != SMLA_OK) return st;
+    EncodeTiledFn enc = nullptr;
+    if ((st = encode_fn(&enc)) != SMLA_OK) return st;
+    alignas(64) CUtensorMap tm_q;
+    alignas(64) CUtensorMap tm_k;
+    alignas(64) CUtensorMap tm_v;
+    auto make = [&](CUtensorMap* tm, const void* base, int d, int64_t rows, uint32_t box_rows) -> CUresult {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                                    static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * h};
+        const cuuint32_t box[3] = {64, 1, box_rows};
+        const cuuint32_t es[3] = {1, 1, 1};
+        return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    CUresult r = make(&tm_q, q, dqk, T, smla::kMmBM);
+    if (r == CUDA_SUCCESS) r = make(&tm_k, k, dqk, S, smla::kMmBN);
+    if (r == CUDA_SUCCESS) r = make(&tm_v, v, dv, S, smla::kMmBN);
+    if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor maps for q/k/v failed (%d)", (int)r);
+    smla::MmParams mp;
+    mp.out = static_cast<__nv_bfloat16*>(out);
+    mp.lse = lse;
+    mp.mask = mask;
+    mp.S = S;
+    mp.T = T;
+    mp.h = h;
+    mp.W = static_cast<int32_t>((S + 31) / 32);
+    mp.nq = static_cast<int32_t>(nq);
+    mp.sm_scale_log2 = scale * 1.4426950408889634f;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nq * h), 1, 1);
+    cfg.blockDim = dim3(smla::kMmThreads, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (dqk == 192 && dv == 128) {
+        cfg.dynamicSmemBytes = smla::MmLayout<192, 128>::kBytes;
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 128>, tm_q, tm_k, tm_v, mp);
+    } else if (dqk == 192) {
+        cfg.dynamicSmemBytes = smla::MmLayout<192, 256>::kBytes;
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 256>, tm_q, tm_k, tm_v, mp);
+    } else if (dv == 128) {
+        cfg.dynamicSmemBytes = smla::MmLayout<256, 128>::kBytes;
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 128>, tm_q, tm_k, tm_v, mp);
+    } else {
+        cfg.dynamicSmemBytes = smla::MmLayout<256, 256>::kBytes;
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 256>, tm_q, tm_k, tm_v, mp);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "masked MHA kernel launch");
     return SMLA_OK;
 }
 

@@ -1,0 +1,456 @@
+// The masked dense route for short prefills (sm_103a): the per-token top-k lists scattered
+// into a bit mask, then dense multi-head attention over the request's per-head K and V in
+// which the mask alone decides which positions attend.
+//
+// PR #55738 report, 实现拆解 (implementation breakdown) items 2 and 5: prefills whose top-k
+// covers most of the history go through a scatter of the top-k lists (_scatter_topk_single_req)
+// and an FA4 attention with a mask_mod instead of the per-token top-k MQA kernel; the
+// `_is_masked_mha_available` geometry table gives (heads, qk_nope, qk_rope, v_head) =
+// (128, 128, 64, 128) for DeepSeek-V3.2, (64, 192, 64, 256) for GLM-5 and (64, 256, 0, 256) for
+// the NoPE layout.  The pages give neither the mask layout nor the arithmetic; read here as:
+//   mask row t: ceil(S / 32) uint32 words, bit s % 32 of word s / 32 set iff position s is in
+//   token t's list (entries outside [0, S) set nothing, a repeated position sets one bit);
+//   per token and head: softmax over the set positions of scale * q.k, O = P.V, natural-log
+//   LSE; a row with no bit set gives O = 0 and LSE = -inf.
+//
+// sparse_mla_scatter_mask_kernel: one CTA per row (grid-stride), the row's words built in shared
+// memory with atomic ORs and written with 16-byte stores.  HBM-bound: the lists in, the mask out.
+//
+// sparse_mla_masked_mha_kernel<DQK, DV>: one CTA per (128-query tile, head).  Unlike the gather,
+// every K/V tile is shared by the tile's 128 queries, so this is a dense contraction on the
+// tensor cores:
+//   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T                   (M=128, N=64, K-major both)
+//   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]             (M=128, N=DV, V MN-major)
+// with S (double-buffered) and O in TMEM.  Roles (192 threads):
+//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring;
+//   warp 1      MMA issuer (one thread) and TMEM owner: S(j) as soon as its tile has landed and
+//               its TMEM buffer is free, then PV(j-1) once P(j-1) is in shared memory;
+//   warps 2-5   softmax and epilogue, one thread per query row (its TMEM lane): the row's mask
+//               bits, a running max in log2 units with the O row rescaled only when it grows by
+//               more than 2^8, fp32 row sums, P as bf16 into the 128B-swizzled operand tile.
+// Before the loop the CTA marks the 64-key tiles in which any of its rows has a bit set; only
+// those tiles are loaded and multiplied (lists over causal histories never reach past the
+// tile's last query, sparse lists skip whole tiles).  Every wait is bounded; a CTA that gives
+// up drains its copies and MMAs before it frees TMEM.
+#pragma once
+
+#include "sparse_mla_common.cuh"
+
+namespace smla {
+
+constexpr int kMmBM = 128;                     // queries per tile (MMA M)
+constexpr int kMmBN = 64;                      // keys per tile
+constexpr int kMmStages = 2;
+constexpr int kMmThreads = 192;
+constexpr int kMmMaxS = 65536;                 // positions per request
+constexpr int kMmMaxTiles = kMmMaxS / kMmBN;   // 1024 key tiles
+constexpr int kScatterThreads = 256;
+constexpr int kScatterMaxS = 1 << 20;          // the row's words live in shared memory (128 KB)
+
+template <int DQK, int DV>
+struct MmLayout {
+    static_assert(DQK == 192 || DQK == 256, "q/k head dim 192 or 256");
+    static_assert(DV == 128 || DV == 256, "v head dim 128 or 256");
+    static constexpr int kQP = DQK / 64;                       // 64-wide panels of q and k
+    static constexpr int kVP = DV / 64;                        // 64-wide panels of v
+    static constexpr int kQPanel = kMmBM * 128;                // 128 rows x 128 bytes
+    static constexpr int kKPanel = kMmBN * 128;                // 64 rows x 128 bytes
+    static constexpr int kStageBytes = (kQP + kVP) * kKPanel;  // K tile then V tile
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQP * kQPanel;
+    static constexpr int kOffP = kOffKV + kMmStages * kStageBytes;
+    static constexpr int kOffTiles = kOffP + kMmBM * 128;      // active key tiles: bitmap, then list
+    static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
+    static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
+    static constexpr int kNumBars = 12;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort flag, tile count
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kTmemCols = 128 + DV <= 256 ? 256 : 512;  // S x2 [0, 128) | O [128, 128 + DV)
+    static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 alignment");
+    static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
+};
+
+enum : int {
+    kMbQ = 0,
+    kMbKvFull = 1,   // +stage
+    kMbKvEmpty = 3,  // +stage
+    kMbSFull = 5,    // +buffer
+    kMbSEmpty = 7,   // +buffer
+    kMbPFull = 9,
+    kMbPvDone = 10,
+    kMbDrain = 11
+};
+
+struct ScatterParams {
+    const int32_t* idx;   // [T, topk] positions
+    uint32_t* mask;       // [T, W]
+    int64_t S;
+    int32_t T, topk, W;
+};
+
+__global__ void __launch_bounds__(kScatterThreads)
+    sparse_mla_scatter_mask_kernel(const ScatterParams p) {
+    extern __shared__ __align__(16) uint32_t words[];
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+    const int W = p.W;
+    const bool vec = (W & 3) == 0;  // rows start on 16-byte boundaries
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+        for (int i = threadIdx.x; i < W; i += kScatterThreads) words[i] = 0u;
+        __syncthreads();
+        const int32_t* row = p.idx + t * p.topk;
+        for (int j = threadIdx.x; j < p.topk; j += kScatterThreads) {
+            const int v = __ldg(row + j);
+            if (v >= 0 && static_cast<int64_t>(v) < p.S) atomicOr(&words[v >> 5], 1u << (v & 31));
+        }
+        __syncthreads();
+        uint32_t* out = p.mask + t * W;
+        if (vec) {
+            for (int i = threadIdx.x; i < W / 4; i += kScatterThreads)
+                reinterpret_cast<uint4*>(out)[i] = reinterpret_cast<const uint4*>(words)[i];
+        } else {
+            for (int i = threadIdx.x; i < W; i += kScatterThreads) out[i] = words[i];
+        }
+        __syncthreads();
+    }
+}
+
+struct MmParams {
+    __nv_bfloat16* out;      // [T, h, DV]
+    float* lse;              // [T, h]
+    const uint32_t* mask;    // [T, W]
+    int64_t S;
+    int32_t T, h, W;
+    int32_t nq;              // ceil(T / 128)
+    float sm_scale_log2;     // scale * log2(e)
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kMmThreads, 1)
+    sparse_mla_masked_mha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                                 const __grid_constant__ CUtensorMap tm_v, const MmParams p) {
+    using L = MmLayout<DQK, DV>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = ptx::smem_u32(smem);
+    if (sbase & 1023u) {  // uniform across the grid: every CTA leaves before any barrier
+        if (threadIdx.x == 0) atomicOr(&g_smla_error, kErrLayout);
+        return;
+    }
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+    volatile int* sNact = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 8);
+    uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + L::kOffTiles);
+    uint16_t* sList = reinterpret_cast<uint16_t*>(smem + L::kOffList);
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * static_cast<uint32_t>(i); };
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        return ptx::mbar_wait(bar(i), parity, sAbort, &g_smla_error, kErrTimeout, kWaitLimitNs);
+    };
+
+    // heaviest query tiles first (later queries reach more key tiles), all heads of one tile
+    // next to each other
+    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) / p.h;
+    const int hh = static_cast<int>(blockIdx.x) % p.h;
+    const int t0 = qt * kMmBM;
+    const int n_tiles = static_cast<int>((p.S + kMmBN - 1) / kMmBN);
+
+    if (threadIdx.x == 0) {
+        *sAbort = 0;
+        ptx::mbar_init(bar(kMbQ), 1);
+        for (int s = 0; s < kMmStages; ++s) {
+            ptx::mbar_init(bar(kMbKvFull + s), 1);
+            ptx::mbar_init(bar(kMbKvEmpty + s), 1);
+            ptx::mbar_init(bar(kMbSFull + s), 1);
+            ptx::mbar_init(bar(kMbSEmpty + s), 4);
+        }
+        ptx::mbar_init(bar(kMbPFull), 4);
+        ptx::mbar_init(bar(kMbPvDone), 1);
+        ptx::mbar_init(bar(kMbDrain), 1);
+        ptx::fence_mbarrier_init();
+    }
+    for (int i = threadIdx.x; i < kMmMaxTiles / 32; i += kMmThreads) sBits[i] = 0u;
+    if (warp == 1) {
+        ptx::tmem_alloc(sbase + L::kOffMisc, L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    // launched as a programmatic dependent: the mask may be the previous launch's output
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+    __syncthreads();
+
+    // ---- the key tiles any row of this query tile attends to: each warp takes rows, its lanes
+    // the row's words (coalesced); tile k covers words 2k and 2k + 1
+    for (int r = warp; r < kMmBM; r += kMmThreads / 32) {
+        const int64_t t = t0 + r;
+        if (t >= p.T) break;
+        const uint32_t* mrow = p.mask + t * p.W;
+        for (int w = lane; w < p.W; w += 32) {
+            if (__ldg(mrow + w) != 0u) {
+                const int k = w >> 1;
+                atomicOr(&sBits[k >> 5], 1u << (k & 31));
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // compact list of the active tiles in ascending order (32 bitmap words, one per lane)
+        const uint32_t bits = lane < (n_tiles + 31) / 32 ? sBits[lane] : 0u;
+        const int cnt = __popc(bits);
+        int pre = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, pre, o);
+            if (lane >= o) pre += v;
+        }
+        int pos = pre - cnt;
+        uint32_t b = bits;
+        while (b) {
+            const int i = __ffs(b) - 1;
+            b &= b - 1;
+            sList[pos++] = static_cast<uint16_t>(lane * 32 + i);
+        }
+        if (lane == 31) *sNact = pre;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffMisc);
+    const int nact = *sNact;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0 && nact > 0) {
+            ptx::prefetch_tmap(&tm_q);
+            ptx::prefetch_tmap(&tm_k);
+            ptx::prefetch_tmap(&tm_v);
+            ptx::mbar_arrive_expect_tx(bar(kMbQ), static_cast<uint32_t>(L::kQP * L::kQPanel));
+            for (int pn = 0; pn < L::kQP; ++pn)
+                ptx::tma_load_3d(sbase + L::kOffQ + pn * L::kQPanel, &tm_q, 64 * pn, hh, t0, bar(kMbQ));
+            int j = 0;
+            for (; j < nact; ++j) {
+                const int s = j % kMmStages;
+                if (j >= kMmStages && !wait(kMbKvEmpty + s, ((j / kMmStages) - 1) & 1)) break;
+                const int key0 = static_cast<int>(sList[j]) * kMmBN;
+                const uint32_t st = sbase + L::kOffKV + s * L::kStageBytes;
+                ptx::mbar_arrive_expect_tx(bar(kMbKvFull + s), static_cast<uint32_t>(L::kStageBytes));
+                for (int pn = 0; pn < L::kQP; ++pn)
+                    ptx::tma_load_3d(st + pn * L::kKPanel, &tm_k, 64 * pn, hh, key0, bar(kMbKvFull + s));
+                for (int pn = 0; pn < L::kVP; ++pn)
+                    ptx::tma_load_3d(st + (L::kQP + pn) * L::kKPanel, &tm_v, 64 * pn, hh, key0, bar(kMbKvFull + s));
+            }
+            // no copy may still be landing when the CTA leaves
+            ptx::mbar_wait(bar(kMbQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+            for (int i = j - (j < kMmStages ? j : kMmStages); i < j; ++i)
+                ptx::mbar_wait(bar(kMbKvFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
+                               kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0 && nact > 0) {
+            constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kMmBM, kMmBN, 0, 0);
+            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kMmBM, DV, 0, 1);
+            const uint64_t dq = ptx::smem_desc_sw128(sbase + L::kOffQ, 16, 1024);
+            const uint64_t dk = ptx::smem_desc_sw128(sbase + L::kOffKV, 16, 1024);
+            const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
+            const uint64_t dp = ptx::smem_desc_sw128(sbase + L::kOffP, 16, 1024);
+            auto issue_pv = [&](int jj) {
+                const int s = jj % kMmStages;
+                const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
+#pragma unroll
+                for (int k = 0; k < kMmBN / 16; ++k)
+                    ptx::mma_bf16_ss(tmem + 128, dp + ((k * 32) >> 4), v0 + ((k * 2048) >> 4), kIdescPV,
+                                     (jj > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(kMbKvEmpty + s));
+                ptx::mma_commit(bar(kMbPvDone));
+            };
+            bool ok = wait(kMbQ, 0);
+            for (int j = 0; ok && j < nact; ++j) {
+                const int s = j % kMmStages;
+                if (!(ok = wait(kMbKvFull + s, (j / kMmStages) & 1))) break;
+                if (j >= kMmStages && !(ok = wait(kMbSEmpty + s, ((j / kMmStages) - 1) & 1))) break;
+                ptx::tc_fence_after();
+                const uint64_t k0 = dk + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
+                const uint32_t d = tmem + static_cast<uint32_t>(s * kMmBN);
+#pragma unroll
+                for (int pn = 0; pn < L::kQP; ++pn)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_bf16_ss(d, dq + ((pn * L::kQPanel + k * 32) >> 4), k0 + ((pn * L::kKPanel + k * 32) >> 4),
+                                         kIdescS, (pn | k) != 0 ? 1u : 0u);
+                ptx::mma_commit(bar(kMbSFull + s));
+                if (j > 0) {
+                    if (!(ok = wait(kMbPFull, (j - 1) & 1))) break;
+                    ptx::tc_fence_after();
+                    issue_pv(j - 1);
+                }
+            }
+            if (ok && wait(kMbPFull, (nact - 1) & 1)) {
+                ptx::tc_fence_after();
+                issue_pv(nact - 1);
+            }
+            ptx::mma_commit(bar(kMbDrain));
+            ptx::mbar_wait(bar(kMbDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax / epilogue
+        const int quad = warp & 3;  // the TMEM lane quadrant this warp may access
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const int r = quad * 32 + lane;          // query row of this thread (its TMEM lane)
+        const int64_t t = t0 + r;
+        const bool live = t < p.T;
+        const uint32_t* mrow = p.mask + (live ? t : 0) * p.W;
+        const float c = p.sm_scale_log2;
+        float m = -CUDART_INF_F, l = 0.f;
+        bool failed = false;
+        auto warp_wait = [&](int i, uint32_t parity) -> bool {
+            bool okw = true;
+            if (lane == 0) okw = wait(i, parity);
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            __syncwarp();
+            return okw;
+        };
+        auto mask_words = [&](int j) -> uint2 {
+            uint2 w = make_uint2(0u, 0u);
+            if (live && j < nact) {
+                const int w0 = 2 * static_cast<int>(sList[j]);
+                w.x = __ldg(mrow + w0);
+                if (w0 + 1 < p.W) w.y = __ldg(mrow + w0 + 1);
+            }
+            return w;
+        };
+        uint2 mw = mask_words(0);
+        const uint32_t prow = sbase + L::kOffP + static_cast<uint32_t>(r) * 128u;
+        for (int j = 0; j < nact; ++j) {
+            const int s = j % kMmStages;
+            const uint2 cur = mw;
+            mw = mask_words(j + 1);
+            if (!warp_wait(kMbSFull + s, (j / kMmStages) & 1)) {
+                failed = true;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t sv[64];
+            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 0, sv);
+            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 16, sv + 16);
+            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32, sv + 32);
+            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 48, sv + 48);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty + s));
+            // scaled logits of the set positions (log2 units), the tile's row max
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const uint32_t bit = (i < 32 ? (cur.x >> i) : (cur.y >> (i - 32))) & 1u;
+                const float x = bit ? __uint_as_float(sv[i]) * c : -CUDART_INF_F;
+                sv[i] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const bool grow = mx > m + kRescaleLog2;
+            bool pv_waited = false;
+            if (__any_sync(0xffffffffu, grow)) {
+                // the running max of some row grew by more than 2^8: that row's O and sum are
+                // rescaled (the other rows of the warp multiply by 1); O must be complete
+                float alpha = 1.f;
+                if (grow) {
+                    const float mn = fmaxf(m, mx);
+                    alpha = (m == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(m - mn);
+                    m = mn;
+                    l *= alpha;
+                }
+                if (j > 0) {
+                    if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
+                        failed = true;
+                        break;
+                    }
+                    pv_waited = true;
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < DV / 16; ++cc) {
+                        uint32_t o[16];
+                        SMLA_TMEM_LD16(tmem + lane_base + 128 + cc * 16, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        SMLA_TMEM_ST16(tmem + lane_base + 128 + cc * 16, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+            }
+            // P = 2^(x - m) as bf16, row sums in fp32; the single P tile is rewritten only after
+            // the previous PV has read it
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
+                const float p0 = x0 == -CUDART_INF_F ? 0.f : ptx::ex2_approx(x0 - m);
+                const float p1 = x1 == -CUDART_INF_F ? 0.f : ptx::ex2_approx(x1 - m);
+                l += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            if (j > 0 && !pv_waited) {
+                if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
+                    failed = true;
+                    break;
+                }
+            }
+            // row r of the K-major SW128 P tile: 16-byte chunk q at ((q ^ (r & 7)) << 4)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                ptx::st_shared_v4(prow + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4),
+                                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kMbPFull));
+        }
+        // ---- epilogue: O / l as bf16 and the natural-log LSE
+        bool have_o = nact > 0 && !failed;
+        if (have_o) {
+            have_o = warp_wait(kMbPvDone, (nact - 1) & 1);
+            if (have_o) ptx::tc_fence_after();
+        }
+        if (!failed) {
+            const float inv = (have_o && l > 0.f) ? 1.0f / l : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(p.out + ((live ? t : 0) * p.h + hh) * DV);
+#pragma unroll 1
+            for (int cc = 0; cc < DV / 16; ++cc) {
+                uint32_t o[16];
+                if (have_o) {
+                    SMLA_TMEM_LD16(tmem + lane_base + 128 + cc * 16, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = 0u;
+                }
+                if (live) {
+                    uint4 v0, v1;
+                    v0.x = pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv);
+                    v0.y = pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv);
+                    v0.z = pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv);
+                    v0.w = pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv);
+                    v1.x = pack_bf16x2(__uint_as_float(o[8]) * inv, __uint_as_float(o[9]) * inv);
+                    v1.y = pack_bf16x2(__uint_as_float(o[10]) * inv, __uint_as_float(o[11]) * inv);
+                    v1.z = pack_bf16x2(__uint_as_float(o[12]) * inv, __uint_as_float(o[13]) * inv);
+                    v1.w = pack_bf16x2(__uint_as_float(o[14]) * inv, __uint_as_float(o[15]) * inv);
+                    orow[2 * cc] = v0;
+                    orow[2 * cc + 1] = v1;
+                }
+            }
+            if (live)
+                p.lse[t * p.h + hh] = (have_o && l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        }
+        if (failed) *sAbort = 1;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace smla
