@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the sm_100-family features the kernel uses:
-// mbarriers (with bounded waits), TMA tensor loads (tiled and tile::gather4),
+// mbarriers (with bounded waits), TMA tensor and bulk loads,
 // tcgen05 MMA / TMEM, named barriers and cluster shared memory.
 #pragma once
 
@@ -111,17 +111,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// Four rows (given by their row coordinates) of one box-wide column window,
-// written as four consecutive box rows at dst.  Out-of-range rows read zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
 // 1-D bulk copy global -> shared, completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -197,29 +186,9 @@ __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t n, bool p
     return r != 0;
 }
 
-// ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
-}
-
-// Split form of cluster_sync: arrive early (no ordering), wait later.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
@@ -281,16 +250,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A read from tensor memory (lanes = M rows).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -363,12 +322,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-__device__ __forceinline__ float warp_max_f32(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
-
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
@@ -429,12 +382,6 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_bytes, flo
     uint32_t out;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi * scale), "f"(lo * scale));
     return out;
-}
-
-__device__ __forceinline__ int ld_nc_s32(const int32_t* p) {
-    int v;
-    asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
 }
 
 }  // namespace ptx
