@@ -27,7 +27,9 @@
 //               its TMEM buffer is free, then PV(j-1) once P(j-1) is in shared memory;
 //   warps 2-5   softmax and epilogue, one thread per query row (its TMEM lane): the row's mask
 //               bits, a running max in log2 units with the O row rescaled only when it grows by
-//               more than 2^8, fp32 row sums, P as bf16 into the 128B-swizzled operand tile.
+//               more than 2^8, fp32 row sums, P as bf16 into one of two 128B-swizzled operand
+//               tiles (tile j into buffer j % 2, so the softmax of tile j runs while PV(j-1) reads
+//               the other buffer).
 // Before the loop the CTA marks the 64-key tiles in which any of its rows has a bit set; only
 // those tiles are loaded and multiplied (lists over causal histories never reach past the
 // tile's last query, sparse lists skip whole tiles).  Every wait is bounded; a CTA that gives
@@ -59,10 +61,11 @@ struct MmLayout {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQP * kQPanel;
     static constexpr int kOffP = kOffKV + kMmStages * kStageBytes;
-    static constexpr int kOffTiles = kOffP + kMmBM * 128;      // active key tiles: bitmap, then list
+    static constexpr int kPBytes = kMmBM * 128;                // one P tile: 128 rows x 64 bf16
+    static constexpr int kOffTiles = kOffP + 2 * kPBytes;      // active key tiles: bitmap, then list
     static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
     static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
-    static constexpr int kNumBars = 12;
+    static constexpr int kNumBars = 15;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort flag, tile count
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kTmemCols = 128 + DV <= 256 ? 256 : 512;  // S x2 [0, 128) | O [128, 128 + DV)
@@ -76,9 +79,10 @@ enum : int {
     kMbKvEmpty = 3,  // +stage
     kMbSFull = 5,    // +buffer
     kMbSEmpty = 7,   // +buffer
-    kMbPFull = 9,
-    kMbPvDone = 10,
-    kMbDrain = 11
+    kMbPFull = 9,    // +buffer
+    kMbPEmpty = 11,  // +buffer
+    kMbPvDone = 13,
+    kMbDrain = 14
 };
 
 struct ScatterParams {
@@ -147,10 +151,11 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         return ptx::mbar_wait(bar(i), parity, sAbort, &g_smla_error, kErrTimeout, kWaitLimitNs);
     };
 
-    // heaviest query tiles first (later queries reach more key tiles), all heads of one tile
-    // next to each other
-    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) / p.h;
-    const int hh = static_cast<int>(blockIdx.x) % p.h;
+    // the query tiles of one head next to each other, so the CTAs in flight share a few heads'
+    // K and V in L2 (all heads' K/V of a long request exceed it); heaviest tiles first within a
+    // head (later queries reach more key tiles)
+    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) % p.nq;
+    const int hh = static_cast<int>(blockIdx.x) / p.nq;
     const int t0 = qt * kMmBM;
     const int n_tiles = static_cast<int>((p.S + kMmBN - 1) / kMmBN);
 
@@ -163,7 +168,10 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::mbar_init(bar(kMbSFull + s), 1);
             ptx::mbar_init(bar(kMbSEmpty + s), 4);
         }
-        ptx::mbar_init(bar(kMbPFull), 4);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(kMbPFull + b), 4);
+            ptx::mbar_init(bar(kMbPEmpty + b), 1);
+        }
         ptx::mbar_init(bar(kMbPvDone), 1);
         ptx::mbar_init(bar(kMbDrain), 1);
         ptx::fence_mbarrier_init();
@@ -257,11 +265,13 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             auto issue_pv = [&](int jj) {
                 const int s = jj % kMmStages;
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
+                const uint64_t p0 = dp + static_cast<uint64_t>(((jj & 1) * L::kPBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < kMmBN / 16; ++k)
-                    ptx::mma_bf16_ss(tmem + 128, dp + ((k * 32) >> 4), v0 + ((k * 2048) >> 4), kIdescPV,
+                    ptx::mma_bf16_ss(tmem + 128, p0 + ((k * 32) >> 4), v0 + ((k * 2048) >> 4), kIdescPV,
                                      (jj > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(kMbKvEmpty + s));
+                ptx::mma_commit(bar(kMbPEmpty + (jj & 1)));
                 ptx::mma_commit(bar(kMbPvDone));
             };
             bool ok = wait(kMbQ, 0);
@@ -280,12 +290,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                                          kIdescS, (pn | k) != 0 ? 1u : 0u);
                 ptx::mma_commit(bar(kMbSFull + s));
                 if (j > 0) {
-                    if (!(ok = wait(kMbPFull, (j - 1) & 1))) break;
+                    if (!(ok = wait(kMbPFull + ((j - 1) & 1), ((j - 1) >> 1) & 1))) break;
                     ptx::tc_fence_after();
                     issue_pv(j - 1);
                 }
             }
-            if (ok && wait(kMbPFull, (nact - 1) & 1)) {
+            if (ok && wait(kMbPFull + ((nact - 1) & 1), ((nact - 1) >> 1) & 1)) {
                 ptx::tc_fence_after();
                 issue_pv(nact - 1);
             }
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             return w;
         };
         uint2 mw = mask_words(0);
-        const uint32_t prow = sbase + L::kOffP + static_cast<uint32_t>(r) * 128u;
+        const uint32_t prow0 = sbase + L::kOffP + static_cast<uint32_t>(r) * 128u;
         for (int j = 0; j < nact; ++j) {
             const int s = j % kMmStages;
             const uint2 cur = mw;
@@ -380,8 +390,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     ptx::tmem_wait_st();
                 }
             }
-            // P = 2^(x - m) as bf16, row sums in fp32; the single P tile is rewritten only after
-            // the previous PV has read it
+            // P = 2^(x - m) as bf16, row sums in fp32; P buffer j % 2 is rewritten only after
+            // PV(j - 2) has read it
             uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -391,12 +401,13 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 l += p0 + p1;
                 pk[i] = pack_bf16x2(p0, p1);
             }
-            if (j > 0 && !pv_waited) {
-                if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
+            if (j >= 2 && !pv_waited) {
+                if (!warp_wait(kMbPEmpty + (j & 1), ((j >> 1) - 1) & 1)) {
                     failed = true;
                     break;
                 }
             }
+            const uint32_t prow = prow0 + static_cast<uint32_t>((j & 1) * L::kPBytes);
             // row r of the K-major SW128 P tile: 16-byte chunk q at ((q ^ (r & 7)) << 4)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -405,7 +416,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(kMbPFull));
+            if (lane == 0) ptx::mbar_arrive(bar(kMbPFull + (j & 1)));
         }
         // ---- epilogue: O / l as bf16 and the natural-log LSE
         bool have_o = nact > 0 && !failed;
