@@ -140,7 +140,11 @@ DEV = "cuda:0"
 @pytest.mark.gpu
 @pytest.mark.parametrize("T,S,k,mode", [(4, 300, 16, "rand"), (3, 5000, 2048, "rand"), (6, 2047, 2048, "rand"),
                                         (5, 4096, 2048, "ties"), (2, 70000, 2048, "rand"), (8, 1000, 1, "rand"),
-                                        (3, 3000, 777, "quant"), (16, 33000, 2048, "rand")])
+                                        (3, 3000, 777, "quant"), (16, 33000, 2048, "rand"),
+                                        # more equal keys in the threshold's top-11-bit bin than the
+                                        # shared-memory candidate buffer holds (the row-scan path)
+                                        (3, 20000, 2048, "ties"), (2, 70000, 3000, "quant"),
+                                        (4, 9000, 1000, "neg")])
 def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
     import token_sparse_mla_gb300 as smla
     s = _scores(T, S, seed=S + k)
@@ -149,6 +153,8 @@ def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
         s[:, ::3] = 1.0  # many equal scores at the threshold
     elif mode == "quant":
         s = torch.round(s * 4) / 4  # few distinct values: ties everywhere
+    elif mode == "neg":
+        s = -s.abs() - 1.0  # every score negative: the low bins of the key
     g = torch.Generator().manual_seed(T + k)
     lens = torch.randint(0, S + 1, (T,), generator=g).to(torch.int32)
     lens[0] = S
