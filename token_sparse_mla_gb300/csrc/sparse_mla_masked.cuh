@@ -186,18 +186,27 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     ptx::grid_launch_dependents();
     __syncthreads();
 
-    // ---- the key tiles any row of this query tile attends to: each warp takes rows, its lanes
-    // the row's words (coalesced); tile k covers words 2k and 2k + 1
+    // ---- the key tiles any row of this query tile attends to (tile k covers words 2k and 2k + 1).
+    // Each warp takes rows, its lanes the row's words (coalesced, independent loads); a nonzero
+    // word raises its flag in the P tiles' memory (free until the loop) with a plain store, since
+    // every writer stores the same value; then each tile ORs its two flags into the bitmap.  (An
+    // atomic on the bitmap per nonzero word put every row of the query tile on the same one or
+    // two words: 18.7 M shared-memory bank conflicts per launch on the 4096-token chunk.)
+    volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffP);
+    static_assert(2 * L::kPBytes >= kMmMaxS / 32 * 4, "word flags fit the P tiles");
+    for (int w = threadIdx.x; w < p.W; w += kMmThreads) sFlag[w] = 0u;
+    __syncthreads();
     for (int r = warp; r < kMmBM; r += kMmThreads / 32) {
         const int64_t t = t0 + r;
         if (t >= p.T) break;
         const uint32_t* mrow = p.mask + t * p.W;
-        for (int w = lane; w < p.W; w += 32) {
-            if (__ldg(mrow + w) != 0u) {
-                const int k = w >> 1;
-                atomicOr(&sBits[k >> 5], 1u << (k & 31));
-            }
-        }
+        for (int w = lane; w < p.W; w += 32)
+            if (__ldg(mrow + w) != 0u) sFlag[w] = 1u;
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < n_tiles; k += kMmThreads) {
+        const bool any = sFlag[2 * k] != 0u || (2 * k + 1 < p.W && sFlag[2 * k + 1] != 0u);
+        if (any) atomicOr(&sBits[k >> 5], 1u << (k & 31));
     }
     __syncthreads();
     if (warp == 0) {
