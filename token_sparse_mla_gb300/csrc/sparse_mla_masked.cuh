@@ -22,7 +22,9 @@
 //   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T                   (M=128, N=64, K-major both)
 //   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]             (M=128, N=DV, V MN-major)
 // with S (double-buffered) and O in TMEM.  Roles (192 threads):
-//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring;
+//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring, K
+//               and V refilled separately (K once S of its slot's previous tile is done, V once
+//               its PV is done);
 //   warp 1      MMA issuer (one thread) and TMEM owner: S(j) as soon as its tile has landed and
 //               its TMEM buffer is free, then PV(j-1) once P(j-1) is in shared memory;
 //   warps 2-5   softmax and epilogue, one thread per query row (its TMEM lane): the row's mask
@@ -65,7 +67,7 @@ struct MmLayout {
     static constexpr int kOffTiles = kOffP + 2 * kPBytes;      // active key tiles: bitmap, then list
     static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
     static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
-    static constexpr int kNumBars = 15;
+    static constexpr int kNumBars = 19;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort flag, tile count
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kTmemCols = 128 + DV <= 256 ? 256 : 512;  // S x2 [0, 128) | O [128, 128 + DV)
@@ -75,14 +77,16 @@ struct MmLayout {
 
 enum : int {
     kMbQ = 0,
-    kMbKvFull = 1,   // +stage
-    kMbKvEmpty = 3,  // +stage
+    kMbKFull = 1,    // +stage: the K tile landed
+    kMbKEmpty = 3,   // +stage: S of the tile is done, its K panels may be refilled
     kMbSFull = 5,    // +buffer
     kMbSEmpty = 7,   // +buffer
     kMbPFull = 9,    // +buffer
     kMbPEmpty = 11,  // +buffer
     kMbPvDone = 13,
-    kMbDrain = 14
+    kMbDrain = 14,
+    kMbVFull = 15,   // +stage: the V tile landed
+    kMbVEmpty = 17   // +stage: PV of the tile is done, its V panels may be refilled
 };
 
 struct ScatterParams {
@@ -163,8 +167,10 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         *sAbort = 0;
         ptx::mbar_init(bar(kMbQ), 1);
         for (int s = 0; s < kMmStages; ++s) {
-            ptx::mbar_init(bar(kMbKvFull + s), 1);
-            ptx::mbar_init(bar(kMbKvEmpty + s), 1);
+            ptx::mbar_init(bar(kMbKFull + s), 1);
+            ptx::mbar_init(bar(kMbKEmpty + s), 1);
+            ptx::mbar_init(bar(kMbVFull + s), 1);
+            ptx::mbar_init(bar(kMbVEmpty + s), 1);
             ptx::mbar_init(bar(kMbSFull + s), 1);
             ptx::mbar_init(bar(kMbSEmpty + s), 4);
         }
@@ -243,22 +249,31 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::mbar_arrive_expect_tx(bar(kMbQ), static_cast<uint32_t>(L::kQP * L::kQPanel));
             for (int pn = 0; pn < L::kQP; ++pn)
                 ptx::tma_load_3d(sbase + L::kOffQ + pn * L::kQPanel, &tm_q, 64 * pn, hh, t0, bar(kMbQ));
-            int j = 0;
-            for (; j < nact; ++j) {
+            // K and V of a tile refill separately: K as soon as S of the tile two back is done,
+            // V once its PV is done, so the K loads run a softmax ahead of the V loads
+            int jk = 0, jv = 0;  // K and V tiles issued
+            for (int j = 0; j < nact; ++j) {
                 const int s = j % kMmStages;
-                if (j >= kMmStages && !wait(kMbKvEmpty + s, ((j / kMmStages) - 1) & 1)) break;
                 const int key0 = static_cast<int>(sList[j]) * kMmBN;
                 const uint32_t st = sbase + L::kOffKV + s * L::kStageBytes;
-                ptx::mbar_arrive_expect_tx(bar(kMbKvFull + s), static_cast<uint32_t>(L::kStageBytes));
+                if (j >= kMmStages && !wait(kMbKEmpty + s, ((j / kMmStages) - 1) & 1)) break;
+                ptx::mbar_arrive_expect_tx(bar(kMbKFull + s), static_cast<uint32_t>(L::kQP * L::kKPanel));
                 for (int pn = 0; pn < L::kQP; ++pn)
-                    ptx::tma_load_3d(st + pn * L::kKPanel, &tm_k, 64 * pn, hh, key0, bar(kMbKvFull + s));
+                    ptx::tma_load_3d(st + pn * L::kKPanel, &tm_k, 64 * pn, hh, key0, bar(kMbKFull + s));
+                ++jk;
+                if (j >= kMmStages && !wait(kMbVEmpty + s, ((j / kMmStages) - 1) & 1)) break;
+                ptx::mbar_arrive_expect_tx(bar(kMbVFull + s), static_cast<uint32_t>(L::kVP * L::kKPanel));
                 for (int pn = 0; pn < L::kVP; ++pn)
-                    ptx::tma_load_3d(st + (L::kQP + pn) * L::kKPanel, &tm_v, 64 * pn, hh, key0, bar(kMbKvFull + s));
+                    ptx::tma_load_3d(st + (L::kQP + pn) * L::kKPanel, &tm_v, 64 * pn, hh, key0, bar(kMbVFull + s));
+                ++jv;
             }
             // no copy may still be landing when the CTA leaves
             ptx::mbar_wait(bar(kMbQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
-            for (int i = j - (j < kMmStages ? j : kMmStages); i < j; ++i)
-                ptx::mbar_wait(bar(kMbKvFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
+            for (int i = jk - (jk < kMmStages ? jk : kMmStages); i < jk; ++i)
+                ptx::mbar_wait(bar(kMbKFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
+                               kDrainLimitNs);
+            for (int i = jv - (jv < kMmStages ? jv : kMmStages); i < jv; ++i)
+                ptx::mbar_wait(bar(kMbVFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
                                kDrainLimitNs);
         }
         __syncwarp();
@@ -271,22 +286,25 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             const uint64_t dk = ptx::smem_desc_sw128(sbase + L::kOffKV, 16, 1024);
             const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
             const uint64_t dp = ptx::smem_desc_sw128(sbase + L::kOffP, 16, 1024);
-            auto issue_pv = [&](int jj) {
+            auto issue_pv = [&](int jj) -> bool {
                 const int s = jj % kMmStages;
+                if (!wait(kMbVFull + s, (jj / kMmStages) & 1)) return false;
+                ptx::tc_fence_after();
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
                 const uint64_t p0 = dp + static_cast<uint64_t>(((jj & 1) * L::kPBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < kMmBN / 16; ++k)
                     ptx::mma_bf16_ss(tmem + 128, p0 + ((k * 32) >> 4), v0 + ((k * 2048) >> 4), kIdescPV,
                                      (jj > 0 || k > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(kMbKvEmpty + s));
+                ptx::mma_commit(bar(kMbVEmpty + s));
                 ptx::mma_commit(bar(kMbPEmpty + (jj & 1)));
                 ptx::mma_commit(bar(kMbPvDone));
+                return true;
             };
             bool ok = wait(kMbQ, 0);
             for (int j = 0; ok && j < nact; ++j) {
                 const int s = j % kMmStages;
-                if (!(ok = wait(kMbKvFull + s, (j / kMmStages) & 1))) break;
+                if (!(ok = wait(kMbKFull + s, (j / kMmStages) & 1))) break;
                 if (j >= kMmStages && !(ok = wait(kMbSEmpty + s, ((j / kMmStages) - 1) & 1))) break;
                 ptx::tc_fence_after();
                 const uint64_t k0 = dk + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
@@ -298,15 +316,16 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                         ptx::mma_bf16_ss(d, dq + ((pn * L::kQPanel + k * 32) >> 4), k0 + ((pn * L::kKPanel + k * 32) >> 4),
                                          kIdescS, (pn | k) != 0 ? 1u : 0u);
                 ptx::mma_commit(bar(kMbSFull + s));
+                ptx::mma_commit(bar(kMbKEmpty + s));
                 if (j > 0) {
                     if (!(ok = wait(kMbPFull + ((j - 1) & 1), ((j - 1) >> 1) & 1))) break;
                     ptx::tc_fence_after();
-                    issue_pv(j - 1);
+                    if (!(ok = issue_pv(j - 1))) break;
                 }
             }
             if (ok && wait(kMbPFull + ((nact - 1) & 1), ((nact - 1) >> 1) & 1)) {
                 ptx::tc_fence_after();
-                issue_pv(nact - 1);
+                issue_pv(nact - 1);  // a failed wait inside has flagged the abort
             }
             ptx::mma_commit(bar(kMbDrain));
             ptx::mbar_wait(bar(kMbDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
