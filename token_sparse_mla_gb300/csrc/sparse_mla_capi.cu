@@ -840,13 +840,15 @@ smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, c
     alignas(64) CUtensorMap tm_q;
     alignas(64) CUtensorMap tm_k;
     alignas(64) CUtensorMap tm_v;
+    // [rows, h, d] viewed as (64 elements, rows, h, d / 64 panels): one box of (64, box_rows, 1,
+    // d / 64) lands as d / 64 SW128 panels of box_rows x 128 bytes, one after another
     auto make = [&](CUtensorMap* tm, const void* base, int d, int64_t rows, uint32_t box_rows) -> CUresult {
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
-                                    static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * h};
-        const cuuint32_t box[3] = {64, 1, box_rows};
-        const cuuint32_t es[3] = {1, 1, 1};
-        return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+        const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(h),
+                                    static_cast<cuuint64_t>(d / 64)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2 * h, static_cast<cuuint64_t>(d) * 2, 128};
+        const cuuint32_t box[4] = {64, box_rows, 1, static_cast<cuuint32_t>(d / 64)};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     };

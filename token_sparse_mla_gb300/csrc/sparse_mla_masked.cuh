@@ -21,17 +21,20 @@
 // tensor cores:
 //   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T                   (M=128, N=64, K-major both)
 //   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]             (M=128, N=DV, V MN-major)
-// with S (double-buffered) and O in TMEM.  Roles (192 threads):
-//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring, K
-//               and V refilled separately (K once S of its slot's previous tile is done, V once
-//               its PV is done);
+// with S (double-buffered), P (double-buffered, bf16, the A operand of PV read from TMEM) and
+// O in TMEM.  Roles (320 threads):
+//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring,
+//               one copy per tile (a 4-D map whose outer dimension is the 64-wide panel); V runs
+//               one tile behind K (K(j) waits for S(j-2), V(j-1) for PV(j-3), the order in which
+//               the tensor cores finish them);
 //   warp 1      MMA issuer (one thread) and TMEM owner: S(j) as soon as its tile has landed and
-//               its TMEM buffer is free, then PV(j-1) once P(j-1) is in shared memory;
-//   warps 2-5   softmax and epilogue, one thread per query row (its TMEM lane): the row's mask
-//               bits, a running max in log2 units with the O row rescaled only when it grows by
-//               more than 2^8, fp32 row sums, P as bf16 into one of two 128B-swizzled operand
-//               tiles (tile j into buffer j % 2, so the softmax of tile j runs while PV(j-1) reads
-//               the other buffer).
+//               its TMEM buffer is free, then PV(j-1) once P(j-1) is in TMEM;
+//   warps 2-9   softmax and epilogue, two warps per TMEM lane quadrant, one query row per
+//               thread: half 0 takes keys [0, 32) of a tile and O columns [0, DV/2), half 1 the
+//               rest.  The row's mask bits, a running max in log2 units with O rescaled only
+//               when the max grows by more than 2^8 (a pair-wide barrier reduction per tile says
+//               whether any row grew; only then do the halves swap maxima through shared
+//               memory), fp32 row sums per half, P as bf16 pairs into TMEM buffer j % 2.
 // Before the loop the CTA marks the 64-key tiles in which any of its rows has a bit set; only
 // those tiles are loaded and multiplied (lists over causal histories never reach past the
 // tile's last query, sparse lists skip whole tiles).  Every wait is bounded; a CTA that gives
@@ -45,7 +48,8 @@ namespace smla {
 constexpr int kMmBM = 128;                     // queries per tile (MMA M)
 constexpr int kMmBN = 64;                      // keys per tile
 constexpr int kMmStages = 2;
-constexpr int kMmThreads = 192;
+constexpr int kMmSoftmaxWarps = 8;             // two per TMEM lane quadrant
+constexpr int kMmThreads = 64 + 32 * kMmSoftmaxWarps;
 constexpr int kMmMaxS = 65536;                 // positions per request
 constexpr int kMmMaxTiles = kMmMaxS / kMmBN;   // 1024 key tiles
 constexpr int kScatterThreads = 256;
@@ -62,16 +66,19 @@ struct MmLayout {
     static constexpr int kStageBytes = (kQP + kVP) * kKPanel;  // K tile then V tile
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQP * kQPanel;
-    static constexpr int kOffP = kOffKV + kMmStages * kStageBytes;
-    static constexpr int kPBytes = kMmBM * 128;                // one P tile: 128 rows x 64 bf16
-    static constexpr int kOffTiles = kOffP + 2 * kPBytes;      // active key tiles: bitmap, then list
+    static constexpr int kOffTiles = kOffKV + kMmStages * kStageBytes;  // active key tiles: bitmap, then list
     static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
     static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
     static constexpr int kNumBars = 19;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort flag, tile count
-    static constexpr int kBytes = kOffMisc + 16;
-    static constexpr int kTmemCols = 128 + DV <= 256 ? 256 : 512;  // S x2 [0, 128) | O [128, 128 + DV)
-    static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 alignment");
+    static constexpr int kOffX = kOffMisc + 16;                // row maxima / sums swapped by a warp pair
+    static constexpr int kBytes = kOffX + kMmBM * 4;
+    // TMEM columns: S x2 [0, 128) | O [128, 128 + DV) | P x2 (bf16 pairs) [128 + DV, 192 + DV)
+    static constexpr int kColO = 128;
+    static constexpr int kColP = 128 + DV;
+    static constexpr int kTmemCols = 512;
+    static_assert(kColP + 2 * (kMmBN / 2) <= kTmemCols, "TMEM columns");
+    static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
 };
 
@@ -172,10 +179,10 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::mbar_init(bar(kMbVFull + s), 1);
             ptx::mbar_init(bar(kMbVEmpty + s), 1);
             ptx::mbar_init(bar(kMbSFull + s), 1);
-            ptx::mbar_init(bar(kMbSEmpty + s), 4);
+            ptx::mbar_init(bar(kMbSEmpty + s), kMmSoftmaxWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar(kMbPFull + b), 4);
+            ptx::mbar_init(bar(kMbPFull + b), kMmSoftmaxWarps);
             ptx::mbar_init(bar(kMbPEmpty + b), 1);
         }
         ptx::mbar_init(bar(kMbPvDone), 1);
@@ -194,12 +201,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
 
     // ---- the key tiles any row of this query tile attends to (tile k covers words 2k and 2k + 1).
     // Each warp takes rows, its lanes the row's words (coalesced, independent loads); a nonzero
-    // word raises its flag in the P tiles' memory (free until the loop) with a plain store, since
-    // every writer stores the same value; then each tile ORs its two flags into the bitmap.  (An
+    // word raises its flag in the first K/V stage (free until the first load) with a plain store,
+    // since every writer stores the same value; then each tile ORs its two flags into the bitmap.  (An
     // atomic on the bitmap per nonzero word put every row of the query tile on the same one or
     // two words: 18.7 M shared-memory bank conflicts per launch on the 4096-token chunk.)
-    volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffP);
-    static_assert(2 * L::kPBytes >= kMmMaxS / 32 * 4, "word flags fit the P tiles");
+    volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffKV);
+    static_assert(L::kStageBytes >= kMmMaxS / 32 * 4, "word flags fit a K/V stage");
     for (int w = threadIdx.x; w < p.W; w += kMmThreads) sFlag[w] = 0u;
     __syncthreads();
     for (int r = warp; r < kMmBM; r += kMmThreads / 32) {
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         const bool any = sFlag[2 * k] != 0u || (2 * k + 1 < p.W && sFlag[2 * k + 1] != 0u);
         if (any) atomicOr(&sBits[k >> 5], 1u << (k & 31));
     }
+    ptx::fence_proxy_async_smem();  // the flags' memory is next written by TMA
     __syncthreads();
     if (warp == 0) {
         // compact list of the active tiles in ascending order (32 bitmap words, one per lane)
@@ -246,26 +254,31 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::prefetch_tmap(&tm_q);
             ptx::prefetch_tmap(&tm_k);
             ptx::prefetch_tmap(&tm_v);
+            // one copy per tile: the maps' outermost dimension is the 64-wide panel, so a box lands
+            // as the panels of the SW128 operand one after another
             ptx::mbar_arrive_expect_tx(bar(kMbQ), static_cast<uint32_t>(L::kQP * L::kQPanel));
-            for (int pn = 0; pn < L::kQP; ++pn)
-                ptx::tma_load_3d(sbase + L::kOffQ + pn * L::kQPanel, &tm_q, 64 * pn, hh, t0, bar(kMbQ));
-            // K and V of a tile refill separately: K as soon as S of the tile two back is done,
-            // V once its PV is done, so the K loads run a softmax ahead of the V loads
+            ptx::tma_load_4d(sbase + L::kOffQ, &tm_q, 0, t0, hh, 0, bar(kMbQ));
+            // K and V of a tile refill separately, V one tile behind K: K(j) waits for S(j - 2),
+            // V(j - 1) for PV(j - 3), the order in which the tensor cores finish them, so no K
+            // load waits behind a V slot
             int jk = 0, jv = 0;  // K and V tiles issued
-            for (int j = 0; j < nact; ++j) {
-                const int s = j % kMmStages;
-                const int key0 = static_cast<int>(sList[j]) * kMmBN;
-                const uint32_t st = sbase + L::kOffKV + s * L::kStageBytes;
-                if (j >= kMmStages && !wait(kMbKEmpty + s, ((j / kMmStages) - 1) & 1)) break;
-                ptx::mbar_arrive_expect_tx(bar(kMbKFull + s), static_cast<uint32_t>(L::kQP * L::kKPanel));
-                for (int pn = 0; pn < L::kQP; ++pn)
-                    ptx::tma_load_3d(st + pn * L::kKPanel, &tm_k, 64 * pn, hh, key0, bar(kMbKFull + s));
-                ++jk;
-                if (j >= kMmStages && !wait(kMbVEmpty + s, ((j / kMmStages) - 1) & 1)) break;
-                ptx::mbar_arrive_expect_tx(bar(kMbVFull + s), static_cast<uint32_t>(L::kVP * L::kKPanel));
-                for (int pn = 0; pn < L::kVP; ++pn)
-                    ptx::tma_load_3d(st + (L::kQP + pn) * L::kKPanel, &tm_v, 64 * pn, hh, key0, bar(kMbVFull + s));
-                ++jv;
+            for (int j = 0; j <= nact; ++j) {
+                if (j < nact) {
+                    const int s = j % kMmStages;
+                    if (j >= kMmStages && !wait(kMbKEmpty + s, ((j / kMmStages) - 1) & 1)) break;
+                    ptx::mbar_arrive_expect_tx(bar(kMbKFull + s), static_cast<uint32_t>(L::kQP * L::kKPanel));
+                    ptx::tma_load_4d(sbase + L::kOffKV + s * L::kStageBytes, &tm_k, 0,
+                                     static_cast<int>(sList[j]) * kMmBN, hh, 0, bar(kMbKFull + s));
+                    ++jk;
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, s = jj % kMmStages;
+                    if (jj >= kMmStages && !wait(kMbVEmpty + s, ((jj / kMmStages) - 1) & 1)) break;
+                    ptx::mbar_arrive_expect_tx(bar(kMbVFull + s), static_cast<uint32_t>(L::kVP * L::kKPanel));
+                    ptx::tma_load_4d(sbase + L::kOffKV + s * L::kStageBytes + L::kQP * L::kKPanel, &tm_v, 0,
+                                     static_cast<int>(sList[jj]) * kMmBN, hh, 0, bar(kMbVFull + s));
+                    ++jv;
+                }
             }
             // no copy may still be landing when the CTA leaves
             ptx::mbar_wait(bar(kMbQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
@@ -285,16 +298,15 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             const uint64_t dq = ptx::smem_desc_sw128(sbase + L::kOffQ, 16, 1024);
             const uint64_t dk = ptx::smem_desc_sw128(sbase + L::kOffKV, 16, 1024);
             const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
-            const uint64_t dp = ptx::smem_desc_sw128(sbase + L::kOffP, 16, 1024);
             auto issue_pv = [&](int jj) -> bool {
                 const int s = jj % kMmStages;
                 if (!wait(kMbVFull + s, (jj / kMmStages) & 1)) return false;
                 ptx::tc_fence_after();
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
-                const uint64_t p0 = dp + static_cast<uint64_t>(((jj & 1) * L::kPBytes) >> 4);
+                const uint32_t p0 = tmem + static_cast<uint32_t>(L::kColP + (jj & 1) * (kMmBN / 2));
 #pragma unroll
-                for (int k = 0; k < kMmBN / 16; ++k)
-                    ptx::mma_bf16_ss(tmem + 128, p0 + ((k * 32) >> 4), v0 + ((k * 2048) >> 4), kIdescPV,
+                for (int k = 0; k < kMmBN / 16; ++k)  // 16 keys: 8 columns of P, 16 rows of V
+                    ptx::mma_bf16_ts(tmem + L::kColO, p0 + 8 * k, v0 + ((k * 2048) >> 4), kIdescPV,
                                      (jj > 0 || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(kMbVEmpty + s));
                 ptx::mma_commit(bar(kMbPEmpty + (jj & 1)));
@@ -333,13 +345,23 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         __syncwarp();
     } else {
         // ================================================================ softmax / epilogue
-        const int quad = warp & 3;  // the TMEM lane quadrant this warp may access
+        // Two warps per TMEM lane quadrant: `half` 0 takes keys [0, 32) of each tile and O
+        // columns [0, DV/2), half 1 the rest.  The pair shares one named barrier per tile, a
+        // reduction that says whether any of its rows' maxima grew by more than 2^8 (or either
+        // warp gave up on a wait); only then do the two halves swap their tile maxima through
+        // shared memory.  Every thread of the pair takes the same barriers in the same order, so a
+        // warp that gives up keeps going to the next reduction, and both leave the loop there.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const int r = quad * 32 + lane;          // query row of this thread (its TMEM lane)
         const int64_t t = t0 + r;
         const bool live = t < p.T;
         const uint32_t* mrow = p.mask + (live ? t : 0) * p.W;
         const float c = p.sm_scale_log2;
+        const uint32_t pair_bar = 1u + static_cast<uint32_t>(quad);
+        volatile float* sX = reinterpret_cast<volatile float*>(smem + L::kOffX);
+        const int ocol0 = half * (DV / 2);
         float m = -CUDART_INF_F, l = 0.f;
         bool failed = false;
         auto warp_wait = [&](int i, uint32_t parity) -> bool {
@@ -349,117 +371,151 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             __syncwarp();
             return okw;
         };
-        auto mask_words = [&](int j) -> uint2 {
-            uint2 w = make_uint2(0u, 0u);
+        auto mask_word = [&](int j) -> uint32_t {
+            uint32_t w = 0u;
             if (live && j < nact) {
-                const int w0 = 2 * static_cast<int>(sList[j]);
-                w.x = __ldg(mrow + w0);
-                if (w0 + 1 < p.W) w.y = __ldg(mrow + w0 + 1);
+                const int wi = 2 * static_cast<int>(sList[j]) + half;
+                if (wi < p.W) w = __ldg(mrow + wi);
             }
             return w;
         };
-        uint2 mw = mask_words(0);
-        const uint32_t prow0 = sbase + L::kOffP + static_cast<uint32_t>(r) * 128u;
+        uint32_t mw = mask_word(0);
         for (int j = 0; j < nact; ++j) {
             const int s = j % kMmStages;
-            const uint2 cur = mw;
-            mw = mask_words(j + 1);
-            if (!warp_wait(kMbSFull + s, (j / kMmStages) & 1)) {
-                failed = true;
-                break;
-            }
-            ptx::tc_fence_after();
-            uint32_t sv[64];
-            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 0, sv);
-            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 16, sv + 16);
-            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32, sv + 32);
-            SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 48, sv + 48);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty + s));
-            // scaled logits of the set positions (log2 units), the tile's row max
+            const uint32_t cur = mw;
+            mw = mask_word(j + 1);
+            if (!failed && !warp_wait(kMbSFull + s, (j / kMmStages) & 1)) failed = true;
+            uint32_t sv[32];
             float mx = -CUDART_INF_F;
+            if (!failed) {
+                ptx::tc_fence_after();
+                SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32 * half, sv);
+                SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32 * half + 16, sv + 16);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty + s));
+                // scaled logits of the set positions (log2 units) and their max (eight partial
+                // maxima: no 32-long dependency chain)
+                float mxa[8];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const uint32_t bit = (i < 32 ? (cur.x >> i) : (cur.y >> (i - 32))) & 1u;
-                const float x = bit ? __uint_as_float(sv[i]) * c : -CUDART_INF_F;
-                sv[i] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int i = 0; i < 8; ++i) mxa[i] = -CUDART_INF_F;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 y = ptx::mul2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                               make_float2(c, c));
+                    const float x0 = (cur & (1u << (2 * i))) ? y.x : -CUDART_INF_F;
+                    const float x1 = (cur & (1u << (2 * i + 1))) ? y.y : -CUDART_INF_F;
+                    sv[2 * i] = __float_as_uint(x0);
+                    sv[2 * i + 1] = __float_as_uint(x1);
+                    mxa[(2 * i) & 7] = fmaxf(mxa[(2 * i) & 7], x0);
+                    mxa[(2 * i + 1) & 7] = fmaxf(mxa[(2 * i + 1) & 7], x1);
+                }
+                mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
             }
-            const bool grow = mx > m + kRescaleLog2;
             bool pv_waited = false;
-            if (__any_sync(0xffffffffu, grow)) {
-                // the running max of some row grew by more than 2^8: that row's O and sum are
-                // rescaled (the other rows of the warp multiply by 1); O must be complete
-                float alpha = 1.f;
-                if (grow) {
-                    const float mn = fmaxf(m, mx);
-                    alpha = (m == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(m - mn);
-                    m = mn;
-                    l *= alpha;
+            if (ptx::named_bar_red_or(pair_bar, 64u, failed || mx > m + kRescaleLog2)) {
+                // half 1 posts its tile max, half 0 posts the row's (NaN: a warp of the pair
+                // gave up)
+                if (half == 1) sX[r] = failed ? CUDART_NAN_F : mx;
+                ptx::named_bar_sync(pair_bar, 64u);
+                if (half == 0) {
+                    const float o = sX[r];
+                    sX[r] = (failed || o != o) ? CUDART_NAN_F : fmaxf(mx, o);
                 }
-                if (j > 0) {
-                    if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
-                        failed = true;
-                        break;
-                    }
-                    pv_waited = true;
-                    ptx::tc_fence_after();
-#pragma unroll 1
-                    for (int cc = 0; cc < DV / 16; ++cc) {
-                        uint32_t o[16];
-                        SMLA_TMEM_LD16(tmem + lane_base + 128 + cc * 16, o);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        SMLA_TMEM_ST16(tmem + lane_base + 128 + cc * 16, o);
-                    }
-                    ptx::tmem_wait_st();
-                }
-            }
-            // P = 2^(x - m) as bf16, row sums in fp32; P buffer j % 2 is rewritten only after
-            // PV(j - 2) has read it
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
-                const float p0 = x0 == -CUDART_INF_F ? 0.f : ptx::ex2_approx(x0 - m);
-                const float p1 = x1 == -CUDART_INF_F ? 0.f : ptx::ex2_approx(x1 - m);
-                l += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            if (j >= 2 && !pv_waited) {
-                if (!warp_wait(kMbPEmpty + (j & 1), ((j >> 1) - 1) & 1)) {
+                ptx::named_bar_sync(pair_bar, 64u);
+                const float v = sX[r];
+                if (v != v) {
                     failed = true;
                     break;
                 }
-            }
-            const uint32_t prow = prow0 + static_cast<uint32_t>((j & 1) * L::kPBytes);
-            // row r of the K-major SW128 P tile: 16-byte chunk q at ((q ^ (r & 7)) << 4)
+                mx = v;
+                const bool grow = mx > m + kRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    // the running max of some row grew by more than 2^8: that row's O half and
+                    // sum are rescaled (the other rows of the warp multiply by 1); O must be
+                    // complete
+                    float alpha = 1.f;
+                    if (grow) {
+                        const float mn = fmaxf(m, mx);
+                        alpha = (m == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(m - mn);
+                        m = mn;
+                        l *= alpha;
+                    }
+                    if (j > 0) {
+                        if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
+                            failed = true;
+                            continue;  // the next reduction takes both warps of the pair out
+                        }
+                        pv_waited = true;
+                        ptx::tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < DV / 32; ++cc) {
+                            uint32_t o[16];
+                            SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + cc * 16, o);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                ptx::st_shared_v4(prow + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4),
-                                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
-            ptx::fence_proxy_async_smem();
+                            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            SMLA_TMEM_ST16(tmem + lane_base + L::kColO + ocol0 + cc * 16, o);
+                        }
+                        ptx::tmem_wait_st();
+                    }
+                }
+            }
+            // P = 2^(x - m) as bf16, row sums in fp32 (a masked position holds -inf and gives 0;
+            // m is -inf only while every position seen so far is masked, and then any finite
+            // offset serves); P buffer j % 2 is rewritten only after PV(j - 2) has read it
+            const float nm = m == -CUDART_INF_F ? 0.f : -m;
+            uint32_t pk[16];
+            float2 la[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) la[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float2 d = ptx::add2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                           make_float2(nm, nm));
+                const float2 pp = make_float2(ptx::ex2_approx(d.x), ptx::ex2_approx(d.y));
+                la[i & 3] = ptx::add2(la[i & 3], pp);
+                pk[i] = pack_bf16x2(pp.x, pp.y);
+            }
+            l += ((la[0].x + la[0].y) + (la[1].x + la[1].y)) + ((la[2].x + la[2].y) + (la[3].x + la[3].y));
+            if (j >= 2 && !pv_waited) {
+                if (!warp_wait(kMbPEmpty + (j & 1), ((j >> 1) - 1) & 1)) {
+                    failed = true;
+                    continue;
+                }
+            }
+            // P(j) into its TMEM buffer, the operand A of PV(j): row r in lane r, keys 2c and
+            // 2c + 1 in column c (this half: keys 32 * half .. 32 * half + 31)
+            ptx::tc_fence_after();
+            SMLA_TMEM_ST16(tmem + lane_base + L::kColP + (j & 1) * (kMmBN / 2) + 16 * half, pk);
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kMbPFull + (j & 1)));
         }
-        // ---- epilogue: O / l as bf16 and the natural-log LSE
+        // ---- epilogue: O / l as bf16 and the natural-log LSE.  The pair's row sums meet in
+        // shared memory (three barriers, taken by both warps whatever happened in the loop).
         bool have_o = nact > 0 && !failed;
         if (have_o) {
             have_o = warp_wait(kMbPvDone, (nact - 1) & 1);
             if (have_o) ptx::tc_fence_after();
         }
+        ptx::named_bar_sync(pair_bar, 64u);
+        if (half == 1) sX[r] = l;
+        ptx::named_bar_sync(pair_bar, 64u);
+        if (half == 0) sX[r] = l + sX[r];
+        ptx::named_bar_sync(pair_bar, 64u);
+        const float lt = sX[r];
         if (!failed) {
-            const float inv = (have_o && l > 0.f) ? 1.0f / l : 0.f;
-            uint4* orow = reinterpret_cast<uint4*>(p.out + ((live ? t : 0) * p.h + hh) * DV);
+            const float inv = (have_o && lt > 0.f) ? 1.0f / lt : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(p.out + ((live ? t : 0) * p.h + hh) * DV + ocol0);
 #pragma unroll 1
-            for (int cc = 0; cc < DV / 16; ++cc) {
+            for (int cc = 0; cc < DV / 32; ++cc) {
                 uint32_t o[16];
                 if (have_o) {
-                    SMLA_TMEM_LD16(tmem + lane_base + 128 + cc * 16, o);
+                    SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + cc * 16, o);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -479,8 +535,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     orow[2 * cc + 1] = v1;
                 }
             }
-            if (live)
-                p.lse[t * p.h + hh] = (have_o && l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+            if (live && half == 0)
+                p.lse[t * p.h + hh] = (have_o && lt > 0.f) ? (m + log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
         }
         if (failed) *sAbort = 1;
     }
