@@ -840,6 +840,7 @@ smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, c
     alignas(64) CUtensorMap tm_q;
     alignas(64) CUtensorMap tm_k;
     alignas(64) CUtensorMap tm_v;
+    alignas(64) CUtensorMap tm_o;
     // [rows, h, d] viewed as (64 elements, rows, h, d / 64 panels): one box of (64, box_rows, 1,
     // d / 64) lands as d / 64 SW128 panels of box_rows x 128 bytes, one after another
     auto make = [&](CUtensorMap* tm, const void* base, int d, int64_t rows, uint32_t box_rows) -> CUresult {
@@ -855,7 +856,8 @@ smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, c
     CUresult r = make(&tm_q, q, dqk, T, smla::kMmBM);
     if (r == CUDA_SUCCESS) r = make(&tm_k, k, dqk, S, smla::kMmBN);
     if (r == CUDA_SUCCESS) r = make(&tm_v, v, dv, S, smla::kMmBN);
-    if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor maps for q/k/v failed (%d)", (int)r);
+    if (r == CUDA_SUCCESS) r = make(&tm_o, out, dv, T, smla::kMmBM);
+    if (r != CUDA_SUCCESS) return fail(SMLA_ERR_CUDA, "tensor maps for q/k/v/out failed (%d)", (int)r);
     smla::MmParams mp;
     mp.out = static_cast<__nv_bfloat16*>(out);
     mp.lse = lse;
@@ -878,16 +880,16 @@ smla_status sparse_mla_masked_mha(const void* q, const void* k, const void* v, c
     cudaError_t e;
     if (dqk == 192 && dv == 128) {
         cfg.dynamicSmemBytes = smla::MmLayout<192, 128>::kBytes;
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 128>, tm_q, tm_k, tm_v, mp);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 128>, tm_q, tm_k, tm_v, tm_o, mp);
     } else if (dqk == 192) {
         cfg.dynamicSmemBytes = smla::MmLayout<192, 256>::kBytes;
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 256>, tm_q, tm_k, tm_v, mp);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<192, 256>, tm_q, tm_k, tm_v, tm_o, mp);
     } else if (dv == 128) {
         cfg.dynamicSmemBytes = smla::MmLayout<256, 128>::kBytes;
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 128>, tm_q, tm_k, tm_v, mp);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 128>, tm_q, tm_k, tm_v, tm_o, mp);
     } else {
         cfg.dynamicSmemBytes = smla::MmLayout<256, 256>::kBytes;
-        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 256>, tm_q, tm_k, tm_v, mp);
+        e = cudaLaunchKernelEx(&cfg, smla::sparse_mla_masked_mha_kernel<256, 256>, tm_q, tm_k, tm_v, tm_o, mp);
     }
     if (e != cudaSuccess) return cuda_fail(e, "masked MHA kernel launch");
     return SMLA_OK;

@@ -19,22 +19,23 @@
 // sparse_mla_masked_mha_kernel<DQK, DV>: one CTA per (128-query tile, head).  Unlike the gather,
 // every K/V tile is shared by the tile's 128 queries, so this is a dense contraction on the
 // tensor cores:
-//   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T                   (M=128, N=64, K-major both)
-//   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]             (M=128, N=DV, V MN-major)
-// with S (double-buffered), P (double-buffered, bf16, the A operand of PV read from TMEM) and
-// O in TMEM.  Roles (320 threads):
-//   warp 0      TMA producer (one thread): Q once, then K and V tiles into a two-stage ring,
-//               one copy per tile (a 4-D map whose outer dimension is the 64-wide panel); V runs
-//               one tile behind K (K(j) waits for S(j-2), V(j-1) for PV(j-3), the order in which
-//               the tensor cores finish them);
-//   warp 1      MMA issuer (one thread) and TMEM owner: S(j) as soon as its tile has landed and
-//               its TMEM buffer is free, then PV(j-1) once P(j-1) is in TMEM;
-//   warps 2-9   softmax and epilogue, two warps per TMEM lane quadrant, one query row per
-//               thread: half 0 takes keys [0, 32) of a tile and O columns [0, DV/2), half 1 the
-//               rest.  The row's mask bits, a running max in log2 units with O rescaled only
-//               when the max grows by more than 2^8 (a pair-wide barrier reduction per tile says
-//               whether any row grew; only then do the halves swap maxima through shared
-//               memory), fp32 row sums per half, P as bf16 pairs into TMEM buffer j % 2.
+//   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T        (M=128, N=64; Q from TMEM, K from smem)
+//   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]  (M=128, N=DV; P from TMEM, V MN-major)
+// TMEM holds S, P (two buffers, bf16 pairs), Q (bf16 pairs, written once) and O; shared memory
+// is a K/V ring of as many stages as fit (3 or 4).  Roles (320 threads):
+//   warp 0      TMA producer (one thread): Q once into the ring (stage 1 on, before the key-tile
+//               pre-pass), then K and V tiles, one copy per tile (a 4-D map whose outer dimension
+//               is the 64-wide panel); V runs one tile behind K (K(j) waits for S(j - stages),
+//               V(j - 1) for PV(j - 1 - stages), the order in which the tensor cores finish them);
+//   warp 1      MMA issuer (one thread) and TMEM owner: S(j) once its tile has landed and the
+//               softmax warps hold S(j - 1) in registers, then PV(j - 1) once P(j - 1) is in TMEM;
+//   warps 2-9   Q from shared memory into TMEM, then softmax and epilogue, two warps per TMEM
+//               lane quadrant, one query row per thread: half 0 takes keys [0, 32) of a tile and
+//               O columns [0, DV/2), half 1 the rest.  The row's mask bits, a running max in log2
+//               units with O rescaled only when the max grows by more than 2^8 (a pair-wide
+//               barrier reduction per tile says whether any row grew; only then do the halves swap
+//               maxima through shared memory), fp32 row sums per half, P as bf16 pairs into TMEM
+//               buffer j % 2.  O / l leaves through shared memory and one TMA store.
 // Before the loop the CTA marks the 64-key tiles in which any of its rows has a bit set; only
 // those tiles are loaded and multiplied (lists over causal histories never reach past the
 // tile's last query, sparse lists skip whole tiles).  Every wait is bounded; a CTA that gives
@@ -47,7 +48,8 @@ namespace smla {
 
 constexpr int kMmBM = 128;                     // queries per tile (MMA M)
 constexpr int kMmBN = 64;                      // keys per tile
-constexpr int kMmStages = 2;
+constexpr int kMmMaxStages = 4;               // K/V ring depth: as many as shared memory holds, up to 4
+constexpr int kMmNumBars = 26;
 constexpr int kMmSoftmaxWarps = 8;             // two per TMEM lane quadrant
 constexpr int kMmThreads = 64 + 32 * kMmSoftmaxWarps;
 constexpr int kMmMaxS = 65536;                 // positions per request
@@ -59,41 +61,54 @@ template <int DQK, int DV>
 struct MmLayout {
     static_assert(DQK == 192 || DQK == 256, "q/k head dim 192 or 256");
     static_assert(DV == 128 || DV == 256, "v head dim 128 or 256");
-    static constexpr int kQP = DQK / 64;                       // 64-wide panels of q and k
+    static constexpr int kQP = DQK / 64;                       // 64-wide panels of k
     static constexpr int kVP = DV / 64;                        // 64-wide panels of v
-    static constexpr int kQPanel = kMmBM * 128;                // 128 rows x 128 bytes
     static constexpr int kKPanel = kMmBN * 128;                // 64 rows x 128 bytes
     static constexpr int kStageBytes = (kQP + kVP) * kKPanel;  // K tile then V tile
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kQP * kQPanel;
-    static constexpr int kOffTiles = kOffKV + kMmStages * kStageBytes;  // active key tiles: bitmap, then list
+    static constexpr int kFixedBytes = kMmMaxTiles / 8 + kMmMaxTiles * 2 + kMmNumBars * 8 + 16 + kMmBM * 4;
+    static constexpr int kStages = (232448 - kFixedBytes) / kStageBytes < kMmMaxStages
+                                       ? (232448 - kFixedBytes) / kStageBytes
+                                       : kMmMaxStages;
+    static constexpr int kOffKV = 0;
+    // Q lands (TMA, SW128 panels of 128 rows) in the ring from stage 1 on, until the softmax warps
+    // have copied it into TMEM; stage 0 holds the pre-pass's word flags until the first K load
+    static constexpr int kQPanel = kMmBM * 128;
+    static constexpr int kOffQ = kOffKV + kStageBytes;
+    static constexpr int kOffTiles = kOffKV + kStages * kStageBytes;  // active key tiles: bitmap, then list
     static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
     static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
-    static constexpr int kNumBars = 19;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort flag, tile count
+    static constexpr int kOffMisc = kOffBar + kMmNumBars * 8;  // tmem base, abort flag, tile count
     static constexpr int kOffX = kOffMisc + 16;                // row maxima / sums swapped by a warp pair
     static constexpr int kBytes = kOffX + kMmBM * 4;
-    // TMEM columns: S x2 [0, 128) | O [128, 128 + DV) | P x2 (bf16 pairs) [128 + DV, 192 + DV)
-    static constexpr int kColO = 128;
-    static constexpr int kColP = 128 + DV;
+    // TMEM columns: S [0, 64) | P x2 (bf16 pairs) [64, 128) | Q (bf16 pairs) [128, 128 + DQK/2)
+    // | O [256, 256 + DV)
+    static constexpr int kColS = 0;
+    static constexpr int kColP = 64;
+    static constexpr int kColQ = 128;
+    static constexpr int kColO = 256;
     static constexpr int kTmemCols = 512;
-    static_assert(kColP + 2 * (kMmBN / 2) <= kTmemCols, "TMEM columns");
-    static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 alignment");
+    static_assert(kColQ + DQK / 2 <= kColO && kColO + DV <= kTmemCols, "TMEM columns");
+    static_assert(kStages >= 2, "at least two K/V stages");
+    static_assert(kOffQ + kQP * kQPanel <= kOffKV + kStages * kStageBytes, "Q fits the ring after stage 0");
+    static_assert(kMmMaxS / 32 * 4 + 32 * 4 <= kStageBytes, "word flags and prefix sums fit stage 0");
+    static_assert(kVP * kQPanel <= kStages * kStageBytes, "the O tile fits the ring");
+    static_assert(kStageBytes % 1024 == 0, "SW128 alignment");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
 };
 
 enum : int {
-    kMbQ = 0,
-    kMbKFull = 1,    // +stage: the K tile landed
-    kMbKEmpty = 3,   // +stage: S of the tile is done, its K panels may be refilled
-    kMbSFull = 5,    // +buffer
-    kMbSEmpty = 7,   // +buffer
-    kMbPFull = 9,    // +buffer
-    kMbPEmpty = 11,  // +buffer
-    kMbPvDone = 13,
-    kMbDrain = 14,
-    kMbVFull = 15,   // +stage: the V tile landed
-    kMbVEmpty = 17   // +stage: PV of the tile is done, its V panels may be refilled
+    kMbKFull = 0,    // +stage: the K tile landed
+    kMbKEmpty = 4,   // +stage: S of the tile is done, its K panels may be refilled
+    kMbVFull = 8,    // +stage: the V tile landed
+    kMbVEmpty = 12,  // +stage: PV of the tile is done, its V panels may be refilled
+    kMbSFull = 16,
+    kMbSEmpty = 17,  // the softmax warps hold S in registers: the next S may be written
+    kMbPFull = 18,   // +buffer
+    kMbPEmpty = 20,  // +buffer
+    kMbPvDone = 22,
+    kMbDrain = 23,
+    kMbQFull = 24,   // the softmax warps have written Q into TMEM
+    kMbQLoad = 25    // Q landed in shared memory
 };
 
 struct ScatterParams {
@@ -143,7 +158,8 @@ struct MmParams {
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kMmThreads, 1)
     sparse_mla_masked_mha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                                 const __grid_constant__ CUtensorMap tm_v, const MmParams p) {
+                                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                                 const MmParams p) {
     using L = MmLayout<DQK, DV>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -172,15 +188,16 @@ __global__ void __launch_bounds__(kMmThreads, 1)
 
     if (threadIdx.x == 0) {
         *sAbort = 0;
-        ptx::mbar_init(bar(kMbQ), 1);
-        for (int s = 0; s < kMmStages; ++s) {
+        for (int s = 0; s < L::kStages; ++s) {
             ptx::mbar_init(bar(kMbKFull + s), 1);
             ptx::mbar_init(bar(kMbKEmpty + s), 1);
             ptx::mbar_init(bar(kMbVFull + s), 1);
             ptx::mbar_init(bar(kMbVEmpty + s), 1);
-            ptx::mbar_init(bar(kMbSFull + s), 1);
-            ptx::mbar_init(bar(kMbSEmpty + s), kMmSoftmaxWarps);
         }
+        ptx::mbar_init(bar(kMbSFull), 1);
+        ptx::mbar_init(bar(kMbSEmpty), kMmSoftmaxWarps);
+        ptx::mbar_init(bar(kMbQFull), kMmSoftmaxWarps);
+        ptx::mbar_init(bar(kMbQLoad), 1);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(kMbPFull + b), kMmSoftmaxWarps);
             ptx::mbar_init(bar(kMbPEmpty + b), 1);
@@ -198,6 +215,11 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
     __syncthreads();
+    if (threadIdx.x == 0) {  // Q's copy runs under the pre-pass
+        ptx::prefetch_tmap(&tm_q);
+        ptx::mbar_arrive_expect_tx(bar(kMbQLoad), static_cast<uint32_t>(L::kQP * L::kQPanel));
+        ptx::tma_load_4d(sbase + L::kOffQ, &tm_q, 0, t0, hh, 0, bar(kMbQLoad));
+    }
 
     // ---- the key tiles any row of this query tile attends to (tile k covers words 2k and 2k + 1).
     // Each warp takes rows, its lanes the row's words (coalesced, independent loads); a nonzero
@@ -209,22 +231,60 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     static_assert(L::kStageBytes >= kMmMaxS / 32 * 4, "word flags fit a K/V stage");
     for (int w = threadIdx.x; w < p.W; w += kMmThreads) sFlag[w] = 0u;
     __syncthreads();
-    for (int r = warp; r < kMmBM; r += kMmThreads / 32) {
-        const int64_t t = t0 + r;
-        if (t >= p.T) break;
-        const uint32_t* mrow = p.mask + t * p.W;
-        for (int w = lane; w < p.W; w += 32)
-            if (__ldg(mrow + w) != 0u) sFlag[w] = 1u;
+    {
+        // each warp ORs its rows' words in registers, all of its rows' loads in flight at once,
+        // then raises the flags of the nonzero words
+        const int nrows = p.T - t0 < kMmBM ? p.T - t0 : kMmBM;
+        constexpr int kWarps = kMmThreads / 32;
+        constexpr int kRows = (kMmBM + kWarps - 1) / kWarps;  // rows per warp
+        if ((p.W & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mask) & 15u) == 0) {
+            const int W4 = p.W >> 2;
+            for (int cw = lane; cw < W4; cw += 32) {
+                uint4 v[kRows];
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    const int r = warp + i * kWarps;
+                    v[i] = r < nrows ? __ldg(reinterpret_cast<const uint4*>(p.mask + static_cast<int64_t>(t0 + r) * p.W) + cw)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint4 acc = v[0];
+#pragma unroll
+                for (int i = 1; i < kRows; ++i) {
+                    acc.x |= v[i].x;
+                    acc.y |= v[i].y;
+                    acc.z |= v[i].z;
+                    acc.w |= v[i].w;
+                }
+                if (acc.x) sFlag[4 * cw] = 1u;
+                if (acc.y) sFlag[4 * cw + 1] = 1u;
+                if (acc.z) sFlag[4 * cw + 2] = 1u;
+                if (acc.w) sFlag[4 * cw + 3] = 1u;
+            }
+        } else {
+            for (int w = lane; w < p.W; w += 32) {
+                uint32_t v[kRows];
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    const int r = warp + i * kWarps;
+                    v[i] = r < nrows ? __ldg(p.mask + static_cast<int64_t>(t0 + r) * p.W + w) : 0u;
+                }
+                uint32_t acc = 0u;
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) acc |= v[i];
+                if (acc) sFlag[w] = 1u;
+            }
+        }
     }
     __syncthreads();
     for (int k = threadIdx.x; k < n_tiles; k += kMmThreads) {
         const bool any = sFlag[2 * k] != 0u || (2 * k + 1 < p.W && sFlag[2 * k + 1] != 0u);
         if (any) atomicOr(&sBits[k >> 5], 1u << (k & 31));
     }
-    ptx::fence_proxy_async_smem();  // the flags' memory is next written by TMA
     __syncthreads();
+    // compact list of the active tiles in ascending order: warp 0 scans the bitmap words' counts
+    // (one word per lane), then every thread places its tiles
+    int* sPre = reinterpret_cast<int*>(smem + L::kOffKV + kMmMaxS / 32 * 4);
     if (warp == 0) {
-        // compact list of the active tiles in ascending order (32 bitmap words, one per lane)
         const uint32_t bits = lane < (n_tiles + 31) / 32 ? sBits[lane] : 0u;
         const int cnt = __popc(bits);
         int pre = cnt;
@@ -233,15 +293,16 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             const int v = __shfl_up_sync(0xffffffffu, pre, o);
             if (lane >= o) pre += v;
         }
-        int pos = pre - cnt;
-        uint32_t b = bits;
-        while (b) {
-            const int i = __ffs(b) - 1;
-            b &= b - 1;
-            sList[pos++] = static_cast<uint16_t>(lane * 32 + i);
-        }
+        sPre[lane] = pre - cnt;
         if (lane == 31) *sNact = pre;
     }
+    __syncthreads();
+    for (int k = threadIdx.x; k < n_tiles; k += kMmThreads) {
+        const uint32_t word = sBits[k >> 5];
+        if ((word >> (k & 31)) & 1u)
+            sList[sPre[k >> 5] + __popc(word & ((1u << (k & 31)) - 1u))] = static_cast<uint16_t>(k);
+    }
+    ptx::fence_proxy_async_smem();  // the flags' and prefix sums' memory is next written by TMA
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -251,29 +312,27 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0 && nact > 0) {
-            ptx::prefetch_tmap(&tm_q);
             ptx::prefetch_tmap(&tm_k);
             ptx::prefetch_tmap(&tm_v);
             // one copy per tile: the maps' outermost dimension is the 64-wide panel, so a box lands
-            // as the panels of the SW128 operand one after another
-            ptx::mbar_arrive_expect_tx(bar(kMbQ), static_cast<uint32_t>(L::kQP * L::kQPanel));
-            ptx::tma_load_4d(sbase + L::kOffQ, &tm_q, 0, t0, hh, 0, bar(kMbQ));
-            // K and V of a tile refill separately, V one tile behind K: K(j) waits for S(j - 2),
-            // V(j - 1) for PV(j - 3), the order in which the tensor cores finish them, so no K
-            // load waits behind a V slot
+            // as the panels of the SW128 operand one after another.  K and V of a tile refill
+            // separately, V one tile behind K: K(j) waits for S(j - stages), V(j - 1) for
+            // PV(j - 1 - stages), the order in which the tensor cores finish them, so no K load
+            // waits behind a V slot
             int jk = 0, jv = 0;  // K and V tiles issued
             for (int j = 0; j <= nact; ++j) {
+                if (j == 1 && !wait(kMbQFull, 0)) break;  // stages 1 on hold Q until it is in TMEM
                 if (j < nact) {
-                    const int s = j % kMmStages;
-                    if (j >= kMmStages && !wait(kMbKEmpty + s, ((j / kMmStages) - 1) & 1)) break;
+                    const int s = j % L::kStages;
+                    if (j >= L::kStages && !wait(kMbKEmpty + s, ((j / L::kStages) - 1) & 1)) break;
                     ptx::mbar_arrive_expect_tx(bar(kMbKFull + s), static_cast<uint32_t>(L::kQP * L::kKPanel));
                     ptx::tma_load_4d(sbase + L::kOffKV + s * L::kStageBytes, &tm_k, 0,
                                      static_cast<int>(sList[j]) * kMmBN, hh, 0, bar(kMbKFull + s));
                     ++jk;
                 }
                 if (j >= 1) {
-                    const int jj = j - 1, s = jj % kMmStages;
-                    if (jj >= kMmStages && !wait(kMbVEmpty + s, ((jj / kMmStages) - 1) & 1)) break;
+                    const int jj = j - 1, s = jj % L::kStages;
+                    if (jj >= L::kStages && !wait(kMbVEmpty + s, ((jj / L::kStages) - 1) & 1)) break;
                     ptx::mbar_arrive_expect_tx(bar(kMbVFull + s), static_cast<uint32_t>(L::kVP * L::kKPanel));
                     ptx::tma_load_4d(sbase + L::kOffKV + s * L::kStageBytes + L::kQP * L::kKPanel, &tm_v, 0,
                                      static_cast<int>(sList[jj]) * kMmBN, hh, 0, bar(kMbVFull + s));
@@ -281,26 +340,25 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 }
             }
             // no copy may still be landing when the CTA leaves
-            ptx::mbar_wait(bar(kMbQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
-            for (int i = jk - (jk < kMmStages ? jk : kMmStages); i < jk; ++i)
-                ptx::mbar_wait(bar(kMbKFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
+            for (int i = jk - (jk < L::kStages ? jk : L::kStages); i < jk; ++i)
+                ptx::mbar_wait(bar(kMbKFull + i % L::kStages), (i / L::kStages) & 1, nullptr, &g_smla_error, 0u,
                                kDrainLimitNs);
-            for (int i = jv - (jv < kMmStages ? jv : kMmStages); i < jv; ++i)
-                ptx::mbar_wait(bar(kMbVFull + i % kMmStages), (i / kMmStages) & 1, nullptr, &g_smla_error, 0u,
+            for (int i = jv - (jv < L::kStages ? jv : L::kStages); i < jv; ++i)
+                ptx::mbar_wait(bar(kMbVFull + i % L::kStages), (i / L::kStages) & 1, nullptr, &g_smla_error, 0u,
                                kDrainLimitNs);
         }
+        if (lane == 0) ptx::mbar_wait(bar(kMbQLoad), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
         __syncwarp();
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0 && nact > 0) {
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kMmBM, kMmBN, 0, 0);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kMmBM, DV, 0, 1);
-            const uint64_t dq = ptx::smem_desc_sw128(sbase + L::kOffQ, 16, 1024);
             const uint64_t dk = ptx::smem_desc_sw128(sbase + L::kOffKV, 16, 1024);
             const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
             auto issue_pv = [&](int jj) -> bool {
-                const int s = jj % kMmStages;
-                if (!wait(kMbVFull + s, (jj / kMmStages) & 1)) return false;
+                const int s = jj % L::kStages;
+                if (!wait(kMbVFull + s, (jj / L::kStages) & 1)) return false;
                 ptx::tc_fence_after();
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
                 const uint32_t p0 = tmem + static_cast<uint32_t>(L::kColP + (jj & 1) * (kMmBN / 2));
@@ -313,21 +371,21 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 ptx::mma_commit(bar(kMbPvDone));
                 return true;
             };
-            bool ok = wait(kMbQ, 0);
+            // S(j) = Q K_j^T with Q from TMEM (16 dims: 8 columns) and K from the ring; S is one
+            // buffer, rewritten once the softmax warps hold S(j - 1) in registers
+            bool ok = wait(kMbQFull, 0);
             for (int j = 0; ok && j < nact; ++j) {
-                const int s = j % kMmStages;
-                if (!(ok = wait(kMbKFull + s, (j / kMmStages) & 1))) break;
-                if (j >= kMmStages && !(ok = wait(kMbSEmpty + s, ((j / kMmStages) - 1) & 1))) break;
+                const int s = j % L::kStages;
+                if (!(ok = wait(kMbKFull + s, (j / L::kStages) & 1))) break;
+                if (j >= 1 && !(ok = wait(kMbSEmpty, (j - 1) & 1))) break;
                 ptx::tc_fence_after();
                 const uint64_t k0 = dk + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
-                const uint32_t d = tmem + static_cast<uint32_t>(s * kMmBN);
 #pragma unroll
-                for (int pn = 0; pn < L::kQP; ++pn)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ptx::mma_bf16_ss(d, dq + ((pn * L::kQPanel + k * 32) >> 4), k0 + ((pn * L::kKPanel + k * 32) >> 4),
-                                         kIdescS, (pn | k) != 0 ? 1u : 0u);
-                ptx::mma_commit(bar(kMbSFull + s));
+                for (int kk = 0; kk < DQK / 16; ++kk)
+                    ptx::mma_bf16_ts(tmem + L::kColS, tmem + L::kColQ + 8 * kk,
+                                     k0 + (((kk >> 2) * L::kKPanel + (kk & 3) * 32) >> 4), kIdescS,
+                                     kk != 0 ? 1u : 0u);
+                ptx::mma_commit(bar(kMbSFull));
                 ptx::mma_commit(bar(kMbKEmpty + s));
                 if (j > 0) {
                     if (!(ok = wait(kMbPFull + ((j - 1) & 1), ((j - 1) >> 1) & 1))) break;
@@ -379,22 +437,47 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             }
             return w;
         };
+        if (nact > 0 && !(failed = !warp_wait(kMbQLoad, 0))) {
+            // Q (its TMA copy issued before the pre-pass; rows past the last token are zero) into
+            // TMEM, the A operand of every S: row r in lane r, dims 2c and 2c + 1 in column c
+            // (this half: dims DQK/2 * half .. DQK/2 * half + DQK/2 - 1).  The row's 16-byte
+            // chunk q of a 64-dim SW128 panel sits at ((q ^ (r & 7)) << 4).
+#pragma unroll
+            for (int cc = 0; cc < DQK / 64; ++cc) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int d0 = half * (DQK / 2) + 8 * (4 * cc + e);  // first dim of the chunk
+                    const uint32_t q = static_cast<uint32_t>((d0 & 63) >> 3);
+                    const uint4 v = ptx::ld_shared_v4(sbase + L::kOffQ + (d0 >> 6) * L::kQPanel + r * 128 +
+                                                      ((q ^ static_cast<uint32_t>(r & 7)) << 4));
+                    w[4 * e] = v.x;
+                    w[4 * e + 1] = v.y;
+                    w[4 * e + 2] = v.z;
+                    w[4 * e + 3] = v.w;
+                }
+                SMLA_TMEM_ST16(tmem + lane_base + L::kColQ + half * (DQK / 4) + 16 * cc, w);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kMbQFull));
+        }
         uint32_t mw = mask_word(0);
         for (int j = 0; j < nact; ++j) {
-            const int s = j % kMmStages;
             const uint32_t cur = mw;
             mw = mask_word(j + 1);
-            if (!failed && !warp_wait(kMbSFull + s, (j / kMmStages) & 1)) failed = true;
+            if (!failed && !warp_wait(kMbSFull, j & 1)) failed = true;
             uint32_t sv[32];
             float mx = -CUDART_INF_F;
             if (!failed) {
                 ptx::tc_fence_after();
-                SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32 * half, sv);
-                SMLA_TMEM_LD16(tmem + lane_base + s * kMmBN + 32 * half + 16, sv + 16);
+                SMLA_TMEM_LD16(tmem + lane_base + L::kColS + 32 * half, sv);
+                SMLA_TMEM_LD16(tmem + lane_base + L::kColS + 32 * half + 16, sv + 16);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty + s));
+                if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty));
                 // scaled logits of the set positions (log2 units) and their max (eight partial
                 // maxima: no 32-long dependency chain)
                 float mxa[8];
@@ -508,9 +591,11 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         if (half == 0) sX[r] = l + sX[r];
         ptx::named_bar_sync(pair_bar, 64u);
         const float lt = sX[r];
+        // O goes out through shared memory (the K/V ring, idle once the last PV is done) as
+        // DV/64 SW128 panels of 128 rows, then one TMA store: the rows' own global addresses are
+        // h * DV * 2 bytes apart, so direct stores would touch a line per lane
         if (!failed) {
             const float inv = (have_o && lt > 0.f) ? 1.0f / lt : 0.f;
-            uint4* orow = reinterpret_cast<uint4*>(p.out + ((live ? t : 0) * p.h + hh) * DV + ocol0);
 #pragma unroll 1
             for (int cc = 0; cc < DV / 32; ++cc) {
                 uint32_t o[16];
@@ -521,7 +606,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) o[e] = 0u;
                 }
-                if (live) {
+                {
                     uint4 v0, v1;
                     v0.x = pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv);
                     v0.y = pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv);
@@ -531,14 +616,25 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     v1.y = pack_bf16x2(__uint_as_float(o[10]) * inv, __uint_as_float(o[11]) * inv);
                     v1.z = pack_bf16x2(__uint_as_float(o[12]) * inv, __uint_as_float(o[13]) * inv);
                     v1.w = pack_bf16x2(__uint_as_float(o[14]) * inv, __uint_as_float(o[15]) * inv);
-                    orow[2 * cc] = v0;
-                    orow[2 * cc + 1] = v1;
+                    const int d0 = ocol0 + 16 * cc;  // first dim of chunk pair (2 x 8 dims)
+                    const uint32_t prow = sbase + L::kOffKV + (d0 >> 6) * L::kQPanel + r * 128;
+                    const uint32_t q0 = static_cast<uint32_t>((d0 & 63) >> 3);
+                    ptx::st_shared_v4(prow + ((q0 ^ static_cast<uint32_t>(r & 7)) << 4), v0);
+                    ptx::st_shared_v4(prow + (((q0 + 1) ^ static_cast<uint32_t>(r & 7)) << 4), v1);
                 }
             }
+            ptx::fence_proxy_async_smem();
             if (live && half == 0)
                 p.lse[t * p.h + hh] = (have_o && lt > 0.f) ? (m + log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
         }
         if (failed) *sAbort = 1;
+        // all eight warps' rows are in shared memory (none gave up): one thread stores the tile;
+        // rows past the last token fall outside the map and are not written
+        if (!ptx::named_bar_red_or(5u, 32u * kMmSoftmaxWarps, failed) && warp == 2 && lane == 0) {
+            ptx::tma_store_4d(&tm_o, sbase + L::kOffKV, 0, t0, hh, 0);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_0();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
