@@ -22,13 +22,16 @@
 //   S[128 q, 64 keys]  = Q[128 x DQK] . K_tile^T        (M=128, N=64; Q from TMEM, K from smem)
 //   O[128 q, DV]      += P[128 x 64] . V_tile[64 x DV]  (M=128, N=DV; P from TMEM, V MN-major)
 // TMEM holds S, P (two buffers, bf16 pairs), Q (bf16 pairs, written once) and O; shared memory
-// is a K/V ring of as many stages as fit (3 or 4).  Roles (320 threads):
+// is a K/V ring of as many stages as fit (3 or 4).  Roles (352 threads):
 //   warp 0      TMA producer (one thread): Q once into the ring (stage 1 on, before the key-tile
 //               pre-pass), then K and V tiles, one copy per tile (a 4-D map whose outer dimension
 //               is the 64-wide panel); V runs one tile behind K (K(j) waits for S(j - stages),
 //               V(j - 1) for PV(j - 1 - stages), the order in which the tensor cores finish them);
-//   warp 1      MMA issuer (one thread) and TMEM owner: S(j) once its tile has landed and the
-//               softmax warps hold S(j - 1) in registers, then PV(j - 1) once P(j - 1) is in TMEM;
+//   warp 1      S issuer (one thread) and TMEM owner: S(j) once its tile has landed and the
+//               softmax warps hold S(j - 1) in registers;
+//   warp 10     PV issuer (one thread): PV(j) once P(j) is in TMEM and V(j) has landed (two
+//               issuing threads, because a thread that issued MMAs stalls while the tensor cores
+//               run them, and its next wait would leave them idle);
 //   warps 2-9   Q from shared memory into TMEM, then softmax and epilogue, two warps per TMEM
 //               lane quadrant, one query row per thread: half 0 takes keys [0, 32) of a tile and
 //               O columns [0, DV/2), half 1 the rest.  The row's mask bits, a running max in log2
@@ -51,7 +54,7 @@ constexpr int kMmBN = 64;                      // keys per tile
 constexpr int kMmMaxStages = 4;               // K/V ring depth: as many as shared memory holds, up to 4
 constexpr int kMmNumBars = 26;
 constexpr int kMmSoftmaxWarps = 8;             // two per TMEM lane quadrant
-constexpr int kMmThreads = 64 + 32 * kMmSoftmaxWarps;
+constexpr int kMmThreads = 96 + 32 * kMmSoftmaxWarps;  // producer, S issuer, softmax x 8, PV issuer
 constexpr int kMmMaxS = 65536;                 // positions per request
 constexpr int kMmMaxTiles = kMmMaxS / kMmBN;   // 1024 key tiles
 constexpr int kScatterThreads = 256;
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             ptx::mbar_init(bar(kMbPEmpty + b), 1);
         }
         ptx::mbar_init(bar(kMbPvDone), 1);
-        ptx::mbar_init(bar(kMbDrain), 1);
+        ptx::mbar_init(bar(kMbDrain), 2);  // one commit from each issuing thread
         ptx::fence_mbarrier_init();
     }
     for (int i = threadIdx.x; i < kMmMaxTiles / 32; i += kMmThreads) sBits[i] = 0u;
@@ -350,29 +353,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         if (lane == 0) ptx::mbar_wait(bar(kMbQLoad), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
         __syncwarp();
     } else if (warp == 1) {
-        // ================================================================ MMA issuer
+        // ================================================================ S issuer (TMEM owner)
+        // S(j) = Q K_j^T with Q from TMEM (16 dims: 8 columns) and K from the ring; S is one
+        // buffer, rewritten once the softmax warps hold S(j - 1) in registers
         if (lane == 0 && nact > 0) {
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kMmBM, kMmBN, 0, 0);
-            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kMmBM, DV, 0, 1);
             const uint64_t dk = ptx::smem_desc_sw128(sbase + L::kOffKV, 16, 1024);
-            const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
-            auto issue_pv = [&](int jj) -> bool {
-                const int s = jj % L::kStages;
-                if (!wait(kMbVFull + s, (jj / L::kStages) & 1)) return false;
-                ptx::tc_fence_after();
-                const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
-                const uint32_t p0 = tmem + static_cast<uint32_t>(L::kColP + (jj & 1) * (kMmBN / 2));
-#pragma unroll
-                for (int k = 0; k < kMmBN / 16; ++k)  // 16 keys: 8 columns of P, 16 rows of V
-                    ptx::mma_bf16_ts(tmem + L::kColO, p0 + 8 * k, v0 + ((k * 2048) >> 4), kIdescPV,
-                                     (jj > 0 || k > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(kMbVEmpty + s));
-                ptx::mma_commit(bar(kMbPEmpty + (jj & 1)));
-                ptx::mma_commit(bar(kMbPvDone));
-                return true;
-            };
-            // S(j) = Q K_j^T with Q from TMEM (16 dims: 8 columns) and K from the ring; S is one
-            // buffer, rewritten once the softmax warps hold S(j - 1) in registers
             bool ok = wait(kMbQFull, 0);
             for (int j = 0; ok && j < nact; ++j) {
                 const int s = j % L::kStages;
@@ -387,16 +373,38 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                                      kk != 0 ? 1u : 0u);
                 ptx::mma_commit(bar(kMbSFull));
                 ptx::mma_commit(bar(kMbKEmpty + s));
-                if (j > 0) {
-                    if (!(ok = wait(kMbPFull + ((j - 1) & 1), ((j - 1) >> 1) & 1))) break;
-                    ptx::tc_fence_after();
-                    if (!(ok = issue_pv(j - 1))) break;
-                }
             }
-            if (ok && wait(kMbPFull + ((nact - 1) & 1), ((nact - 1) >> 1) & 1)) {
+        }
+        if (lane == 0) {  // this thread's MMAs are done before TMEM is freed
+            ptx::mma_commit(bar(kMbDrain));
+            ptx::mbar_wait(bar(kMbDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == kMmThreads / 32 - 1) {
+        // ================================================================ PV issuer
+        // O += P(j) V_j with P from TMEM buffer j % 2 (16 keys: 8 columns) and V MN-major from the
+        // ring.  A thread of its own, so that a PV waiting for its P or V never holds back an S
+        // (an issuing thread stalls while the tensor cores run what it issued).
+        if (lane == 0 && nact > 0) {
+            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kMmBM, DV, 0, 1);
+            const uint64_t dv = ptx::smem_desc_sw128(sbase + L::kOffKV + L::kQP * L::kKPanel, L::kKPanel, 1024);
+            for (int j = 0; j < nact; ++j) {
+                const int s = j % L::kStages;
+                if (!wait(kMbPFull + (j & 1), (j >> 1) & 1)) break;
+                if (!wait(kMbVFull + s, (j / L::kStages) & 1)) break;
                 ptx::tc_fence_after();
-                issue_pv(nact - 1);  // a failed wait inside has flagged the abort
+                const uint64_t v0 = dv + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
+                const uint32_t p0 = tmem + static_cast<uint32_t>(L::kColP + (j & 1) * (kMmBN / 2));
+#pragma unroll
+                for (int k = 0; k < kMmBN / 16; ++k)
+                    ptx::mma_bf16_ts(tmem + L::kColO, p0 + 8 * k, v0 + ((k * 2048) >> 4), kIdescPV,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(kMbVEmpty + s));
+                ptx::mma_commit(bar(kMbPEmpty + (j & 1)));
+                ptx::mma_commit(bar(kMbPvDone));
             }
+        }
+        if (lane == 0) {
             ptx::mma_commit(bar(kMbDrain));
             ptx::mbar_wait(bar(kMbDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
         }
