@@ -130,8 +130,11 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t src,
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Waits until every committed bulk group of this thread has completed (its writes done).
-__device__ __forceinline__ void bulk_wait_group_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until every committed bulk group of this thread has read its shared-memory source (the
+// global writes finish on their own).
+__device__ __forceinline__ void bulk_wait_group_read_0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // 1-D bulk copy global -> shared, completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,

@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         if (!ptx::named_bar_red_or(5u, 32u * kMmSoftmaxWarps, failed) && warp == 2 && lane == 0) {
             ptx::tma_store_4d(&tm_o, sbase + L::kOffKV, 0, t0, hh, 0);
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_0();
+            ptx::bulk_wait_group_read_0();  // shared memory may not be released before it is read
         }
     }
     ptx::tc_fence_before();
