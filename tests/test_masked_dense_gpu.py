@@ -150,3 +150,36 @@ def test_full_size_glm5_prefill_sampled_tokens():
     toks = sorted(set([0, 127, 128, 2047, 2048, T - 1] + torch.randint(0, T, (10,), generator=g).tolist()))
     ref_o, ref_l = oracle.masked_mha(q[toks], k, v, oracle.scatter_mask(lists[toks], S), dqk ** -0.5)
     assert_parity(out.cpu()[toks], lse.cpu()[toks], ref_o, ref_l, what="glm5 full sampled")
+
+
+def test_every_list_empty_writes_zeros_everywhere():
+    # no query tile reaches any key tile: every CTA skips its loop, still drains the copy of Q it
+    # started, and stores zeros over whatever the output held (two query tiles, the second ragged)
+    T, S, h = 200, 500, 3
+    q, k, v = (x.to(DEV) for x in make_masked_dense_inputs(T, S, h, 192, 256, seed=21))
+    lists = torch.full((T, 16), -1, dtype=torch.int32, device=DEV)
+    mask = smla.sparse_mla_scatter_mask(lists, S)
+    out = torch.full((T, h, 256), 7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, h), 3.0, dtype=torch.float32, device=DEV)
+    smla.sparse_mla_masked_mha(q, k, v, mask, 0.05, out=out, lse=lse)
+    smla.sync_status()
+    assert int(out.float().abs().sum()) == 0
+    assert torch.all(torch.isneginf(lse.cpu()))
+
+
+def test_longest_request_reaches_the_last_key_tiles():
+    # S at its maximum (65536 positions, 1024 key tiles): sparse lists over the whole range, so
+    # the tile list holds indices up to 1023; two query tiles, the second ragged
+    T, S, h = 130, 65536, 1
+    q, k, v = make_masked_dense_inputs(T, S, h, 256, 128, seed=23)
+    g = torch.Generator().manual_seed(24)
+    lists = torch.randint(0, S, (T, 48), generator=g, dtype=torch.int32)
+    lists[:, 0] = S - 1
+    lists[:, 1] = 0
+    lists[::5, 2:] = -1
+    mask = smla.sparse_mla_scatter_mask(lists.to(DEV), S)
+    out, lse = smla.sparse_mla_masked_mha(q.to(DEV), k.to(DEV), v.to(DEV), mask, 256 ** -0.5)
+    smla.sync_status()
+    assert np.array_equal(_mask_u32(mask), oracle.scatter_mask(lists, S))
+    ref_o, ref_l = oracle.masked_mha(q, k, v, oracle.scatter_mask(lists, S), 256 ** -0.5)
+    assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, what="S = 65536")
