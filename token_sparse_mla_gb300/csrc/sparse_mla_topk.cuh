@@ -6,17 +6,18 @@
 // to the lower position, written in ascending position order, mapped through a block table of
 // 64-slot blocks to cache slots (or left as positions), -1 padded when the history is shorter.
 //
-// One CTA per row.  Radix select on an order-preserving 32-bit key, one byte per pass: a
-// shared-memory histogram of the candidates that match the prefix found so far, then one warp
-// scans the 256 bins from the top for the bin where the count reaches the number still to take.
-// Each pass scans the row, four scores per 16-byte load when the row is 16-byte aligned.
-// After four passes the threshold key is exact; a last scan in position order writes every
-// key above it and the first ties at it, with a block-wide scan giving each selected position
-// its output slot.  The first scan reads the row from HBM; the later ones find it in L1 or L2.
-// (Copying the candidates left after the first byte into shared memory for the last two
-// passes, through one shared counter, measured slower: 2.73 vs 2.39 ms on the prefill rows.)
-// 256 threads a CTA: at 48 registers five rows share an SM, so one row's barrier-separated
-// phases overlap another's scans (1.74 ms on the prefill rows, 2.25 ms at 512 threads).
+// One CTA per row.  Radix select on an order-preserving 32-bit key: a 4096-bin shared-memory
+// histogram of the keys' top 12 bits over the row, a block-wide scan of the bins from the top
+// for the bin where the count reaches k, then one more scan of the row that copies the keys of
+// that bin into shared memory (a few hundred on score distributions like a normal one).  The
+// remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates alone; when the
+// bin holds more keys than the buffer (many equal scores), those passes scan the row instead.
+// The threshold key is then exact; a last scan in position order writes every key above it and
+// the first ties at it, with a block-wide scan giving each selected position its output slot.
+// Each scan of the row takes four scores per 16-byte load when the row is 16-byte aligned; the
+// first reads it from HBM, the later ones find it in L1 or L2.  So three scans of the row
+// instead of five (one histogram per byte).  256 threads a CTA: several rows share an SM and
+// one row's barrier-separated phases overlap another's scans.
 #pragma once
 
 #include "sparse_mla_common.cuh"
@@ -25,8 +26,10 @@ namespace smla {
 
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkPerThread = 4;                          // consecutive scores per thread
+constexpr int kTopkPerThread = 16;                         // consecutive scores per thread
 constexpr int kTopkChunk = kTopkThreads * kTopkPerThread;  // scores per compaction step
+constexpr int kTopkBins0 = 4096;                           // first pass: the top 12 key bits
+constexpr int kTopkCand = 2048;                            // candidate keys held in shared memory
 
 struct TopkParams {
     const float* scores;         // [T, S]
@@ -80,10 +83,49 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea
     __syncthreads();  // s_warp is reused by the next call
 }
 
-__global__ void __launch_bounds__(kTopkThreads) sparse_mla_topk_kernel(const TopkParams p) {
-    __shared__ uint32_t hist[256];
+// The bin of hist[0, nb) (nb = 16, 256 or 4096) where the count of keys, taken from the top bin
+// down, reaches krem (1 <= krem <= the total): thread i covers nb / 256 bins (one when nb <=
+// 256) from the top, a block-wide scan of the threads' totals finds the one thread whose bins
+// hold the krem-th key, and that thread writes the bin and the count above it to s_sel[0..1].
+// Every thread reads them after the closing barrier.
+__device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* s_warp,
+                                              uint32_t* s_sel) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nb > kTopkThreads ? nb / kTopkThreads : 1;
+    const int top = nb - 1 - per * tid;  // this thread's highest bin
+    uint32_t tot = 0;
+    if (top >= 0)
+        for (int j = 0; j < per; ++j) tot += hist[top - j];
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    uint32_t above = incl - tot;
+    for (int w = 0; w < warp; ++w) above += s_warp[w];
+    if (above < krem && krem <= above + tot) {
+        uint32_t a = above;
+        for (int j = 0; j < per; ++j) {
+            const uint32_t c = hist[top - j];
+            if (a + c >= krem) {
+                s_sel[0] = static_cast<uint32_t>(top - j);
+                s_sel[1] = a;
+                break;
+            }
+            a += c;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const TopkParams p) {
+    __shared__ uint32_t hist[kTopkBins0];
+    __shared__ uint32_t cand[kTopkCand];
     __shared__ uint32_t s_warp[2 * kTopkWarps];
-    __shared__ uint32_t s_sel[2];
+    __shared__ uint32_t s_sel[3];
     // launched as a programmatic dependent: the scores may be the previous launch's output
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
@@ -96,68 +138,64 @@ __global__ void __launch_bounds__(kTopkThreads) sparse_mla_topk_kernel(const Top
     const int k = n < p.topk ? n : p.topk;
     const bool take_all = k == n;  // the history is no longer than topk: every position
 
-    // ---- radix select of the threshold key: the k-th largest, one byte per pass
+    // ---- radix select of the threshold key: the k-th largest
     uint32_t prefix = 0, pmask = 0, krem = static_cast<uint32_t>(k);
-    if (threadIdx.x == 0) s_sel[0] = s_sel[1] = 0u;  // read only after a barrier
     // 16-byte loads when the row starts on a 16-byte boundary (S a multiple of 4)
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     const int n4 = vec ? n / 4 : 0;
+    auto scan_row = [&](auto&& visit) {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        for (int i = threadIdx.x; i < n4; i += kTopkThreads) {
+            const float4 v = __ldg(row4 + i);
+            visit(score_key(v.x));
+            visit(score_key(v.y));
+            visit(score_key(v.z));
+            visit(score_key(v.w));
+        }
+        for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) visit(score_key(__ldg(row + i)));
+    };
     if (!take_all) {
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = threadIdx.x; i < 256; i += kTopkThreads) hist[i] = 0;
+        // pass 1: the top 12 bits of every key
+        for (int i = threadIdx.x; i < kTopkBins0; i += kTopkThreads) hist[i] = 0;
+        if (threadIdx.x == 0) s_sel[2] = 0;
+        __syncthreads();
+        scan_row([&](uint32_t key) { atomicAdd(&hist[key >> 20], 1u); });
+        __syncthreads();
+        topk_find_bin(hist, kTopkBins0, krem, s_warp, s_sel);
+        krem -= s_sel[1];
+        prefix = s_sel[0] << 20;
+        pmask = 0xFFF00000u;
+        // pass 2: the keys of that bin into shared memory (the count goes on past the buffer)
+        scan_row([&](uint32_t key) {
+            if ((key & pmask) == prefix) {
+                const uint32_t c = atomicAdd(&s_sel[2], 1u);
+                if (c < kTopkCand) cand[c] = key;
+            }
+        });
+        __syncthreads();
+        const uint32_t ncand = s_sel[2];
+        const bool in_smem = ncand <= static_cast<uint32_t>(kTopkCand);
+        // passes 3-5: key bits 19-12, 11-4 and 3-0, over the candidates (over the row when
+        // they did not fit)
+#pragma unroll 1
+        for (int step = 0; step < 3; ++step) {
+            const int shift = step == 0 ? 12 : (step == 1 ? 4 : 0);
+            const int nb = step == 2 ? 16 : 256;
+            for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
             __syncthreads();
-            auto count = [&](float x) {
-                const uint32_t key = score_key(x);
-                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            auto count = [&](uint32_t key) {
+                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
             };
-            const float4* row4 = reinterpret_cast<const float4*>(row);
-            for (int i = threadIdx.x; i < n4; i += kTopkThreads) {
-                const float4 v = __ldg(row4 + i);
-                count(v.x);
-                count(v.y);
-                count(v.z);
-                count(v.w);
-            }
-            for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) count(__ldg(row + i));
-            __syncthreads();
-            if (threadIdx.x < 32) {
-                // lane l holds bins 255 - 8l - j (j = 0..7), highest first
-                const int lane = threadIdx.x;
-                uint32_t c[8], tot = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = hist[255 - 8 * lane - j];
-                    tot += c[j];
-                }
-                uint32_t incl = tot;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += x;
-                }
-                const uint32_t above = incl - tot;  // candidates in higher bins
-                const bool mine = above < krem && krem <= above + tot;
-                const unsigned m = __ballot_sync(0xffffffffu, mine);
-                if (lane == __ffs(m) - 1) {
-                    uint32_t a = above;
-                    int bin = -1;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (bin < 0) {
-                            if (a + c[j] >= krem)
-                                bin = 255 - 8 * lane - j;
-                            else
-                                a += c[j];
-                        }
-                    }
-                    s_sel[0] = static_cast<uint32_t>(bin);
-                    s_sel[1] = a;
-                }
+            if (in_smem) {
+                for (int c = threadIdx.x; c < static_cast<int>(ncand); c += kTopkThreads) count(cand[c]);
+            } else {
+                scan_row(count);
             }
             __syncthreads();
+            topk_find_bin(hist, nb, krem, s_warp, s_sel);
             krem -= s_sel[1];
             prefix |= s_sel[0] << shift;
-            pmask |= 0xFFu << shift;
+            pmask |= static_cast<uint32_t>(nb - 1) << shift;
             __syncthreads();  // hist and s_sel are rewritten by the next pass
         }
     }
@@ -167,11 +205,27 @@ __global__ void __launch_bounds__(kTopkThreads) sparse_mla_topk_kernel(const Top
     for (int c0 = 0; c0 < n; c0 += kTopkChunk) {
         const int i0 = c0 + static_cast<int>(threadIdx.x) * kTopkPerThread;
         uint32_t flags = 0, ngt = 0, neq = 0;  // 2 bits per score: above, tie
+        float xs[kTopkPerThread];
+        if (!take_all) {
+            if (vec && i0 + kTopkPerThread <= n) {  // i0 is a multiple of 16: aligned
+#pragma unroll
+                for (int e = 0; e < kTopkPerThread / 4; ++e) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0) + e);
+                    xs[4 * e] = v.x;
+                    xs[4 * e + 1] = v.y;
+                    xs[4 * e + 2] = v.z;
+                    xs[4 * e + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kTopkPerThread; ++e) xs[e] = i0 + e < n ? __ldg(row + i0 + e) : 0.f;
+            }
+        }
 #pragma unroll
         for (int e = 0; e < kTopkPerThread; ++e) {
             const int i = i0 + e;
             if (i < n) {
-                const uint32_t key = take_all ? 0u : score_key(__ldg(row + i));
+                const uint32_t key = take_all ? 0u : score_key(xs[e]);
                 if (take_all || key > prefix) {
                     flags |= 1u << (2 * e);
                     ++ngt;
