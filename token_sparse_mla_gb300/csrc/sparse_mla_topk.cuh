@@ -204,7 +204,6 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
     uint32_t base_gt = 0, base_eq = 0;
     for (int c0 = 0; c0 < n; c0 += kTopkChunk) {
         const int i0 = c0 + static_cast<int>(threadIdx.x) * kTopkPerThread;
-        uint32_t flags = 0, ngt = 0, neq = 0;  // 2 bits per score: above, tie
         float xs[kTopkPerThread];
         if (!take_all) {
             if (vec && i0 + kTopkPerThread <= n) {  // i0 is a multiple of 16: aligned
@@ -221,32 +220,28 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
                 for (int e = 0; e < kTopkPerThread; ++e) xs[e] = i0 + e < n ? __ldg(row + i0 + e) : 0.f;
             }
         }
+        // bit e of gt / eq: score i0 + e is above the threshold / equal to it
+        uint32_t gt = 0, eq = 0;
 #pragma unroll
         for (int e = 0; e < kTopkPerThread; ++e) {
-            const int i = i0 + e;
-            if (i < n) {
+            if (i0 + e < n) {
                 const uint32_t key = take_all ? 0u : score_key(xs[e]);
-                if (take_all || key > prefix) {
-                    flags |= 1u << (2 * e);
-                    ++ngt;
-                } else if (key == prefix) {
-                    flags |= 2u << (2 * e);
-                    ++neq;
-                }
+                gt |= static_cast<uint32_t>(take_all || key > prefix) << e;
+                eq |= static_cast<uint32_t>(!take_all && key == prefix) << e;
             }
         }
         uint32_t egt, eeq, tgt, teq;
-        block_scan2(ngt, neq, egt, eeq, tgt, teq, s_warp);
+        block_scan2(__popc(gt), __popc(eq), egt, eeq, tgt, teq, s_warp);
         uint32_t rgt = base_gt + egt, req = base_eq + eeq;
-#pragma unroll
-        for (int e = 0; e < kTopkPerThread; ++e) {
+        // only the marked scores, in position order
+        for (uint32_t m = gt | eq; m != 0u; m &= m - 1u) {
+            const int e = __ffs(m) - 1;
             const int i = i0 + e;
-            const uint32_t f = (flags >> (2 * e)) & 3u;
             int slot_out = -1;
-            if (f == 1u) {
+            if ((gt >> e) & 1u) {
                 slot_out = static_cast<int>(rgt + (req < krem ? req : krem));
                 ++rgt;
-            } else if (f == 2u) {
+            } else {
                 if (req < krem) slot_out = static_cast<int>(rgt + req);
                 ++req;
             }
