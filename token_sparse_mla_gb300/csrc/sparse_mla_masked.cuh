@@ -604,27 +604,33 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         // h * DV * 2 bytes apart, so direct stores would touch a line per lane
         if (!failed) {
             const float inv = (have_o && lt > 0.f) ? 1.0f / lt : 0.f;
+            // this half's DV/2 columns, four 16-column TMEM loads per wait
 #pragma unroll 1
-            for (int cc = 0; cc < DV / 32; ++cc) {
-                uint32_t o[16];
+            for (int cg = 0; cg < DV / 128; ++cg) {
+                uint32_t o[4][16];
                 if (have_o) {
-                    SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + cc * 16, o);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + (4 * cg + g) * 16, o[g]);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = 0u;
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[g][e] = 0u;
                 }
-                {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
                     uint4 v0, v1;
-                    v0.x = pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv);
-                    v0.y = pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv);
-                    v0.z = pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv);
-                    v0.w = pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv);
-                    v1.x = pack_bf16x2(__uint_as_float(o[8]) * inv, __uint_as_float(o[9]) * inv);
-                    v1.y = pack_bf16x2(__uint_as_float(o[10]) * inv, __uint_as_float(o[11]) * inv);
-                    v1.z = pack_bf16x2(__uint_as_float(o[12]) * inv, __uint_as_float(o[13]) * inv);
-                    v1.w = pack_bf16x2(__uint_as_float(o[14]) * inv, __uint_as_float(o[15]) * inv);
-                    const int d0 = ocol0 + 16 * cc;  // first dim of chunk pair (2 x 8 dims)
+                    v0.x = pack_bf16x2(__uint_as_float(o[g][0]) * inv, __uint_as_float(o[g][1]) * inv);
+                    v0.y = pack_bf16x2(__uint_as_float(o[g][2]) * inv, __uint_as_float(o[g][3]) * inv);
+                    v0.z = pack_bf16x2(__uint_as_float(o[g][4]) * inv, __uint_as_float(o[g][5]) * inv);
+                    v0.w = pack_bf16x2(__uint_as_float(o[g][6]) * inv, __uint_as_float(o[g][7]) * inv);
+                    v1.x = pack_bf16x2(__uint_as_float(o[g][8]) * inv, __uint_as_float(o[g][9]) * inv);
+                    v1.y = pack_bf16x2(__uint_as_float(o[g][10]) * inv, __uint_as_float(o[g][11]) * inv);
+                    v1.z = pack_bf16x2(__uint_as_float(o[g][12]) * inv, __uint_as_float(o[g][13]) * inv);
+                    v1.w = pack_bf16x2(__uint_as_float(o[g][14]) * inv, __uint_as_float(o[g][15]) * inv);
+                    const int d0 = ocol0 + 16 * (4 * cg + g);  // first dim of chunk pair (2 x 8 dims)
                     const uint32_t prow = sbase + L::kOffKV + (d0 >> 6) * L::kQPanel + r * 128;
                     const uint32_t q0 = static_cast<uint32_t>((d0 & 63) >> 3);
                     ptx::st_shared_v4(prow + ((q0 ^ static_cast<uint32_t>(r & 7)) << 4), v0);
