@@ -305,6 +305,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
           "=r"((r)[12]), "=r"((r)[13]), "=r"((r)[14]), "=r"((r)[15])                              \
         : "r"(taddr))
 
+#define SMLA_TMEM_ST8(taddr, r)                                                                   \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"          \
+                 ::"r"(taddr), "r"((r)[0]), "r"((r)[1]), "r"((r)[2]), "r"((r)[3]), "r"((r)[4]),     \
+                 "r"((r)[5]), "r"((r)[6]), "r"((r)[7])                                             \
+                 : "memory")
+
 #define SMLA_TMEM_ST16(taddr, r)                                                                  \
     asm volatile(                                                                                 \
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" \

@@ -29,16 +29,18 @@
 //               V(j - 1) for PV(j - 1 - stages), the order in which the tensor cores finish them);
 //   warp 1      S issuer (one thread) and TMEM owner: S(j) once its tile has landed and the
 //               softmax warps hold S(j - 1) in registers;
-//   warp 10     PV issuer (one thread): PV(j) once P(j) is in TMEM and V(j) has landed (two
+//   last warp   PV issuer (one thread): PV(j) once P(j) is in TMEM and V(j) has landed (two
 //               issuing threads, because a thread that issued MMAs stalls while the tensor cores
 //               run them, and its next wait would leave them idle);
-//   warps 2-9   Q from shared memory into TMEM, then softmax and epilogue, two warps per TMEM
-//               lane quadrant, one query row per thread: half 0 takes keys [0, 32) of a tile and
-//               O columns [0, DV/2), half 1 the rest.  The row's mask bits, a running max in log2
-//               units with O rescaled only when the max grows by more than 2^8 (a pair-wide
-//               barrier reduction per tile says whether any row grew; only then do the halves swap
-//               maxima through shared memory), fp32 row sums per half, P as bf16 pairs into TMEM
-//               buffer j % 2.  O / l leaves through shared memory and one TMA store.
+//   warps 2-9   Q from shared memory into TMEM, then softmax and epilogue, kMmParts (two) warps
+//               per TMEM lane quadrant, one query row per thread, each on 64 / kMmParts keys of
+//               a tile and DV / kMmParts columns of O.  The row's mask bits, a running max in
+//               log2 units with O rescaled only when the max grows by more than 2^8 (a barrier
+//               reduction per tile over the quadrant's warps says whether any row grew; only then
+//               do they swap maxima through shared memory), fp32 row sums per warp, P as bf16
+//               pairs into TMEM buffer j % 2.  O / l leaves through shared memory and one TMA
+//               store.  (Four warps per quadrant measured 0.679 ms against 0.614 on the 4096-token
+//               GLM-5 chunk: the extra barrier arrivals cost more than the shorter passes save.)
 // Before the loop the CTA marks the 64-key tiles in which any of its rows has a bit set; only
 // those tiles are loaded and multiplied (lists over causal histories never reach past the
 // tile's last query, sparse lists skip whole tiles).  Every wait is bounded; a CTA that gives
@@ -53,8 +55,9 @@ constexpr int kMmBM = 128;                     // queries per tile (MMA M)
 constexpr int kMmBN = 64;                      // keys per tile
 constexpr int kMmMaxStages = 4;               // K/V ring depth: as many as shared memory holds, up to 4
 constexpr int kMmNumBars = 26;
-constexpr int kMmSoftmaxWarps = 8;             // two per TMEM lane quadrant
-constexpr int kMmThreads = 96 + 32 * kMmSoftmaxWarps;  // producer, S issuer, softmax x 8, PV issuer
+constexpr int kMmParts = 2;                    // softmax warps per TMEM lane quadrant
+constexpr int kMmSoftmaxWarps = 4 * kMmParts;
+constexpr int kMmThreads = 96 + 32 * kMmSoftmaxWarps;  // producer, S issuer, softmax warps, PV issuer
 constexpr int kMmMaxS = 65536;                 // positions per request
 constexpr int kMmMaxTiles = kMmMaxS / kMmBN;   // 1024 key tiles
 constexpr int kScatterThreads = 256;
@@ -68,7 +71,7 @@ struct MmLayout {
     static constexpr int kVP = DV / 64;                        // 64-wide panels of v
     static constexpr int kKPanel = kMmBN * 128;                // 64 rows x 128 bytes
     static constexpr int kStageBytes = (kQP + kVP) * kKPanel;  // K tile then V tile
-    static constexpr int kFixedBytes = kMmMaxTiles / 8 + kMmMaxTiles * 2 + kMmNumBars * 8 + 16 + kMmBM * 4;
+    static constexpr int kFixedBytes = kMmMaxTiles / 8 + kMmMaxTiles * 2 + kMmNumBars * 8 + 16 + kMmParts * kMmBM * 4;
     static constexpr int kStages = (232448 - kFixedBytes) / kStageBytes < kMmMaxStages
                                        ? (232448 - kFixedBytes) / kStageBytes
                                        : kMmMaxStages;
@@ -81,8 +84,8 @@ struct MmLayout {
     static constexpr int kOffList = kOffTiles + kMmMaxTiles / 8;
     static constexpr int kOffBar = kOffList + kMmMaxTiles * 2;
     static constexpr int kOffMisc = kOffBar + kMmNumBars * 8;  // tmem base, abort flag, tile count
-    static constexpr int kOffX = kOffMisc + 16;                // row maxima / sums swapped by a warp pair
-    static constexpr int kBytes = kOffX + kMmBM * 4;
+    static constexpr int kOffX = kOffMisc + 16;                // row maxima / sums swapped by a warp group
+    static constexpr int kBytes = kOffX + kMmParts * kMmBM * 4;
     // TMEM columns: S [0, 64) | P x2 (bf16 pairs) [64, 128) | Q (bf16 pairs) [128, 128 + DQK/2)
     // | O [256, 256 + DV)
     static constexpr int kColS = 0;
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         }
         ptx::mbar_init(bar(kMbSFull), 1);
         ptx::mbar_init(bar(kMbSEmpty), kMmSoftmaxWarps);
-        ptx::mbar_init(bar(kMbQFull), kMmSoftmaxWarps);
+        ptx::mbar_init(bar(kMbQFull), 8);  // the quadrants' first two warps copy Q
         ptx::mbar_init(bar(kMbQLoad), 1);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(kMbPFull + b), kMmSoftmaxWarps);
@@ -411,23 +414,27 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         __syncwarp();
     } else {
         // ================================================================ softmax / epilogue
-        // Two warps per TMEM lane quadrant: `half` 0 takes keys [0, 32) of each tile and O
-        // columns [0, DV/2), half 1 the rest.  The pair shares one named barrier per tile, a
-        // reduction that says whether any of its rows' maxima grew by more than 2^8 (or either
-        // warp gave up on a wait); only then do the two halves swap their tile maxima through
-        // shared memory.  Every thread of the pair takes the same barriers in the same order, so a
-        // warp that gives up keeps going to the next reduction, and both leave the loop there.
+        // kMmParts warps per TMEM lane quadrant: `part` takes keys [kKeys * part, kKeys * part +
+        // kKeys) of each tile and O columns [kOCols * part, kOCols * part + kOCols).  The
+        // quadrant's warps share one named barrier per tile, a reduction that says whether any of
+        // their rows' maxima grew by more than 2^8 (or one of them gave up on a wait); only then do
+        // they swap their tile maxima through shared memory.  Every thread of the group takes the
+        // same barriers in the same order, so a warp that gives up keeps going to the next
+        // reduction, and the whole group leaves the loop there.
+        constexpr int kKeys = kMmBN / kMmParts;   // keys of a tile per warp
+        constexpr int kOCols = DV / kMmParts;     // O columns per warp
+        constexpr uint32_t kGroup = 32u * kMmParts;
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int part = (warp - 2) >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const int r = quad * 32 + lane;          // query row of this thread (its TMEM lane)
         const int64_t t = t0 + r;
         const bool live = t < p.T;
         const uint32_t* mrow = p.mask + (live ? t : 0) * p.W;
         const float c = p.sm_scale_log2;
-        const uint32_t pair_bar = 1u + static_cast<uint32_t>(quad);
-        volatile float* sX = reinterpret_cast<volatile float*>(smem + L::kOffX);
-        const int ocol0 = half * (DV / 2);
+        const uint32_t grp_bar = 1u + static_cast<uint32_t>(quad);
+        volatile float* sX = reinterpret_cast<volatile float*>(smem + L::kOffX);  // [kMmParts][128]
+        const int ocol0 = part * kOCols;
         float m = -CUDART_INF_F, l = 0.f;
         bool failed = false;
         auto warp_wait = [&](int i, uint32_t parity) -> bool {
@@ -437,25 +444,39 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             __syncwarp();
             return okw;
         };
+        // this warp's kKeys mask bits of tile j (word 2k + kKeys * part / 32 of tile k)
         auto mask_word = [&](int j) -> uint32_t {
             uint32_t w = 0u;
             if (live && j < nact) {
-                const int wi = 2 * static_cast<int>(sList[j]) + half;
-                if (wi < p.W) w = __ldg(mrow + wi);
+                const int wi = 2 * static_cast<int>(sList[j]) + (kKeys * part) / 32;
+                if (wi < p.W) w = __ldg(mrow + wi) >> ((kKeys * part) % 32);
             }
             return w;
         };
-        if (nact > 0 && !(failed = !warp_wait(kMbQLoad, 0))) {
+        // the group's values of row r meet in shared memory: each posts its own, all read all
+        auto group_max = [&](float mine) -> float {
+            sX[part * kMmBM + r] = mine;
+            ptx::named_bar_sync(grp_bar, kGroup);
+            float v = sX[r];
+#pragma unroll
+            for (int q = 1; q < kMmParts; ++q) {
+                const float o = sX[q * kMmBM + r];
+                v = (v != v || o != o) ? CUDART_NAN_F : fmaxf(v, o);
+            }
+            return v;
+        };
+        if (nact > 0 && part < 2 && !(failed = !warp_wait(kMbQLoad, 0))) {
             // Q (its TMA copy issued before the pre-pass; rows past the last token are zero) into
-            // TMEM, the A operand of every S: row r in lane r, dims 2c and 2c + 1 in column c
-            // (this half: dims DQK/2 * half .. DQK/2 * half + DQK/2 - 1).  The row's 16-byte
-            // chunk q of a 64-dim SW128 panel sits at ((q ^ (r & 7)) << 4).
+            // TMEM, the A operand of every S, by the quadrant's first two warps: row r in lane r,
+            // dims 2c and 2c + 1 in column c (warp `part`: dims DQK/2 * part .. DQK/2 * part +
+            // DQK/2 - 1).  The row's 16-byte chunk q of a 64-dim SW128 panel sits at
+            // ((q ^ (r & 7)) << 4).
 #pragma unroll
             for (int cc = 0; cc < DQK / 64; ++cc) {
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int d0 = half * (DQK / 2) + 8 * (4 * cc + e);  // first dim of the chunk
+                    const int d0 = part * (DQK / 2) + 8 * (4 * cc + e);  // first dim of the chunk
                     const uint32_t q = static_cast<uint32_t>((d0 & 63) >> 3);
                     const uint4 v = ptx::ld_shared_v4(sbase + L::kOffQ + (d0 >> 6) * L::kQPanel + r * 128 +
                                                       ((q ^ static_cast<uint32_t>(r & 7)) << 4));
@@ -464,7 +485,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     w[4 * e + 2] = v.z;
                     w[4 * e + 3] = v.w;
                 }
-                SMLA_TMEM_ST16(tmem + lane_base + L::kColQ + half * (DQK / 4) + 16 * cc, w);
+                SMLA_TMEM_ST16(tmem + lane_base + L::kColQ + part * (DQK / 4) + 16 * cc, w);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -476,23 +497,23 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             const uint32_t cur = mw;
             mw = mask_word(j + 1);
             if (!failed && !warp_wait(kMbSFull, j & 1)) failed = true;
-            uint32_t sv[32];
+            uint32_t sv[kKeys];
             float mx = -CUDART_INF_F;
             if (!failed) {
                 ptx::tc_fence_after();
-                SMLA_TMEM_LD16(tmem + lane_base + L::kColS + 32 * half, sv);
-                SMLA_TMEM_LD16(tmem + lane_base + L::kColS + 32 * half + 16, sv + 16);
+#pragma unroll
+                for (int q = 0; q < kKeys / 16; ++q) SMLA_TMEM_LD16(tmem + lane_base + L::kColS + kKeys * part + 16 * q, sv + 16 * q);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kMbSEmpty));
                 // scaled logits of the set positions (log2 units) and their max (eight partial
-                // maxima: no 32-long dependency chain)
+                // maxima: no long dependency chain)
                 float mxa[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mxa[i] = -CUDART_INF_F;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < kKeys / 2; ++i) {
                     const float2 y = ptx::mul2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                                                make_float2(c, c));
                     const float x0 = (cur & (1u << (2 * i))) ? y.x : -CUDART_INF_F;
@@ -506,17 +527,9 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                            fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
             }
             bool pv_waited = false;
-            if (ptx::named_bar_red_or(pair_bar, 64u, failed || mx > m + kRescaleLog2)) {
-                // half 1 posts its tile max, half 0 posts the row's (NaN: a warp of the pair
-                // gave up)
-                if (half == 1) sX[r] = failed ? CUDART_NAN_F : mx;
-                ptx::named_bar_sync(pair_bar, 64u);
-                if (half == 0) {
-                    const float o = sX[r];
-                    sX[r] = (failed || o != o) ? CUDART_NAN_F : fmaxf(mx, o);
-                }
-                ptx::named_bar_sync(pair_bar, 64u);
-                const float v = sX[r];
+            if (ptx::named_bar_red_or(grp_bar, kGroup, failed || mx > m + kRescaleLog2)) {
+                // the row's max over the group's keys (NaN: a warp of the group gave up)
+                const float v = group_max(failed ? CUDART_NAN_F : mx);
                 if (v != v) {
                     failed = true;
                     break;
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 mx = v;
                 const bool grow = mx > m + kRescaleLog2;
                 if (__any_sync(0xffffffffu, grow)) {
-                    // the running max of some row grew by more than 2^8: that row's O half and
+                    // the running max of some row grew by more than 2^8: that row's O columns and
                     // sum are rescaled (the other rows of the warp multiply by 1); O must be
                     // complete
                     float alpha = 1.f;
@@ -537,12 +550,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     if (j > 0) {
                         if (!warp_wait(kMbPvDone, (j - 1) & 1)) {
                             failed = true;
-                            continue;  // the next reduction takes both warps of the pair out
+                            continue;  // the next reduction takes the whole group out
                         }
                         pv_waited = true;
                         ptx::tc_fence_after();
 #pragma unroll 1
-                        for (int cc = 0; cc < DV / 32; ++cc) {
+                        for (int cc = 0; cc < kOCols / 16; ++cc) {
                             uint32_t o[16];
                             SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + cc * 16, o);
                             ptx::tmem_wait_ld();
@@ -558,12 +571,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             // m is -inf only while every position seen so far is masked, and then any finite
             // offset serves); P buffer j % 2 is rewritten only after PV(j - 2) has read it
             const float nm = m == -CUDART_INF_F ? 0.f : -m;
-            uint32_t pk[16];
+            uint32_t pk[kKeys / 2];
             float2 la[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) la[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < kKeys / 2; ++i) {
                 const float2 d = ptx::add2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                                            make_float2(nm, nm));
                 const float2 pp = make_float2(ptx::ex2_approx(d.x), ptx::ex2_approx(d.y));
@@ -578,49 +591,56 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 }
             }
             // P(j) into its TMEM buffer, the operand A of PV(j): row r in lane r, keys 2c and
-            // 2c + 1 in column c (this half: keys 32 * half .. 32 * half + 31)
+            // 2c + 1 in column c (this warp: keys kKeys * part .. kKeys * part + kKeys - 1)
             ptx::tc_fence_after();
-            SMLA_TMEM_ST16(tmem + lane_base + L::kColP + (j & 1) * (kMmBN / 2) + 16 * half, pk);
+            if constexpr (kKeys == 32) {
+                SMLA_TMEM_ST16(tmem + lane_base + L::kColP + (j & 1) * (kMmBN / 2) + (kKeys / 2) * part, pk);
+            } else {
+                SMLA_TMEM_ST8(tmem + lane_base + L::kColP + (j & 1) * (kMmBN / 2) + (kKeys / 2) * part, pk);
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kMbPFull + (j & 1)));
         }
-        // ---- epilogue: O / l as bf16 and the natural-log LSE.  The pair's row sums meet in
-        // shared memory (three barriers, taken by both warps whatever happened in the loop).
+        // ---- epilogue: O / l as bf16 and the natural-log LSE.  The group's row sums meet in
+        // shared memory (two barriers, taken by every warp of the group whatever happened in the
+        // loop).
         bool have_o = nact > 0 && !failed;
         if (have_o) {
             have_o = warp_wait(kMbPvDone, (nact - 1) & 1);
             if (have_o) ptx::tc_fence_after();
         }
-        ptx::named_bar_sync(pair_bar, 64u);
-        if (half == 1) sX[r] = l;
-        ptx::named_bar_sync(pair_bar, 64u);
-        if (half == 0) sX[r] = l + sX[r];
-        ptx::named_bar_sync(pair_bar, 64u);
-        const float lt = sX[r];
+        ptx::named_bar_sync(grp_bar, kGroup);  // every read of sX in the loop is done
+        sX[part * kMmBM + r] = l;
+        ptx::named_bar_sync(grp_bar, kGroup);
+        float lt = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMmParts; ++q) lt += sX[q * kMmBM + r];
         // O goes out through shared memory (the K/V ring, idle once the last PV is done) as
         // DV/64 SW128 panels of 128 rows, then one TMA store: the rows' own global addresses are
         // h * DV * 2 bytes apart, so direct stores would touch a line per lane
         if (!failed) {
             const float inv = (have_o && lt > 0.f) ? 1.0f / lt : 0.f;
-            // this half's DV/2 columns, four 16-column TMEM loads per wait
+            // this warp's kOCols columns, up to four 16-column TMEM loads per wait
+            constexpr int kChunks = kOCols / 16;
+            constexpr int kBatch = kChunks < 4 ? kChunks : 4;
 #pragma unroll 1
-            for (int cg = 0; cg < DV / 128; ++cg) {
-                uint32_t o[4][16];
+            for (int cg = 0; cg < kChunks / kBatch; ++cg) {
+                uint32_t o[kBatch][16];
                 if (have_o) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + (4 * cg + g) * 16, o[g]);
+                    for (int g = 0; g < kBatch; ++g)
+                        SMLA_TMEM_LD16(tmem + lane_base + L::kColO + ocol0 + (kBatch * cg + g) * 16, o[g]);
                     ptx::tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
+                    for (int g = 0; g < kBatch; ++g)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) o[g][e] = 0u;
                 }
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
+                for (int g = 0; g < kBatch; ++g) {
                     uint4 v0, v1;
                     v0.x = pack_bf16x2(__uint_as_float(o[g][0]) * inv, __uint_as_float(o[g][1]) * inv);
                     v0.y = pack_bf16x2(__uint_as_float(o[g][2]) * inv, __uint_as_float(o[g][3]) * inv);
@@ -630,7 +650,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                     v1.y = pack_bf16x2(__uint_as_float(o[g][10]) * inv, __uint_as_float(o[g][11]) * inv);
                     v1.z = pack_bf16x2(__uint_as_float(o[g][12]) * inv, __uint_as_float(o[g][13]) * inv);
                     v1.w = pack_bf16x2(__uint_as_float(o[g][14]) * inv, __uint_as_float(o[g][15]) * inv);
-                    const int d0 = ocol0 + 16 * (4 * cg + g);  // first dim of chunk pair (2 x 8 dims)
+                    const int d0 = ocol0 + 16 * (kBatch * cg + g);  // first dim of chunk pair (2 x 8 dims)
                     const uint32_t prow = sbase + L::kOffKV + (d0 >> 6) * L::kQPanel + r * 128;
                     const uint32_t q0 = static_cast<uint32_t>((d0 & 63) >> 3);
                     ptx::st_shared_v4(prow + ((q0 ^ static_cast<uint32_t>(r & 7)) << 4), v0);
@@ -638,12 +658,12 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                 }
             }
             ptx::fence_proxy_async_smem();
-            if (live && half == 0)
+            if (live && part == 0)
                 p.lse[t * p.h + hh] = (have_o && lt > 0.f) ? (m + log2f(lt)) * 0.69314718055994531f : -CUDART_INF_F;
         }
         if (failed) *sAbort = 1;
-        // all eight warps' rows are in shared memory (none gave up): one thread stores the tile;
-        // rows past the last token fall outside the map and are not written
+        // all the softmax warps' rows are in shared memory (none gave up): one thread stores the
+        // tile; rows past the last token fall outside the map and are not written
         if (!ptx::named_bar_red_or(5u, 32u * kMmSoftmaxWarps, failed) && warp == 2 && lane == 0) {
             ptx::tma_store_4d(&tm_o, sbase + L::kOffKV, 0, t0, hh, 0);
             ptx::bulk_commit_group();
