@@ -9,9 +9,11 @@
 // One CTA per row.  Radix select on an order-preserving 32-bit key: a 4096-bin shared-memory
 // histogram of the keys' top 12 bits over the row, a block-wide scan of the bins from the top
 // for the bin where the count reaches k, then one more scan of the row that copies the keys of
-// that bin into shared memory (a few hundred on score distributions like a normal one).  The
-// remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates alone; when the
-// bin holds more keys than the buffer (many equal scores), those passes scan the row instead.
+// that bin into shared memory, each warp into its own region through its own counter (a few
+// hundred keys on score distributions like a normal one; one counter for the CTA serialised
+// them).  The
+// remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates alone; when a
+// warp's share overflows its region (many equal scores), those passes scan the row instead.
 // The threshold key is then exact; a last scan in position order writes every key above it and
 // the first ties at it, with a block-wide scan giving each selected position its output slot.
 // Each scan of the row takes four scores per 16-byte load when the row is 16-byte aligned; the
@@ -30,6 +32,7 @@ constexpr int kTopkPerThread = 16;                         // consecutive scores
 constexpr int kTopkChunk = kTopkThreads * kTopkPerThread;  // scores per compaction step
 constexpr int kTopkBins0 = 4096;                           // first pass: the top 12 key bits
 constexpr int kTopkCand = 2048;                            // candidate keys held in shared memory
+constexpr int kTopkCandW = kTopkCand / kTopkWarps;         // per warp
 
 struct TopkParams {
     const float* scores;         // [T, S]
@@ -125,7 +128,8 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
     __shared__ uint32_t hist[kTopkBins0];
     __shared__ uint32_t cand[kTopkCand];
     __shared__ uint32_t s_warp[2 * kTopkWarps];
-    __shared__ uint32_t s_sel[3];
+    __shared__ uint32_t s_sel[2];
+    __shared__ uint32_t s_cnt[kTopkWarps];  // candidates per warp (each warp fills its own region)
     // launched as a programmatic dependent: the scores may be the previous launch's output
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
     if (!take_all) {
         // pass 1: the top 12 bits of every key
         for (int i = threadIdx.x; i < kTopkBins0; i += kTopkThreads) hist[i] = 0;
-        if (threadIdx.x == 0) s_sel[2] = 0;
+        if (threadIdx.x < kTopkWarps) s_cnt[threadIdx.x] = 0;
         __syncthreads();
         scan_row([&](uint32_t key) { atomicAdd(&hist[key >> 20], 1u); });
         __syncthreads();
@@ -165,16 +169,22 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
         krem -= s_sel[1];
         prefix = s_sel[0] << 20;
         pmask = 0xFFF00000u;
-        // pass 2: the keys of that bin into shared memory (the count goes on past the buffer)
-        scan_row([&](uint32_t key) {
-            if ((key & pmask) == prefix) {
-                const uint32_t c = atomicAdd(&s_sel[2], 1u);
-                if (c < kTopkCand) cand[c] = key;
-            }
-        });
+        // pass 2: the keys of that bin into shared memory, each warp into its own region of the
+        // buffer through its own counter (one counter for the CTA serialised a few hundred
+        // atomics); the counts go on past the regions
+        {
+            const int w = threadIdx.x >> 5;
+            scan_row([&](uint32_t key) {
+                if ((key & pmask) == prefix) {
+                    const uint32_t c = atomicAdd(&s_cnt[w], 1u);
+                    if (c < kTopkCandW) cand[w * kTopkCandW + c] = key;
+                }
+            });
+        }
         __syncthreads();
-        const uint32_t ncand = s_sel[2];
-        const bool in_smem = ncand <= static_cast<uint32_t>(kTopkCand);
+        bool in_smem = true;
+#pragma unroll
+        for (int w = 0; w < kTopkWarps; ++w) in_smem = in_smem && s_cnt[w] <= static_cast<uint32_t>(kTopkCandW);
         // passes 3-5: key bits 19-12, 11-4 and 3-0, over the candidates (over the row when
         // they did not fit)
 #pragma unroll 1
@@ -187,7 +197,8 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
                 if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
             };
             if (in_smem) {
-                for (int c = threadIdx.x; c < static_cast<int>(ncand); c += kTopkThreads) count(cand[c]);
+                for (int c = threadIdx.x; c < kTopkCand; c += kTopkThreads)
+                    if (static_cast<uint32_t>(c % kTopkCandW) < s_cnt[c / kTopkCandW]) count(cand[c]);
             } else {
                 scan_row(count);
             }
