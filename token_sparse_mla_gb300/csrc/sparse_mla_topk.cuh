@@ -11,9 +11,9 @@
 // for the bin where the count reaches k, then one more scan of the row that copies the keys of
 // that bin into shared memory, each warp into its own region through its own counter (a few
 // hundred keys on score distributions like a normal one; one counter for the CTA serialised
-// them).  The
-// remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates alone; when a
-// warp's share overflows its region (many equal scores), those passes scan the row instead.
+// them).  The remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates
+// alone; when a warp's share overflows its region (many equal scores), those passes scan the
+// row instead.
 // The threshold key is then exact; a last scan in position order writes every key above it and
 // the first ties at it, with a block-wide scan giving each selected position its output slot.
 // Each scan of the row takes four scores per 16-byte load when the row is 16-byte aligned; the
