@@ -14,6 +14,7 @@ fixed width, only the set of selected rows matters).  Pins of the oracle, from o
 """
 
 import ctypes
+import math
 import re
 import subprocess
 from pathlib import Path
@@ -51,6 +52,14 @@ def test_short_history_selects_all_and_pads():
     assert np.all(out[0] == -1)
     assert out[1].tolist() == list(range(7)) + [-1] * 9
     assert len(set(out[2].tolist())) == 16 and -1 not in out[2]
+
+
+def test_signed_zeros_are_equal_scores():
+    # -0 and +0 are the same real number: a tie, broken towards the lower position
+    s = torch.tensor([[-0.0, 0.0, -0.0, 0.0, 1.0, -1.0], [0.0, -0.0, 2.0, -0.0, 0.0, 0.0]])
+    out = oracle.topk(s, np.array([6, 6], dtype=np.int32), 3)
+    assert out[0].tolist() == [0, 1, 4]
+    assert out[1].tolist() == [0, 1, 2]
 
 
 def test_ties_go_to_the_lower_positions():
@@ -144,7 +153,15 @@ DEV = "cuda:0"
                                         # more equal keys in the threshold's top-11-bit bin than the
                                         # shared-memory candidate buffer holds (the row-scan path)
                                         (3, 20000, 2048, "ties"), (2, 70000, 3000, "quant"),
-                                        (4, 9000, 1000, "neg")])
+                                        (4, 9000, 1000, "neg"),
+                                        # equal +0 and -0 at the threshold, on the candidate path
+                                        # (few keys in the threshold's bin) and the row-scan path
+                                        (3, 3000, 1000, "zeros"), (3, 9000, 3000, "zeros"),
+                                        # the threshold at -inf: candidates from the lowest bins
+                                        (3, 3000, 1000, "neginf"), (3, 9000, 2048, "neginf"),
+                                        (3, 3000, 777, "denorm"), (4, 20000, 2048, "rising"),
+                                        # rows that do not start on a 16-byte boundary
+                                        (5, 9999, 1500, "rand"), (3, 4097, 2048, "rand")])
 def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
     import token_sparse_mla_gb300 as smla
     s = _scores(T, S, seed=S + k)
@@ -155,6 +172,15 @@ def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
         s = torch.round(s * 4) / 4  # few distinct values: ties everywhere
     elif mode == "neg":
         s = -s.abs() - 1.0  # every score negative: the low bins of the key
+    elif mode == "zeros":
+        z = torch.where(torch.rand(T, S, generator=torch.Generator().manual_seed(S)) < 0.5, -0.0, 0.0)
+        s = torch.where(s < 0.5, z, s)  # about 69 % zeros of either sign
+    elif mode == "neginf":
+        s = torch.where(torch.rand(T, S, generator=torch.Generator().manual_seed(S)) < 0.9, -math.inf, s)
+    elif mode == "denorm":
+        s = s * 1e-39  # subnormal scores (and their zeros)
+    elif mode == "rising":
+        s = torch.arange(S, dtype=torch.float32) * 1e-3 + s * 1e-2  # the top near the row's end
     g = torch.Generator().manual_seed(T + k)
     lens = torch.randint(0, S + 1, (T,), generator=g).to(torch.int32)
     lens[0] = S
@@ -166,6 +192,26 @@ def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
         smla.sync_status()
         ref = oracle.topk(s, lens, k, block_table=bt)
         assert np.array_equal(out.cpu().numpy(), ref), f"T={T} S={S} k={k} {mode} table={bt is not None}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("in_bin", [2095, 2096, 2097])
+def test_gpu_topk_candidate_capacity_edge(in_bin):
+    """2000 scores above the threshold's 12-bit bin and in_bin in it, k = 2048: 4095 or 4096
+    candidates take the candidate path, 4097 the row scan; both exact."""
+    import token_sparse_mla_gb300 as smla
+    T, S, k = 2, 12000, 2048
+    g = torch.Generator().manual_seed(in_bin)
+    s = torch.rand(T, S, generator=g) * 0.5  # below the bin [1, 1.125)
+    for t in range(T):
+        perm = torch.randperm(S, generator=g)
+        s[t, perm[:2000]] = 10.0 + torch.rand(2000, generator=g)
+        vals = 1.0 + torch.floor(torch.rand(in_bin, generator=g) * 300) / 2400  # ties inside the bin
+        s[t, perm[2000:2000 + in_bin]] = vals
+    lens = torch.full((T,), S, dtype=torch.int32)
+    out = smla.sparse_mla_topk(s.to(DEV), lens.to(DEV), k)
+    smla.sync_status()
+    assert np.array_equal(out.cpu().numpy(), oracle.topk(s, lens, k))
 
 
 @pytest.mark.gpu

@@ -3,24 +3,27 @@
 // k as a fixed-width int32 list whose order does not matter (vLLM PR #54951, Summary and
 // Additional checks).  The pages do not give the indexer's scoring, so the scores are the
 // input here.  Row t keeps the topk positions with the largest scores among [0, len[t]), ties
-// to the lower position, written in ascending position order, mapped through a block table of
-// 64-slot blocks to cache slots (or left as positions), -1 padded when the history is shorter.
+// to the lower position (-0 and +0 are equal scores), written in ascending position order,
+// mapped through a block table of 64-slot blocks to cache slots (or left as positions), -1
+// padded when the history is shorter.
 //
-// One CTA per row.  Radix select on an order-preserving 32-bit key: a 4096-bin shared-memory
-// histogram of the keys' top 12 bits over the row, a block-wide scan of the bins from the top
-// for the bin where the count reaches k, then one more scan of the row that copies the keys of
-// that bin into shared memory, each warp into its own region through its own counter (a few
-// hundred keys on score distributions like a normal one; one counter for the CTA serialised
-// them).  The remaining 20 bits are found in passes of 8, 8 and 4 bits over those candidates
-// alone; when a warp's share overflows its region (many equal scores), those passes scan the
-// row instead.
-// The threshold key is then exact; a last scan in position order writes every key above it and
-// the first ties at it, with a block-wide scan giving each selected position its output slot.
-// Each scan of the row takes four scores per 16-byte load when the row is 16-byte aligned; the
-// first reads it from HBM, the later ones find it in L1 or L2.  So three scans of the row
-// instead of five (one histogram per byte).  256 threads a CTA: several rows share an SM and
-// one row's barrier-separated phases overlap another's scans.
+// One CTA per row, radix select on an order-preserving 32-bit key.  Pass 1 reads the row from
+// HBM into a 4096-bin shared-memory histogram of the keys' top 12 bits; a block-wide scan of
+// the bins from the top finds the bin B where the count reaches k.  Every key in a bin above B
+// is selected, so when those keys and B's own number at most 4096 (a few hundred more than k
+// on score distributions like a normal one), pass 2 reads the row once more (from L2) and
+// copies, in position order, the position of every score at or above the lowest score of bin
+// B into shared memory: a block-wide scan per 4096 scores gives each its slot.  The remaining
+// 20 key bits are then found in two 10-bit passes over those candidates alone (their scores
+// gathered once into registers, 16 a thread), and the lists come out of one more block-wide
+// scan over the candidates: two reads of the row in all.  When bin B holds too many keys
+// (many equal scores), pass 2 keeps B's keys alone (each warp in its own region while they
+// fit), 8-, 8- and 4-bit passes find the rest of the threshold, over those keys or over the
+// row, and a last scan of the row writes the lists.  Scans step 4096 scores at a time, each
+// thread four 16-byte loads a step (a warp reads 512 contiguous bytes per load).
 #pragma once
+
+#include <type_traits>
 
 #include "sparse_mla_common.cuh"
 
@@ -28,11 +31,14 @@ namespace smla {
 
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkPerThread = 16;                         // consecutive scores per thread
-constexpr int kTopkChunk = kTopkThreads * kTopkPerThread;  // scores per compaction step
-constexpr int kTopkBins0 = 4096;                           // first pass: the top 12 key bits
-constexpr int kTopkCand = 2048;                            // candidate keys held in shared memory
-constexpr int kTopkCandW = kTopkCand / kTopkWarps;         // per warp
+constexpr int kTopkGroups = 4;                               // 16-byte loads a thread per scan step
+constexpr int kTopkChunk = kTopkThreads * 4 * kTopkGroups;   // scores per scan step
+constexpr int kTopkBins0 = 4096;                             // pass 1: the top 12 key bits
+constexpr int kTopkBins1 = 1024;                             // candidate passes: 10 bits each
+constexpr int kTopkPerThread = 16;                           // candidates (or row scores) a thread
+constexpr int kTopkCand = kTopkThreads * kTopkPerThread;     // candidate positions held
+constexpr int kTopkBinKeys = 2048;                           // threshold-bin keys held otherwise
+constexpr int kTopkBinKeysW = kTopkBinKeys / kTopkWarps;     // per warp
 
 struct TopkParams {
     const float* scores;         // [T, S]
@@ -43,11 +49,25 @@ struct TopkParams {
     int32_t T, topk;
 };
 
-// Order-preserving key: a larger score gives a larger unsigned key.
+// Order-preserving key: a larger score gives a larger unsigned key, and -0 the key of +0.
 __device__ __forceinline__ uint32_t score_key(float x) {
-    const uint32_t u = __float_as_uint(x);
+    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.f));  // -0 + 0 = +0; no other value moves
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// The lowest score whose key's top 12 bits are b or more: for every score x that is not NaN,
+// x >= bin_floor(b) exactly when score_key(x) >> 20 >= b.  Bins 0-7 hold -inf and NaN keys only,
+// and their floor keys are NaN patterns, so those give -inf.
+__device__ __forceinline__ float bin_floor(uint32_t b) {
+    if (b <= 7u) return -INFINITY;
+    const uint32_t key = b << 20;
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Where candidate c sits in shared memory: within its 16-word group, xor-ed with bits 5-8 of c,
+// so that the 32 threads of a warp reading candidate e of their own 16 (c = 16 tid + e) hit 32
+// different banks.
+__device__ __forceinline__ int cand_at(int c) { return c ^ ((c >> 5) & 15); }
 
 // Exclusive block-wide prefix sums of two per-thread counts, and their block totals.
 __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb, uint32_t& ta,
@@ -68,10 +88,18 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea
         s_warp[kTopkWarps + warp] = ib;
     }
     __syncthreads();
+    uint32_t tot_a[kTopkWarps], tot_b[kTopkWarps];  // four 16-byte reads, one wavefront each
+#pragma unroll
+    for (int q = 0; q < kTopkWarps / 4; ++q) {
+        const uint4 x = reinterpret_cast<const uint4*>(s_warp)[q];
+        const uint4 y = reinterpret_cast<const uint4*>(s_warp + kTopkWarps)[q];
+        tot_a[4 * q] = x.x, tot_a[4 * q + 1] = x.y, tot_a[4 * q + 2] = x.z, tot_a[4 * q + 3] = x.w;
+        tot_b[4 * q] = y.x, tot_b[4 * q + 1] = y.y, tot_b[4 * q + 2] = y.z, tot_b[4 * q + 3] = y.w;
+    }
     uint32_t wa = 0, wb = 0, sa = 0, sb = 0;
 #pragma unroll
     for (int w = 0; w < kTopkWarps; ++w) {
-        const uint32_t va = s_warp[w], vb = s_warp[kTopkWarps + w];
+        const uint32_t va = tot_a[w], vb = tot_b[w];
         if (w < warp) {
             wa += va;
             wb += vb;
@@ -86,19 +114,21 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea
     __syncthreads();  // s_warp is reused by the next call
 }
 
-// The bin of hist[0, nb) (nb = 16, 256 or 4096) where the count of keys, taken from the top bin
-// down, reaches krem (1 <= krem <= the total): thread i covers nb / 256 bins (one when nb <=
-// 256) from the top, a block-wide scan of the threads' totals finds the one thread whose bins
-// hold the krem-th key, and that thread writes the bin and the count above it to s_sel[0..1].
-// Every thread reads them after the closing barrier.
+// The bin of hist[0, nb) (nb = 16, 256, 1024 or 4096) where the count of keys, taken from the
+// top bin down, reaches krem (1 <= krem <= the total): thread i covers nb / 256 bins (one when
+// nb <= 256) from the top, a block-wide scan of the threads' totals finds the one thread whose
+// bins hold the krem-th key, and that thread writes the bin, the count above it and the bin's
+// own count to s_sel[0..2].  Every thread reads them after the closing barrier.  The threads of
+// a warp sum their bins in rotated orders, so that each read of the warp hits 32 banks.
 __device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* s_warp,
                                               uint32_t* s_sel) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = nb > kTopkThreads ? nb / kTopkThreads : 1;
     const int top = nb - 1 - per * tid;  // this thread's highest bin
+    const int rot = (lane * per) >> 5;   // per <= 16: lanes with equal per * lane mod 32 differ here
     uint32_t tot = 0;
     if (top >= 0)
-        for (int j = 0; j < per; ++j) tot += hist[top - j];
+        for (int j = 0; j < per; ++j) tot += hist[top - ((j + rot) & (per - 1))];
     uint32_t incl = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -116,6 +146,7 @@ __device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nb, uint
             if (a + c >= krem) {
                 s_sel[0] = static_cast<uint32_t>(top - j);
                 s_sel[1] = a;
+                s_sel[2] = c;
                 break;
             }
             a += c;
@@ -124,15 +155,16 @@ __device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nb, uint
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const TopkParams p) {
-    __shared__ uint32_t hist[kTopkBins0];
-    __shared__ uint32_t cand[kTopkCand];
-    __shared__ uint32_t s_warp[2 * kTopkWarps];
-    __shared__ uint32_t s_sel[2];
-    __shared__ uint32_t s_cnt[kTopkWarps];  // candidates per warp (each warp fills its own region)
+__global__ void __launch_bounds__(kTopkThreads, 6) sparse_mla_topk_kernel(const TopkParams p) {
+    __shared__ __align__(16) uint32_t buf[kTopkBins0];  // pass-1 histogram, then the candidates
+    __shared__ uint32_t hist1[kTopkBins1];
+    __shared__ __align__(16) uint32_t s_warp[2 * kTopkWarps];
+    __shared__ uint32_t s_sel[3];
+    __shared__ uint32_t s_cnt[kTopkWarps];  // threshold-bin keys per warp (each warp its own region)
     // launched as a programmatic dependent: the scores may be the previous launch's output
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
+    const int tid = threadIdx.x;
     const int64_t t = blockIdx.x;
     const float* row = p.scores + t * p.S;
     int32_t* orow = p.out + t * p.topk;
@@ -140,105 +172,224 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
     n64 = n64 < 0 ? 0 : (n64 > p.S ? p.S : n64);  // a length outside [0, S] is clamped
     const int n = static_cast<int>(n64);
     const int k = n < p.topk ? n : p.topk;
-    const bool take_all = k == n;  // the history is no longer than topk: every position
+    auto slot_of = [&](int i) -> int32_t { return p.block_table ? __ldg(p.block_table + (i >> 6)) * 64 + (i & 63) : i; };
+    if (k == n) {  // the history is no longer than topk: all of it, then the padding
+        for (int i = tid; i < p.topk; i += kTopkThreads) orow[i] = i < n ? slot_of(i) : -1;
+        return;
+    }
 
-    // ---- radix select of the threshold key: the k-th largest
-    uint32_t prefix = 0, pmask = 0, krem = static_cast<uint32_t>(k);
-    // 16-byte loads when the row starts on a 16-byte boundary (S a multiple of 4)
+    // the scores at q .. q + 3; in a partial step (full false) those at or past n read as -inf
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-    const int n4 = vec ? n / 4 : 0;
-    auto scan_row = [&](auto&& visit) {
-        const float4* row4 = reinterpret_cast<const float4*>(row);
-        for (int i = threadIdx.x; i < n4; i += kTopkThreads) {
-            const float4 v = __ldg(row4 + i);
-            visit(score_key(v.x));
-            visit(score_key(v.y));
-            visit(score_key(v.z));
-            visit(score_key(v.w));
+    auto load4 = [&](int q, float* x, auto full) {
+        if (vec && (decltype(full)::value || q + 4 <= n)) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(row + q));
+            x[0] = v.x;
+            x[1] = v.y;
+            x[2] = v.z;
+            x[3] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                x[j] = (decltype(full)::value || q + j < n) ? __ldg(row + q + j) : -INFINITY;
         }
-        for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) visit(score_key(__ldg(row + i)));
     };
-    if (!take_all) {
-        // pass 1: the top 12 bits of every key
-        for (int i = threadIdx.x; i < kTopkBins0; i += kTopkThreads) hist[i] = 0;
-        if (threadIdx.x < kTopkWarps) s_cnt[threadIdx.x] = 0;
-        __syncthreads();
-        scan_row([&](uint32_t key) { atomicAdd(&hist[key >> 20], 1u); });
-        __syncthreads();
-        topk_find_bin(hist, kTopkBins0, krem, s_warp, s_sel);
-        krem -= s_sel[1];
-        prefix = s_sel[0] << 20;
-        pmask = 0xFFF00000u;
-        // pass 2: the keys of that bin into shared memory, each warp into its own region of the
-        // buffer through its own counter (one counter for the CTA serialised a few hundred
-        // atomics); the counts go on past the regions
-        {
-            const int w = threadIdx.x >> 5;
-            scan_row([&](uint32_t key) {
-                if ((key & pmask) == prefix) {
-                    const uint32_t c = atomicAdd(&s_cnt[w], 1u);
-                    if (c < kTopkCandW) cand[w * kTopkCandW + c] = key;
+    // one scan step: thread tid's scores of step c0 are c0 + 1024 g + 4 tid + j (g, j < 4);
+    // visit(x, g, j, valid) for each
+    auto scan_step = [&](int c0, auto full, auto&& visit) {
+        float x[kTopkGroups][4];
+#pragma unroll
+        for (int g = 0; g < kTopkGroups; ++g) load4(c0 + 1024 * g + 4 * tid, x[g], full);
+#pragma unroll
+        for (int g = 0; g < kTopkGroups; ++g)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                visit(x[g][j], g, j, decltype(full)::value || c0 + 1024 * g + 4 * tid + j < n);
+    };
+    // every step of the row: the full ones unchecked, then the partial one
+    auto scan_row = [&](auto&& step) {
+        int c0 = 0;
+        for (; c0 + kTopkChunk <= n; c0 += kTopkChunk) step(c0, std::true_type{});
+        if (c0 < n) step(c0, std::false_type{});
+    };
+
+    // ---- pass 1: histogram of the top 12 key bits
+    for (int i = tid; i < kTopkBins0 / 4; i += kTopkThreads) reinterpret_cast<uint4*>(buf)[i] = make_uint4(0, 0, 0, 0);
+    if (tid < kTopkWarps) s_cnt[tid] = 0;
+    __syncthreads();
+    scan_row([&](int c0, auto full) {
+        scan_step(c0, full, [&](float x, int, int, bool valid) {
+            if (valid) atomicAdd(&buf[score_key(x) >> 20], 1u);
+        });
+    });
+    __syncthreads();
+    uint32_t krem = static_cast<uint32_t>(k);
+    topk_find_bin(buf, kTopkBins0, krem, s_warp, s_sel);
+    const uint32_t bin = s_sel[0];
+    krem -= s_sel[1];
+    const bool few = s_sel[1] + s_sel[2] <= static_cast<uint32_t>(kTopkCand);
+    __syncthreads();  // s_sel is rewritten below; buf is free
+
+    if (few) {
+        // ---- pass 2: the positions of every score at or above bin's lowest, in position order
+        const float lo = bin_floor(bin);
+        uint32_t base = 0;
+        scan_row([&](int c0, auto full) {
+            uint32_t m = 0;  // bit 4 g + j: score c0 + 1024 g + 4 tid + j is a candidate
+            scan_step(c0, full, [&](float x, int g, int j, bool valid) {
+                m |= static_cast<uint32_t>(valid && x >= lo) << (4 * g + j);
+            });
+            // the step's candidates in position order: group g of every thread before group g + 1,
+            // threads in order within a group; two 16-bit counts a word (a group holds <= 1024)
+            const uint32_t a = __popc(m & 0xFu) | (__popc(m & 0xF0u) << 16);
+            const uint32_t b = __popc(m & 0xF00u) | (__popc(m & 0xF000u) << 16);
+            uint32_t ea, eb, ta, tb;
+            block_scan2(a, b, ea, eb, ta, tb, s_warp);
+            const uint32_t g1 = ta & 0xFFFFu, g2 = g1 + (ta >> 16), g3 = g2 + (tb & 0xFFFFu), tot = g3 + (tb >> 16);
+            // always fits unless scores are NaN; a step that would not is dropped whole, so
+            // buf[0, base) always holds positions of the row
+            if (base + tot <= static_cast<uint32_t>(kTopkCand)) {
+                const uint32_t r0 = base + (ea & 0xFFFFu), r1 = base + g1 + (ea >> 16);
+                const uint32_t r2 = base + g2 + (eb & 0xFFFFu), r3 = base + g3 + (eb >> 16);
+                // only the marked scores: a warp stores as often as its busiest thread has marks
+                for (uint32_t mm = m; mm != 0u; mm &= mm - 1u) {
+                    const int bit = __ffs(mm) - 1, g = bit >> 2;
+                    const uint32_t before = m & ((1u << bit) - 1u) & (0xFu << (4 * g));  // same group
+                    const uint32_t r = (g == 0 ? r0 : g == 1 ? r1 : g == 2 ? r2 : r3) + __popc(before);
+                    buf[cand_at(static_cast<int>(r))] = static_cast<uint32_t>(c0 + 1024 * g + 4 * tid + (bit & 3));
                 }
+                base += tot;
+            }
+        });
+        __syncthreads();
+        // ---- candidates 16 tid .. 16 tid + 15, their keys gathered once
+        const int nc = static_cast<int>(base);
+        uint32_t key[kTopkPerThread];
+        uint32_t valid = 0;
+#pragma unroll
+        for (int e = 0; e < kTopkPerThread; ++e) {
+            const int c = kTopkPerThread * tid + e;
+            key[e] = c < nc ? score_key(__ldg(row + buf[cand_at(c)])) : 0u;
+            valid |= static_cast<uint32_t>(c < nc) << e;
+        }
+        // ---- key bits 19-10, then 9-0, over the candidates in bin
+        uint32_t prefix = bin << 20, pmask = 0xFFF00000u;
+#pragma unroll 1
+        for (int shift = 10; shift >= 0; shift -= 10) {
+            for (int i = tid; i < kTopkBins1; i += kTopkThreads) hist1[i] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kTopkPerThread; ++e)
+                if (((valid >> e) & 1u) && (key[e] & pmask) == prefix)
+                    atomicAdd(&hist1[(key[e] >> shift) & (kTopkBins1 - 1)], 1u);
+            __syncthreads();
+            topk_find_bin(hist1, kTopkBins1, krem, s_warp, s_sel);
+            krem -= s_sel[1];
+            prefix |= s_sel[0] << shift;
+            pmask |= static_cast<uint32_t>(kTopkBins1 - 1) << shift;
+            __syncthreads();  // hist1 and s_sel are rewritten by the next pass
+        }
+        // ---- every candidate above the threshold key and the first krem at it, in order
+        uint32_t gt = 0, eq = 0;
+#pragma unroll
+        for (int e = 0; e < kTopkPerThread; ++e) {
+            const bool v = (valid >> e) & 1u;
+            gt |= static_cast<uint32_t>(v && key[e] > prefix) << e;
+            eq |= static_cast<uint32_t>(v && key[e] == prefix) << e;
+        }
+        uint32_t egt, eeq, tgt, teq;
+        block_scan2(__popc(gt), __popc(eq), egt, eeq, tgt, teq, s_warp);
+        for (uint32_t m = gt | eq; m != 0u; m &= m - 1u) {
+            const int e = __ffs(m) - 1;
+            int slot_out = -1;
+            if ((gt >> e) & 1u) {
+                slot_out = static_cast<int>(egt + (eeq < krem ? eeq : krem));
+                ++egt;
+            } else {
+                if (eeq < krem) slot_out = static_cast<int>(egt + eeq);
+                ++eeq;
+            }
+            if (slot_out >= 0 && slot_out < k)  // always below k; the check keeps every store in the row
+                orow[slot_out] = slot_of(static_cast<int>(buf[cand_at(kTopkPerThread * tid + e)]));
+        }
+        for (int i = k + tid; i < p.topk; i += kTopkThreads) orow[i] = -1;
+        return;
+    }
+
+    // ---- many keys in bin: its keys alone into shared memory, each warp into its own region
+    // through its own counter (one counter for the CTA serialised them); the counts go on past
+    // the regions
+    uint32_t prefix = bin << 20, pmask = 0xFFF00000u;
+    {
+        const int w = tid >> 5;
+        scan_row([&](int c0, auto full) {
+            scan_step(c0, full, [&](float x, int, int, bool valid) {
+                const uint32_t key = score_key(x);
+                if (valid && (key & pmask) == prefix) {
+                    const uint32_t c = atomicAdd(&s_cnt[w], 1u);
+                    if (c < kTopkBinKeysW) buf[w * kTopkBinKeysW + c] = key;
+                }
+            });
+        });
+    }
+    __syncthreads();
+    bool in_smem = true;
+#pragma unroll
+    for (int w = 0; w < kTopkWarps; ++w) in_smem = in_smem && s_cnt[w] <= static_cast<uint32_t>(kTopkBinKeysW);
+    // key bits 19-12, 11-4 and 3-0, over those keys (over the row when they did not fit)
+#pragma unroll 1
+    for (int step = 0; step < 3; ++step) {
+        const int shift = step == 0 ? 12 : (step == 1 ? 4 : 0);
+        const int nb = step == 2 ? 16 : 256;
+        for (int i = tid; i < nb; i += kTopkThreads) hist1[i] = 0;
+        __syncthreads();
+        auto count = [&](uint32_t key) {
+            if ((key & pmask) == prefix) atomicAdd(&hist1[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        };
+        if (in_smem) {
+            for (int c = tid; c < kTopkBinKeys; c += kTopkThreads)
+                if (static_cast<uint32_t>(c % kTopkBinKeysW) < s_cnt[c / kTopkBinKeysW]) count(buf[c]);
+        } else {
+            scan_row([&](int c0, auto full) {
+                scan_step(c0, full, [&](float x, int, int, bool valid) {
+                    if (valid) count(score_key(x));
+                });
             });
         }
         __syncthreads();
-        bool in_smem = true;
-#pragma unroll
-        for (int w = 0; w < kTopkWarps; ++w) in_smem = in_smem && s_cnt[w] <= static_cast<uint32_t>(kTopkCandW);
-        // passes 3-5: key bits 19-12, 11-4 and 3-0, over the candidates (over the row when
-        // they did not fit)
-#pragma unroll 1
-        for (int step = 0; step < 3; ++step) {
-            const int shift = step == 0 ? 12 : (step == 1 ? 4 : 0);
-            const int nb = step == 2 ? 16 : 256;
-            for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
-            __syncthreads();
-            auto count = [&](uint32_t key) {
-                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-            };
-            if (in_smem) {
-                for (int c = threadIdx.x; c < kTopkCand; c += kTopkThreads)
-                    if (static_cast<uint32_t>(c % kTopkCandW) < s_cnt[c / kTopkCandW]) count(cand[c]);
-            } else {
-                scan_row(count);
-            }
-            __syncthreads();
-            topk_find_bin(hist, nb, krem, s_warp, s_sel);
-            krem -= s_sel[1];
-            prefix |= s_sel[0] << shift;
-            pmask |= static_cast<uint32_t>(nb - 1) << shift;
-            __syncthreads();  // hist and s_sel are rewritten by the next pass
-        }
+        topk_find_bin(hist1, nb, krem, s_warp, s_sel);
+        krem -= s_sel[1];
+        prefix |= s_sel[0] << shift;
+        pmask |= static_cast<uint32_t>(nb - 1) << shift;
+        __syncthreads();  // hist1 and s_sel are rewritten by the next pass
     }
 
-    // ---- every key above the threshold and the first krem ties at it, in position order
+    // ---- every key above the threshold and the first krem at it, in position order: thread
+    // tid takes 16 consecutive scores a step
     uint32_t base_gt = 0, base_eq = 0;
-    for (int c0 = 0; c0 < n; c0 += kTopkChunk) {
-        const int i0 = c0 + static_cast<int>(threadIdx.x) * kTopkPerThread;
+    for (int c0 = 0; c0 < n; c0 += kTopkCand) {
+        const int i0 = c0 + tid * kTopkPerThread;
         float xs[kTopkPerThread];
-        if (!take_all) {
-            if (vec && i0 + kTopkPerThread <= n) {  // i0 is a multiple of 16: aligned
+        if (vec && i0 + kTopkPerThread <= n) {  // i0 is a multiple of 16: aligned
 #pragma unroll
-                for (int e = 0; e < kTopkPerThread / 4; ++e) {
-                    const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0) + e);
-                    xs[4 * e] = v.x;
-                    xs[4 * e + 1] = v.y;
-                    xs[4 * e + 2] = v.z;
-                    xs[4 * e + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < kTopkPerThread; ++e) xs[e] = i0 + e < n ? __ldg(row + i0 + e) : 0.f;
+            for (int e = 0; e < kTopkPerThread / 4; ++e) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0) + e);
+                xs[4 * e] = v.x;
+                xs[4 * e + 1] = v.y;
+                xs[4 * e + 2] = v.z;
+                xs[4 * e + 3] = v.w;
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kTopkPerThread; ++e) xs[e] = i0 + e < n ? __ldg(row + i0 + e) : 0.f;
         }
         // bit e of gt / eq: score i0 + e is above the threshold / equal to it
         uint32_t gt = 0, eq = 0;
 #pragma unroll
         for (int e = 0; e < kTopkPerThread; ++e) {
             if (i0 + e < n) {
-                const uint32_t key = take_all ? 0u : score_key(xs[e]);
-                gt |= static_cast<uint32_t>(take_all || key > prefix) << e;
-                eq |= static_cast<uint32_t>(!take_all && key == prefix) << e;
+                const uint32_t key = score_key(xs[e]);
+                gt |= static_cast<uint32_t>(key > prefix) << e;
+                eq |= static_cast<uint32_t>(key == prefix) << e;
             }
         }
         uint32_t egt, eeq, tgt, teq;
@@ -257,12 +408,12 @@ __global__ void __launch_bounds__(kTopkThreads, 5) sparse_mla_topk_kernel(const 
                 ++req;
             }
             if (slot_out >= 0 && slot_out < k)  // always below k; the check keeps every store in the row
-                orow[slot_out] = p.block_table ? __ldg(p.block_table + (i >> 6)) * 64 + (i & 63) : i;
+                orow[slot_out] = slot_of(i);
         }
         base_gt += tgt;
         base_eq += teq;
     }
-    for (int i = k + static_cast<int>(threadIdx.x); i < p.topk; i += kTopkThreads) orow[i] = -1;
+    for (int i = k + tid; i < p.topk; i += kTopkThreads) orow[i] = -1;
 }
 
 }  // namespace smla
