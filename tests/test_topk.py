@@ -195,6 +195,34 @@ def test_gpu_topk_matches_oracle_exactly(T, S, k, mode):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["rand", "zeros", "neginf", "denorm", "rising", "ties"])
+@pytest.mark.parametrize("k", [1000, 2048])
+def test_gpu_topk_long_rows_mixed_histories(mode, k):
+    """Long rows (S = 40003, off the 16-byte boundary): histories short and long in one launch,
+    each special score set, on both the candidate path and the row-scan path."""
+    import token_sparse_mla_gb300 as smla
+    S = 40000 + 3  # rows off the 16-byte boundary too
+    lens = torch.tensor([S, 3000, 9000, k - 1, 33000, 4100], dtype=torch.int32)
+    T = lens.numel()
+    g = torch.Generator().manual_seed(k)
+    s = torch.randn(T, S, generator=g)
+    if mode == "zeros":
+        z = torch.where(torch.rand(T, S, generator=g) < 0.5, -0.0, 0.0)
+        s = torch.where(s < 0.5, z, s)
+    elif mode == "neginf":
+        s = torch.where(torch.rand(T, S, generator=g) < 0.9, -math.inf, s)
+    elif mode == "denorm":
+        s = s * 1e-39
+    elif mode == "rising":
+        s = torch.arange(S, dtype=torch.float32) * 1e-3 + s * 1e-2
+    elif mode == "ties":
+        s = torch.round(s * 4) / 4
+    out = smla.sparse_mla_topk(s.to(DEV), lens.to(DEV), k)
+    smla.sync_status()
+    assert np.array_equal(out.cpu().numpy(), oracle.topk(s, lens, k)), mode
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("in_bin", [2095, 2096, 2097])
 def test_gpu_topk_candidate_capacity_edge(in_bin):
     """2000 scores above the threshold's 12-bit bin and in_bin in it, k = 2048: 4095 or 4096

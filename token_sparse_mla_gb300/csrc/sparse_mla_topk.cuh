@@ -39,6 +39,7 @@ constexpr int kTopkPerThread = 16;                           // candidates (or r
 constexpr int kTopkCand = kTopkThreads * kTopkPerThread;     // candidate positions held
 constexpr int kTopkBinKeys = 2048;                           // threshold-bin keys held otherwise
 constexpr int kTopkBinKeysW = kTopkBinKeys / kTopkWarps;     // per warp
+constexpr int kTopkWin = kTopkBins1 * 32;                    // positions a candidate bitmap covers
 
 struct TopkParams {
     const float* scores;         // [T, S]
@@ -63,11 +64,6 @@ __device__ __forceinline__ float bin_floor(uint32_t b) {
     const uint32_t key = b << 20;
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
-
-// Where candidate c sits in shared memory: within its 16-word group, xor-ed with bits 5-8 of c,
-// so that the 32 threads of a warp reading candidate e of their own 16 (c = 16 tid + e) hit 32
-// different banks.
-__device__ __forceinline__ int cand_at(int c) { return c ^ ((c >> 5) & 15); }
 
 // Exclusive block-wide prefix sums of two per-thread counts, and their block totals.
 __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb, uint32_t& ta,
@@ -230,46 +226,63 @@ __global__ void __launch_bounds__(kTopkThreads, 6) sparse_mla_topk_kernel(const 
     __syncthreads();  // s_sel is rewritten below; buf is free
 
     if (few) {
-        // ---- pass 2: the positions of every score at or above bin's lowest, in position order
+        // ---- pass 2: a bitmap of the candidates (every score at or above bin's lowest) in
+        // position order, then their positions in that order into buf, a window of kTopkWin
+        // positions at a time.  Warp w of a scan step reads positions c0 + 512 w + 32 e + lane
+        // (e < 16): one ballot per load gives 32 consecutive positions' bits.
         const float lo = bin_floor(bin);
-        uint32_t base = 0;
-        scan_row([&](int c0, auto full) {
-            uint32_t m = 0;  // bit 4 g + j: score c0 + 1024 g + 4 tid + j is a candidate
-            scan_step(c0, full, [&](float x, int g, int j, bool valid) {
-                m |= static_cast<uint32_t>(valid && x >= lo) << (4 * g + j);
-            });
-            // the step's candidates in position order: group g of every thread before group g + 1,
-            // threads in order within a group; two 16-bit counts a word (a group holds <= 1024)
-            const uint32_t a = __popc(m & 0xFu) | (__popc(m & 0xF0u) << 16);
-            const uint32_t b = __popc(m & 0xF00u) | (__popc(m & 0xF000u) << 16);
-            uint32_t ea, eb, ta, tb;
-            block_scan2(a, b, ea, eb, ta, tb, s_warp);
-            const uint32_t g1 = ta & 0xFFFFu, g2 = g1 + (ta >> 16), g3 = g2 + (tb & 0xFFFFu), tot = g3 + (tb >> 16);
-            // always fits unless scores are NaN; a step that would not is dropped whole, so
-            // buf[0, base) always holds positions of the row
-            if (base + tot <= static_cast<uint32_t>(kTopkCand)) {
-                const uint32_t r0 = base + (ea & 0xFFFFu), r1 = base + g1 + (ea >> 16);
-                const uint32_t r2 = base + g2 + (eb & 0xFFFFu), r3 = base + g3 + (eb >> 16);
-                // only the marked scores: a warp stores as often as its busiest thread has marks
-                for (uint32_t mm = m; mm != 0u; mm &= mm - 1u) {
-                    const int bit = __ffs(mm) - 1, g = bit >> 2;
-                    const uint32_t before = m & ((1u << bit) - 1u) & (0xFu << (4 * g));  // same group
-                    const uint32_t r = (g == 0 ? r0 : g == 1 ? r1 : g == 2 ? r2 : r3) + __popc(before);
-                    buf[cand_at(static_cast<int>(r))] = static_cast<uint32_t>(c0 + 1024 * g + 4 * tid + (bit & 3));
+        const int lane = tid & 31, warp = tid >> 5;
+        uint32_t* bits = hist1;  // kTopkWin / 32 words, free until the candidate passes
+        uint32_t nc = 0;
+        for (int w0 = 0; w0 < n; w0 += kTopkWin) {
+            const int wn = n - w0 < kTopkWin ? n - w0 : kTopkWin;
+            auto ballot_step = [&](int c0, auto full) {  // c0: a multiple of kTopkChunk below wn
+                const int q0 = w0 + c0 + 512 * warp + lane;
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    x[e] = (decltype(full)::value || q0 + 32 * e < n) ? __ldg(row + q0 + 32 * e) : -INFINITY;
+                uint32_t mine = 0;  // lane e < 16 keeps word e and stores it
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const uint32_t wd =
+                        __ballot_sync(0xffffffffu, (decltype(full)::value || q0 + 32 * e < n) && x[e] >= lo);
+                    mine = lane == e ? wd : mine;
                 }
-                base += tot;
+                if (lane < 16) bits[(c0 + 512 * warp) / 32 + lane] = mine;
+            };
+            int c0 = 0;
+            for (; c0 + kTopkChunk <= wn; c0 += kTopkChunk) ballot_step(c0, std::true_type{});
+            if (c0 < wn) ballot_step(c0, std::false_type{});
+            __syncthreads();
+            // thread tid's words 4 tid .. 4 tid + 3: positions w0 + 128 tid .. + 127 (words past
+            // the window's last step were not written this window: zero)
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (128 * tid < wn) v = reinterpret_cast<const uint4*>(bits)[tid];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t cnt = __popc(wv[0]) + __popc(wv[1]) + __popc(wv[2]) + __popc(wv[3]);
+            uint32_t off, off2, tot, tot2;
+            block_scan2(cnt, 0u, off, off2, tot, tot2, s_warp);
+            // always fits unless scores are NaN; a window that would not is dropped whole, so
+            // buf[0, nc) always holds positions of the row
+            if (nc + tot <= static_cast<uint32_t>(kTopkCand)) {
+                uint32_t r = nc + off;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    for (uint32_t m = wv[q]; m != 0u; m &= m - 1u)
+                        buf[r++] = static_cast<uint32_t>(w0 + 128 * tid + 32 * q + __ffs(m) - 1);
+                nc += tot;
             }
-        });
-        __syncthreads();
-        // ---- candidates 16 tid .. 16 tid + 15, their keys gathered once
-        const int nc = static_cast<int>(base);
+            __syncthreads();  // bits is rewritten by the next window (or becomes hist1)
+        }
+        // ---- candidates 512 warp + 32 e + lane (e < 16), their keys gathered once
         uint32_t key[kTopkPerThread];
         uint32_t valid = 0;
 #pragma unroll
         for (int e = 0; e < kTopkPerThread; ++e) {
-            const int c = kTopkPerThread * tid + e;
-            key[e] = c < nc ? score_key(__ldg(row + buf[cand_at(c)])) : 0u;
-            valid |= static_cast<uint32_t>(c < nc) << e;
+            const int c = 512 * warp + 32 * e + lane;
+            key[e] = c < static_cast<int>(nc) ? score_key(__ldg(row + buf[c])) : 0u;
+            valid |= static_cast<uint32_t>(c < static_cast<int>(nc)) << e;
         }
         // ---- key bits 19-10, then 9-0, over the candidates in bin
         uint32_t prefix = bin << 20, pmask = 0xFFF00000u;
@@ -288,7 +301,8 @@ __global__ void __launch_bounds__(kTopkThreads, 6) sparse_mla_topk_kernel(const 
             pmask |= static_cast<uint32_t>(kTopkBins1 - 1) << shift;
             __syncthreads();  // hist1 and s_sel are rewritten by the next pass
         }
-        // ---- every candidate above the threshold key and the first krem at it, in order
+        // ---- every candidate above the threshold key and the first krem at it, in order: the
+        // warps' counts scanned across the CTA, then within a warp one ballot per e
         uint32_t gt = 0, eq = 0;
 #pragma unroll
         for (int e = 0; e < kTopkPerThread; ++e) {
@@ -296,20 +310,35 @@ __global__ void __launch_bounds__(kTopkThreads, 6) sparse_mla_topk_kernel(const 
             gt |= static_cast<uint32_t>(v && key[e] > prefix) << e;
             eq |= static_cast<uint32_t>(v && key[e] == prefix) << e;
         }
-        uint32_t egt, eeq, tgt, teq;
-        block_scan2(__popc(gt), __popc(eq), egt, eeq, tgt, teq, s_warp);
-        for (uint32_t m = gt | eq; m != 0u; m &= m - 1u) {
-            const int e = __ffs(m) - 1;
-            int slot_out = -1;
-            if ((gt >> e) & 1u) {
-                slot_out = static_cast<int>(egt + (eeq < krem ? eeq : krem));
-                ++egt;
-            } else {
-                if (eeq < krem) slot_out = static_cast<int>(egt + eeq);
-                ++eeq;
+        const uint32_t wgt = __reduce_add_sync(0xffffffffu, __popc(gt));
+        const uint32_t weq = __reduce_add_sync(0xffffffffu, __popc(eq));
+        if (lane == 0) {
+            s_warp[warp] = wgt;
+            s_warp[kTopkWarps + warp] = weq;
+        }
+        __syncthreads();
+        uint32_t rgt = 0, req = 0;
+#pragma unroll
+        for (int w = 0; w < kTopkWarps; ++w)
+            if (w < warp) {
+                rgt += s_warp[w];
+                req += s_warp[kTopkWarps + w];
             }
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int e = 0; e < kTopkPerThread; ++e) {
+            const uint32_t bg = __ballot_sync(0xffffffffu, (gt >> e) & 1u);
+            const uint32_t be = __ballot_sync(0xffffffffu, (eq >> e) & 1u);
+            const uint32_t g_before = rgt + __popc(bg & lt), e_before = req + __popc(be & lt);
+            int slot_out = -1;
+            if ((gt >> e) & 1u)
+                slot_out = static_cast<int>(g_before + (e_before < krem ? e_before : krem));
+            else if (((eq >> e) & 1u) && e_before < krem)
+                slot_out = static_cast<int>(g_before + e_before);
             if (slot_out >= 0 && slot_out < k)  // always below k; the check keeps every store in the row
-                orow[slot_out] = slot_of(static_cast<int>(buf[cand_at(kTopkPerThread * tid + e)]));
+                orow[slot_out] = slot_of(static_cast<int>(buf[512 * warp + 32 * e + lane]));
+            rgt += __popc(bg);
+            req += __popc(be);
         }
         for (int i = k + tid; i < p.topk; i += kTopkThreads) orow[i] = -1;
         return;
