@@ -4,8 +4,9 @@ Each wrapper is driven to its C-ABI call with stand-ins: CPU tensors that report
 device, a device guard and a current stream that only record what they are given, and a
 library object that records its calls.  The checks: every wrapper passes the right pointers,
 sizes and stream handle in the order include/sparse_mla.h declares, runs the call under a
-guard for the tensors' device, and rejects tensors (or a stream) on another device, or a
-host tensor where device memory is expected, before anything reaches the library.
+guard for the tensors' device (entered only when another device is current), and rejects
+tensors (or a stream) on another device, or a host tensor where device memory is expected,
+before anything reaches the library.
 """
 
 from types import SimpleNamespace
@@ -57,11 +58,13 @@ def fake(monkeypatch):
         def __exit__(self, *exc):
             return False
 
+    current = {"index": 1}  # another device is current: every call enters the guard
     monkeypatch.setattr(_binding, "library", lambda: lib)
     monkeypatch.setattr(torch.cuda, "device", _Guard)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: current["index"])
     monkeypatch.setattr(torch.cuda, "current_stream",
                         lambda device=None: SimpleNamespace(device=device, cuda_stream=STREAM))
-    return SimpleNamespace(lib=lib, entered=entered)
+    return SimpleNamespace(lib=lib, entered=entered, current=current)
 
 
 def _d(shape, dtype, index=0):
@@ -129,9 +132,7 @@ def test_forward_host(fake):
 
 def test_forward_host_packed(fake, monkeypatch):
     T, h, topk = 4, 8, 64
-    monkeypatch.setattr(_binding, "host_io_layout",
-                        lambda T_, h_, k_: {"in_bytes": 100, "indices_offset": 64, "out_bytes": 80,
-                                           "lse_offset": 48})
+    monkeypatch.setattr(_binding, "_host_io_layout", lambda T_, h_, k_: (100, 64, 80, 48))
     inb = torch.zeros(100, dtype=torch.uint8)
     outb = torch.zeros(80, dtype=torch.uint8)
     kv = _d((50, 576), torch.bfloat16)
@@ -236,3 +237,11 @@ def test_mixed_devices_are_rejected_before_the_library(fake, what):
     with pytest.raises(ValueError):
         call()
     assert fake.lib.calls == []
+
+
+def test_no_guard_when_the_device_is_already_current(fake):
+    fake.current["index"] = 0
+    q, kv, idx, out, lse = _fwd_args()
+    smla.sparse_mla_fwd(q, kv, idx, 0.5, out=out, lse=lse)
+    assert fake.entered == []
+    assert [c[0] for c in fake.lib.calls] == ["sparse_mla_fwd_ex"]

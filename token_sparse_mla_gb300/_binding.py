@@ -1,6 +1,8 @@
 """ctypes binding of libsparse_mla.so (argument marshalling only)."""
 
+import contextlib
 import ctypes
+import functools
 from pathlib import Path
 from typing import Optional, Tuple
 
@@ -102,6 +104,12 @@ def _device_of(tensors) -> torch.device:
     return dev
 
 
+def _on(dev: torch.device):
+    """Context that makes `dev` the current device: a no-op when it already is (entering
+    torch.cuda.device costs several microseconds a call, a sizeable share of a decode step)."""
+    return contextlib.nullcontext() if torch.cuda.current_device() == dev.index else torch.cuda.device(dev)
+
+
 def _stream_handle(stream, device: Optional[torch.device] = None) -> Optional[int]:
     """Raw handle of `stream` (default: the current stream of `device`, else of the current
     device).  A stream object must belong to `device`; a raw int handle is passed as is."""
@@ -168,7 +176,7 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
     _device_of((("q", q), ("out", out), ("lse", lse)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         lib = library()
         fn = lib.sparse_mla_fwd_checked if checked else lib.sparse_mla_fwd_ex
         st = fn(
@@ -193,7 +201,7 @@ def sparse_mla_fwd_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: tor
         raise ValueError("out must be a contiguous [T, h, 512] bf16 tensor")
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_fwd_noalloc(
             q.data_ptr(), kv_cache.data_ptr(), indices.data_ptr(), T, h, topk, num_slots,
             KV_FORMATS[kv_format], float(scale), out.data_ptr(), lse.data_ptr(), int(splits),
@@ -228,7 +236,7 @@ def sparse_mla_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
     _device_of((("o_parts", o_parts), ("out", out), ("lse", lse)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, T, h,
                                         out.data_ptr(), lse.data_ptr(), _stream_handle(stream, dev))
     _check(st)
@@ -255,7 +263,7 @@ def sparse_mla_v_up(o: torch.Tensor, w: torch.Tensor, *, out: Optional[torch.Ten
     if out.shape != (T, h, v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, h, v] bf16 tensor")
     _device_of((("o", o), ("out", out)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_v_up(o.data_ptr(), w.data_ptr(), T, h, v, out.data_ptr(),
                                        _stream_handle(stream, dev))
     _check(st)
@@ -287,7 +295,7 @@ def sparse_mla_topk(scores: torch.Tensor, lengths: torch.Tensor, topk: int, *,
     if out.shape != (T, topk) or out.dtype != torch.int32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [T, topk] int32 tensor")
     _device_of((("scores", scores), ("out", out)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_topk(scores.data_ptr(), T, S, lengths.data_ptr(), int(topk),
                                        None if block_table is None else block_table.data_ptr(),
                                        out.data_ptr(), _stream_handle(stream, dev))
@@ -312,7 +320,7 @@ def sparse_mla_scatter_mask(indices: torch.Tensor, S: int, *, out: Optional[torc
     if out.shape != (T, W) or out.dtype != torch.int32 or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [T, {W}] int32 tensor")
     _device_of((("indices", indices), ("out", out)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_scatter_mask(indices.data_ptr(), T, topk, int(S), out.data_ptr(),
                                                _stream_handle(stream, dev))
     _check(st)
@@ -351,7 +359,7 @@ def sparse_mla_masked_mha(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mas
     if lse.shape != (T, h) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [T, h] fp32 tensor")
     _device_of((("q", q), ("out", out), ("lse", lse)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_masked_mha(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), T, S, h,
                                              dqk, dv, float(scale), out.data_ptr(), lse.data_ptr(),
                                              _stream_handle(stream, dev))
@@ -372,7 +380,7 @@ def sparse_mla_fwd_host(q_host: torch.Tensor, kv_cache: torch.Tensor, indices_ho
     if q_host.is_cuda or indices_host.is_cuda or out_host.is_cuda or lse_host.is_cuda:
         raise ValueError("q, indices, out and lse must be host tensors here")
     dev = _device_of((("kv_cache", kv_cache), ("workspace", workspace)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_fwd_host(
             q_host.data_ptr(), kv_cache.data_ptr(), indices_host.data_ptr(), T, h, topk,
             num_slots, KV_FORMATS[kv_format], float(scale), out_host.data_ptr(),
@@ -381,12 +389,19 @@ def sparse_mla_fwd_host(q_host: torch.Tensor, kv_cache: torch.Tensor, indices_ho
     _check(st)
 
 
-def host_io_layout(T: int, h: int, topk: int) -> dict:
-    """Sizes and offsets of the packed host buffers of sparse_mla_fwd_host_packed."""
+@functools.lru_cache(maxsize=256)
+def _host_io_layout(T: int, h: int, topk: int) -> Tuple[int, int, int, int]:
     a, b, c, d = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
     _check(library().sparse_mla_host_io_layout(T, h, topk, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
                                                ctypes.byref(d)))
-    return {"in_bytes": a.value, "indices_offset": b.value, "out_bytes": c.value, "lse_offset": d.value}
+    return a.value, b.value, c.value, d.value
+
+
+def host_io_layout(T: int, h: int, topk: int) -> dict:
+    """Sizes and offsets of the packed host buffers of sparse_mla_fwd_host_packed (the library's
+    answer, asked once per shape)."""
+    a, b, c, d = _host_io_layout(int(T), int(h), int(topk))
+    return {"in_bytes": a, "indices_offset": b, "out_bytes": c, "lse_offset": d}
 
 
 def host_io_views(in_host: torch.Tensor, out_host: torch.Tensor, T: int, h: int, topk: int):
@@ -417,11 +432,11 @@ def sparse_mla_fwd_host_packed(in_host: torch.Tensor, kv_cache: torch.Tensor, T:
             raise ValueError(f"{name} must be a contiguous uint8 tensor")
     if kv_format not in KV_FORMATS:
         raise ValueError(f"kv_format must be one of {sorted(KV_FORMATS)}")
-    lay = host_io_layout(T, h, topk)
-    if in_host.numel() < lay["in_bytes"] or out_host.numel() < lay["out_bytes"]:
+    in_bytes, _, out_bytes, _ = _host_io_layout(int(T), int(h), int(topk))
+    if in_host.numel() < in_bytes or out_host.numel() < out_bytes:
         raise ValueError("in_host / out_host smaller than host_io_layout says")
     dev = _device_of((("kv_cache", kv_cache), ("workspace", workspace)))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().sparse_mla_fwd_host_packed(
             in_host.data_ptr(), kv_cache.data_ptr(), T, h, topk, int(kv_cache.shape[0]),
             KV_FORMATS[kv_format], float(scale), out_host.data_ptr(), workspace.data_ptr(),
