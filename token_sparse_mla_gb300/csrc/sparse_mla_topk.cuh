@@ -8,19 +8,20 @@
 // padded when the history is shorter.
 //
 // One CTA per row, radix select on an order-preserving 32-bit key.  Pass 1 reads the row from
-// HBM into a 4096-bin shared-memory histogram of the keys' top 12 bits; a block-wide scan of
-// the bins from the top finds the bin B where the count reaches k.  Every key in a bin above B
-// is selected, so when those keys and B's own number at most 4096 (a few hundred more than k
-// on score distributions like a normal one), pass 2 reads the row once more (from L2) and
-// copies, in position order, the position of every score at or above the lowest score of bin
-// B into shared memory: a block-wide scan per 4096 scores gives each its slot.  The remaining
-// 20 key bits are then found in two 10-bit passes over those candidates alone (their scores
-// gathered once into registers, 16 a thread), and the lists come out of one more block-wide
-// scan over the candidates: two reads of the row in all.  When bin B holds too many keys
-// (many equal scores), pass 2 keeps B's keys alone (each warp in its own region while they
-// fit), 8-, 8- and 4-bit passes find the rest of the threshold, over those keys or over the
-// row, and a last scan of the row writes the lists.  Scans step 4096 scores at a time, each
-// thread four 16-byte loads a step (a warp reads 512 contiguous bytes per load).
+// HBM (four 16-byte loads a thread per 4096 scores) into a 4096-bin shared-memory histogram of
+// the keys' top 12 bits; a block-wide scan of the bins from the top finds the bin B where the
+// count reaches k.  Every key in a bin above B is selected, so when those keys and B's own
+// number at most 4096 (a few hundred more than k on score distributions like a normal one),
+// pass 2 reads the row once more (mostly from L2), 32 consecutive positions per warp load: one
+// warp ballot of "score >= the lowest score of bin B" per load is one word of a candidate
+// bitmap in position order.  A block-wide scan of the words' popcounts then places every
+// candidate's position in shared memory, in order.  The remaining 20 key bits are found in two
+// 10-bit passes over the candidates in B (their scores gathered once into registers, 16 a
+// thread), and the lists come out of ballots over the candidates, 32 consecutive ones per warp
+// row: two reads of the row in all.  When bin B holds too many keys (many equal scores), pass 2
+// keeps B's keys alone (each warp in its own region while they fit), 8-, 8- and 4-bit passes
+// find the rest of the threshold, over those keys or over the row, and a last scan of the row
+// writes the lists.
 #pragma once
 
 #include <type_traits>
