@@ -80,11 +80,11 @@ __device__ __forceinline__ int valid_slot(int raw, int64_t num_slots) {
     return (raw >= 0 && static_cast<int64_t>(raw) < num_slots) ? raw : -1;
 }
 
-// The KV row gather, run by producer warp pw (of kProducerWarps) for this CTA's nb blocks of
+// The KV row gather, run by producer warp pw (of NPW) for this CTA's nb blocks of
 // ROWS list entries [j0, j1).  Block b goes to stage b % NST; a stage is a ROWS-row tile in the
 // 128-byte-swizzled K-major operand layout: 9 panels of ROWS x 128 bytes, the 16-byte chunk c of
 // row r in panel p at p * ROWS * 128 + r * 128 + ((c ^ (r & 7)) << 4).  Each producer thread
-// arrives once per block on the stage's full barrier (expected count 32 * kProducerWarps) and a
+// arrives once per block on the stage's full barrier (expected count 32 * NPW) and a
 // stage is refilled only after its empty barrier completes.
 //   KVF 0: bf16 rows, copied with 16-byte cp.async, one warp instruction = 512 contiguous bytes
 //          of a row; invalid entries are zero-filled without a read.
@@ -92,22 +92,22 @@ __device__ __forceinline__ int valid_slot(int raw, int64_t num_slots) {
 //          rope]); each lane loads 16 latent bytes, its tile scale and (lanes 0-7) 16 rope bytes
 //          of a row into registers, dequantises (e4m3 -> f16 exactly, x scale in fp32, -> bf16
 //          round to nearest even) and stores into the same bf16 tile.
-template <int ROWS, int NST, int KVF>
+template <int ROWS, int NST, int KVF, int NPW>
 __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* idx_row, int j0, int j1,
                                             int nb, int pw, int lane, uint32_t sKV, uint32_t bar_full0,
                                             uint32_t bar_empty0, volatile int* sAbort) {
     constexpr int kRows = ROWS;
     constexpr int kPanelBytes = ROWS * 128;
     constexpr int kStageBytes = kPanels * kPanelBytes;
-    constexpr int kPerWarp = (ROWS + kProducerWarps - 1) / kProducerWarps;
+    constexpr int kPerWarp = (ROWS + NPW - 1) / NPW;
     auto wait_empty = [&](int s, uint32_t parity) -> bool {
         return ptx::mbar_wait(bar_empty0 + 8u * s, parity, sAbort, &g_smla_error, kErrTimeout,
                               kWaitLimitNs);
     };
-    // warp pw copies rows pw, pw + 7, pw + 14, ... of each block; lane i < kPerWarp
+    // warp pw copies rows pw, pw + NPW, pw + 2 NPW, ... of each block; lane i < kPerWarp
     // holds the slot of the warp's i-th row.
     const char* kv_bytes = reinterpret_cast<const char*>(p.kv);
-    const int my_row = pw + kProducerWarps * lane;
+    const int my_row = pw + NPW * lane;
     const bool row_owner = lane < kPerWarp && my_row < kRows;
     // The entries of this lane's row are loaded kAhead blocks (256 list entries) ahead into a
     // ring indexed by b % kAhead; the block loop is unrolled kAhead times so every ring index is
@@ -140,7 +140,7 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
                 const uint32_t st = sKV + s * kStageBytes;
 #pragma unroll 1
                 for (int i = 0; i < kPerWarp; ++i) {
-                    const int r = pw + kProducerWarps * i;
+                    const int r = pw + NPW * i;
                     if (r >= kRows) break;
                     const int slot = __shfl_sync(0xffffffffu, my_slot, i);
                     const char* src = kv_bytes + static_cast<int64_t>(slot < 0 ? 0 : slot) * (kDQK * 2);
@@ -166,7 +166,7 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
                 float scl[kPerWarp];
 #pragma unroll
                 for (int i = 0; i < kPerWarp; ++i) {
-                    const int r = pw + kProducerWarps * i;
+                    const int r = pw + NPW * i;
                     const int slot = __shfl_sync(0xffffffffu, my_slot, i);
                     lat[i] = make_uint4(0u, 0u, 0u, 0u);
                     rope[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -191,7 +191,7 @@ __device__ __forceinline__ void gather_rows(const FwdParams& p, const int32_t* i
                 const uint32_t st = sKV + s * kStageBytes;
 #pragma unroll
                 for (int i = 0; i < kPerWarp; ++i) {
-                    const int r = pw + kProducerWarps * i;
+                    const int r = pw + NPW * i;
                     if (r < kRows) {
                         const uint32_t sw = static_cast<uint32_t>(r & 7);
                         const uint32_t row_dst = st + r * 128;

@@ -8,26 +8,29 @@
 //
 // The pass is bound by the KV row gather (PR #55738 report, 功能与动机: the
 // per-token top-k MQA kernel is HBM-bound by its KV gather).  Rows are fetched
-// with 16-byte cp.async from seven producer warps, one warp per row at a time
+// with 16-byte cp.async from six producer warps, one warp per row at a time
 // (each warp instruction moves 512 contiguous bytes of a row), written straight
 // into the 128-byte-swizzled K-major operand layout; invalid entries are
 // zero-filled without a memory read.
 //
 // Roles (384 threads):
-//   warp 0      MMA issuer (one thread) and TMEM owner.  Swap-AB form, so the head
+//   warp 0      S^T issuer (one thread) and TMEM owner.  Swap-AB form, so the head
 //               count only has to fill the MMA's N dimension (no padding to 64):
 //                 S^T[64 rows, HP]        = K_blk[64 x 576] . Q^T          (M=64)
+//   warps 1-6   producers: cp.async gather of 64 rows per stage, 2 stages.
+//   warp 7      PV issuer (one thread):
 //                 O^T[512 dims, HP]      += V_blk^T[512 x 64] . P^T        (4 x M=128)
 //               V^T is read from the SAME shared-memory tile as K, as an MN-major
 //               operand.
-//   warps 1-7   producers: cp.async gather of 64 rows per stage, 2 stages.
 //   warps 8-11  softmax warpgroup: reads S^T from TMEM (16x256b loads: two KV rows and
 //               a quarter of the heads per thread, all 32 lanes busy), masks invalid
 //               entries, keeps a running max per head in log2 units and only rescales
 //               O when that max grows by more than 2^8, keeps fp32 partial softmax sums
 //               in registers, writes P^T (bf16) to shared memory, runs the epilogue.
-//   The MMA thread issues PV(b) and S^T(b+1) in whichever order their inputs arrive, so
-//   the softmax of one block overlaps the MMAs of its neighbours.
+//   A thread that issues an MMA waits while the tensor cores take it, so the two products
+//   have an issuer each: PV(b) goes out as soon as P^T(b) is ready, even while S^T(b+1)'s
+//   36 MMAs are still being issued, and the softmax of one block overlaps the MMAs of its
+//   neighbours.
 //
 // HP is the MMA N size: the head count rounded up to 16 (h = 8 runs N = 16 with
 // the upper 8 query rows zero in shared memory; nothing is padded in HBM).
@@ -41,8 +44,10 @@ constexpr int kRows = 64;                           // KV rows per pipeline stag
 constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
 constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
 constexpr int kStages = 2;
-constexpr int kThreads = 32 * (1 + kProducerWarps + 4);  // 384
-constexpr int kSoftmaxThread0 = 32 * (1 + kProducerWarps);
+constexpr int kTcProducers = 6;                         // producer warps 1 .. 6
+constexpr int kTcPvWarp = 1 + kTcProducers;             // the PV issuer's warp
+constexpr int kThreads = 32 * (kTcPvWarp + 1 + 4);      // 384
+constexpr int kSoftmaxThread0 = 32 * (kTcPvWarp + 1);
 
 template <int HP>
 struct Layout {
@@ -129,25 +134,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         *sAbort = 0;
         ptx::mbar_init(bar(kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar(kBarKvFull + s), 32 * kProducerWarps);
+            ptx::mbar_init(bar(kBarKvFull + s), 32 * kTcProducers);
             ptx::mbar_init(bar(kBarKvEmpty + s), 1);
             ptx::mbar_init(bar(kBarSFull + s), 1);
             ptx::mbar_init(bar(kBarSEmpty + s), 4);
         }
         ptx::mbar_init(bar(kBarPFull), 4);
         ptx::mbar_init(bar(kBarPvDone), 1);
-        ptx::mbar_init(bar(kBarDrain), 1);
+        ptx::mbar_init(bar(kBarDrain), 2);  // one commit from each issuer
         ptx::fence_mbarrier_init();
     }
     if (warp == 0) {
         ptx::tmem_alloc(sbase + L::kOffMisc, L::kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (warp >= 1 && warp <= kProducerWarps && p.h < HP) {
+    if (warp >= 1 && warp <= kTcProducers && p.h < HP) {
         // zero the query rows h..HP-1 of every panel (the MMA N padding of h = 8)
         const int pad_rows = HP - p.h;
         const int n16 = kPanels * pad_rows * 8;
-        for (int i = threadIdx.x - 32; i < n16; i += 32 * kProducerWarps) {
+        for (int i = threadIdx.x - 32; i < n16; i += 32 * kTcProducers) {
             const int pn = i / (pad_rows * 8);
             const int rem = i % (pad_rows * 8);
             *reinterpret_cast<uint4*>(smem + L::kOffQ + pn * HP * 128 + (p.h + rem / 8) * 128 +
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::fence_proxy_async_smem();
     }
-    if (warp > kProducerWarps) {
+    if (warp > kTcPvWarp) {
         const int wtid = threadIdx.x - kSoftmaxThread0;
         if (wtid < HP) sM[wtid] = -CUDART_INF_F;
     }
@@ -168,10 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *sTmem;
 
     if (warp == 0) {
-        // ================================================================ MMA issuer
+        // ================================================================ S^T issuer
         if (lane == 0) {
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(64, HP, 0, 0);
-            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
             ptx::prefetch_tmap(&tm_q);
             ptx::mbar_arrive_expect_tx(bar(kBarQ), static_cast<uint32_t>(kPanels * p.h * 128));
             for (int pn = 0; pn < kPanels; ++pn)
@@ -180,10 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // low 14 bits), so each operand is its base descriptor plus a constant.
             const uint64_t dq = ptx::smem_desc_sw128(sQ, 16, 1024);
             const uint64_t dkv = ptx::smem_desc_sw128(sKV, 16, 1024);
-            const uint64_t dv = ptx::smem_desc_sw128(sKV, kPanelBytes, 1024);
-            const uint64_t dp = ptx::smem_desc_sw128(sP, 16, 1024);
-            auto issue_s = [&](int b) {
+            bool ok = wait(kBarQ, 0);
+            for (int b = 0; ok && b < nb; ++b) {
+                // rows of block b landed; S^T buffer b % 2 read out by the softmax of block b - 2
                 const int s = b & 1;
+                ok = wait(kBarKvFull + s, (b >> 1) & 1);
+                if (ok && b >= 2) ok = wait(kBarSEmpty + s, ((b >> 1) - 1) & 1);
+                if (!ok) break;
+                ptx::tc_fence_after();
                 const uint64_t a0 = dkv + static_cast<uint64_t>((s * kStageBytes) >> 4);
                 const uint32_t d = tmem + L::kColS + s * HP;
 #pragma unroll
@@ -195,19 +203,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ptx::mma_commit(bar(kBarSFull + s));
-            };
-            bool ok = wait(kBarQ, 0);
-            if (ok && nb > 0) {
-                ok = wait(kBarKvFull + 0, 0);
-                if (ok) {
-                    ptx::tc_fence_after();
-                    issue_s(0);
-                }
             }
-            // Each iteration issues PV(b) and S^T(b+1), in whichever order their inputs arrive
-            // (P^T of block b from the softmax, rows of block b+1 from the producers): neither
-            // waits behind the other, so the softmax of one block overlaps its neighbours' MMAs.
-            auto issue_pv = [&](int b) {
+            // every MMA of both issuers done before TMEM is read out or released; an aborted
+            // CTA also waits for its Q copy so that nothing is in flight when it leaves
+            ptx::mma_commit(bar(kBarDrain));
+            ptx::mbar_wait(bar(kBarDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+            if (*sAbort) ptx::mbar_wait(bar(kBarQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp <= kTcProducers) {
+        // ================================================================ producers
+        gather_rows<kRows, kStages, KVF, kTcProducers>(p, idx_row, j0, j1, nb, warp - 1, lane, sKV,
+                                                       bar(kBarKvFull), bar(kBarKvEmpty), sAbort);
+    } else if (warp == kTcPvWarp) {
+        // ================================================================ PV issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
+            const uint64_t dv = ptx::smem_desc_sw128(sKV, kPanelBytes, 1024);
+            const uint64_t dp = ptx::smem_desc_sw128(sP, 16, 1024);
+            for (int b = 0; b < nb; ++b) {
+                if (!wait(kBarPFull, b & 1)) break;  // P^T of block b from the softmax
+                ptx::tc_fence_after();
                 const int s = b & 1;
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * kStageBytes) >> 4);
 #pragma unroll
@@ -220,54 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
                 ptx::mma_commit(bar(kBarPvDone));
-            };
-            for (int b = 0; ok && b < nb; ++b) {
-                const int s1 = (b + 1) & 1;
-                const uint32_t kv_par = ((b + 1) >> 1) & 1, se_par = (((b + 1) >> 1) - 1) & 1;
-                bool s_pending = b + 1 < nb;
-                bool pv_pending = true;
-                const uint64_t t0 = ptx::globaltimer_ns();
-                for (uint32_t it = 0; pv_pending; ++it) {
-                    if (s_pending && ptx::mbar_test_wait(bar(kBarKvFull + s1), kv_par) &&
-                        (b + 1 < 2 || ptx::mbar_test_wait(bar(kBarSEmpty + s1), se_par))) {
-                        ptx::tc_fence_after();
-                        issue_s(b + 1);
-                        s_pending = false;
-                    }
-                    if (ptx::mbar_test_wait(bar(kBarPFull), b & 1)) {
-                        ptx::tc_fence_after();
-                        issue_pv(b);
-                        pv_pending = false;
-                    } else if ((it & 15u) == 15u) {
-                        if (*sAbort) {
-                            ok = false;
-                            break;
-                        }
-                        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-                            *sAbort = 1;
-                            atomicOr(&g_smla_error, kErrTimeout);
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                if (ok && s_pending) {
-                    ok = wait(kBarKvFull + s1, kv_par);
-                    if (ok && b + 1 >= 2) ok = wait(kBarSEmpty + s1, se_par);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_s(b + 1);
-                }
             }
             ptx::mma_commit(bar(kBarDrain));
-            ptx::mbar_wait(bar(kBarDrain), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
-            if (*sAbort) ptx::mbar_wait(bar(kBarQ), 0, nullptr, &g_smla_error, 0u, kDrainLimitNs);
         }
         __syncwarp();
-    } else if (warp <= kProducerWarps) {
-        // ================================================================ producers
-        gather_rows<kRows, kStages, KVF>(p, idx_row, j0, j1, nb, warp - 1, lane, sKV, bar(kBarKvFull),
-                                         bar(kBarKvEmpty), sAbort);
     } else {
         // ================================================================ softmax warpgroup
         // Warp `quad` owns block rows quad*16 .. quad*16+15 (M=64 accumulator: TMEM lanes
@@ -513,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ cluster merge
         ptx::cluster_sync();  // every CTA's (m, L) is in its shared memory
         float* obuf = reinterpret_cast<float*>(smem + L::kOffKV);  // [HP][512] fp32
-        if (warp > kProducerWarps) {
+        if (warp > kTcPvWarp) {
             const int wtid = threadIdx.x - kSoftmaxThread0;
             const int quad = warp & 3;
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
@@ -565,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
         }
         ptx::cluster_sync();  // every CTA's weighted partial O is in its shared memory
-        if (warp > kProducerWarps) {
+        if (warp > kTcPvWarp) {
             // this CTA sums dims [rank*ds, (rank+1)*ds) of every head over the cluster,
             // eight dims per item, and stores them as one 16-byte vector
             const int wtid = threadIdx.x - kSoftmaxThread0;
