@@ -53,23 +53,23 @@ template <int HP>
 struct Layout {
     static_assert(HP == 16 || HP == 32 || HP == 64, "MMA N must be 16, 32 or 64");
     static constexpr int kQBytes = kPanels * HP * 128;
-    static constexpr int kPBytes = HP * 128;  // P^T: HP rows x 64 bf16
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
-    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffRed = kOffP + kPBytes;                // [4 warps][HP]
+    // P^T of block b (HP rows x 64 bf16) lives in the rope panel of block b's own stage
+    static constexpr int kOffRed = kOffKV + kStages * kStageBytes;  // [4 warps][HP]
     static constexpr int kOffM = kOffRed + 4 * HP * 4;             // running max (log2 units)
     static constexpr int kOffAlpha = kOffM + HP * 4;               // rescale factor / 1/L / merge weight
     static constexpr int kOffML = kOffAlpha + HP * 4;              // final m[HP], L[HP]
     static constexpr int kOffBar = kOffML + 2 * HP * 4;
-    static constexpr int kNumBars = 12;
+    static constexpr int kNumBars = 13;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kBytes = kOffMisc + 16;
     // TMEM columns: O^T [0,4HP) | S^T x2 [4HP,6HP)
     static constexpr int kColS = 4 * HP;
     static constexpr int kTmemCols = (6 * HP <= 128) ? 128 : ((6 * HP <= 256) ? 256 : 512);
     static_assert(6 * HP <= kTmemCols, "TMEM budget");
-    static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
+    static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled operands need 1 KB alignment");
+    static_assert(HP * 128 <= kPanelBytes, "P^T fits a stage's rope panel");
     static_assert(kBytes <= 232448, "shared memory budget (227 KB)");
     static_assert(HP * kDV * 4 <= kStages * kStageBytes, "merge buffer fits the stages");
 };
@@ -82,8 +82,8 @@ enum : int {
     kBarSFull = 5,    // +buffer
     kBarSEmpty = 7,   // +buffer
     kBarPFull = 9,
-    kBarPvDone = 10,
-    kBarDrain = 11
+    kBarPvDone = 10,  // +stage: PV of the blocks of that stage (so a wait never falls two phases behind)
+    kBarDrain = 12
 };
 
 // KVF: 0 = bf16 rows of 576 values (1152 bytes); 1 = fp8 rows of 656 bytes
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t sQ = sbase + L::kOffQ;
     const uint32_t sKV = sbase + L::kOffKV;
-    const uint32_t sP = sbase + L::kOffP;
+    const uint32_t sRope = sKV + (kPanels - 1) * kPanelBytes;  // stage 0's rope panel
     float* sRed = reinterpret_cast<float*>(smem + L::kOffRed);
     float* sM = reinterpret_cast<float*>(smem + L::kOffM);
     float* sAlpha = reinterpret_cast<float*>(smem + L::kOffAlpha);
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(bar(kBarPFull), 4);
         ptx::mbar_init(bar(kBarPvDone), 1);
+        ptx::mbar_init(bar(kBarPvDone + 1), 1);
         ptx::mbar_init(bar(kBarDrain), 2);  // one commit from each issuer
         ptx::fence_mbarrier_init();
     }
@@ -220,22 +221,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, HP, 1, 0);
             const uint64_t dv = ptx::smem_desc_sw128(sKV, kPanelBytes, 1024);
-            const uint64_t dp = ptx::smem_desc_sw128(sP, 16, 1024);
+            const uint64_t dp = ptx::smem_desc_sw128(sRope, 16, 1024);  // P^T, stage 0
             for (int b = 0; b < nb; ++b) {
                 if (!wait(kBarPFull, b & 1)) break;  // P^T of block b from the softmax
                 ptx::tc_fence_after();
                 const int s = b & 1;
                 const uint64_t v0 = dv + static_cast<uint64_t>((s * kStageBytes) >> 4);
+                const uint64_t p0 = dp + static_cast<uint64_t>((s * kStageBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t acc = (b > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         ptx::mma_bf16_ss(tmem + i * HP, v0 + ((2 * i * kPanelBytes + k * 2048) >> 4),
-                                         dp + ((k * 32) >> 4), kIdescPV, acc);
+                                         p0 + ((k * 32) >> 4), kIdescPV, acc);
                 }
                 ptx::mma_commit(bar(kBarKvEmpty + s));
-                ptx::mma_commit(bar(kBarPvDone));
+                ptx::mma_commit(bar(kBarPvDone + s));
             }
             ptx::mma_commit(bar(kBarDrain));
         }
@@ -257,9 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // raw list entries of this thread's two rows for the next block (checked when used)
         int raw0 = fetch_entry(idx_row, j0 + r0, j1, nb > 0);
         int raw1 = fetch_entry(idx_row, j0 + r1, j1, nb > 0);
-        // P^T[h][r] (128B-swizzled K-major rows of 64 bf16, eight heads per 1 KB atom)
-        auto p_addr = [&](int h, int r) -> uint32_t {
-            return sP + (h >> 3) * 1024 + (h & 7) * 128 + ((((r >> 3) ^ (h & 7)) << 4) | ((r & 7) << 1));
+        // P^T[h][r] of a block in stage s (128B-swizzled K-major rows of 64 bf16, eight heads
+        // per 1 KB atom), over the stage's rope panel: the logits are done with it, and the
+        // stage is refilled only after this block's PV
+        auto p_addr = [&](int s, int h, int r) -> uint32_t {
+            return sRope + static_cast<uint32_t>(s * kStageBytes) + (h >> 3) * 1024 + (h & 7) * 128 +
+                   ((((r >> 3) ^ (h & 7)) << 4) | ((r & 7) << 1));
         };
         // fp32 partial softmax sums of this thread's heads 8i + 2tq + e over its two rows
         float lsum[NG][2];
@@ -306,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sv[i][e] = __float_as_uint(-CUDART_INF_F);
             }
-            bool pv_waited = false;
             // one warpgroup barrier per block in the common case (no new max, no abort)
             if (ptx::named_bar_red_or(1, 128, need || failed || *sAbort)) {
                 if (ptx::named_bar_red_or(1, 128, failed || *sAbort)) {
@@ -340,12 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lsum[i][0] *= sAlpha[8 * i + 2 * tq];
                     lsum[i][1] *= sAlpha[8 * i + 2 * tq + 1];
                 }
-                if (b > 0) {
+                if (b > 0) {  // O^T complete: PV(b - 1) done
                     bool okw = true;
-                    if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
+                    if (lane == 0) okw = wait(kBarPvDone + ((b - 1) & 1), ((b - 1) >> 1) & 1);
                     okw = __shfl_sync(0xffffffffu, okw, 0);
                     __syncwarp();
-                    pv_waited = true;
                     if (okw) {
                         ptx::tc_fence_after();
 #pragma unroll 1
@@ -371,8 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // P = 2^(x - m) for this thread's 2 rows x 2*NG heads; exponentials before the wait
-            // for the previous PV (the single P^T buffer is still being read until then)
+            // P = 2^(x - m) for this thread's 2 rows x 2*NG heads
             uint16_t pb[NG][4];
 #pragma unroll
             for (int i = 0; i < NG; ++i) {
@@ -387,19 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pb[i][2 + e] = bf16_bits(p1);
                 }
             }
-            if (b > 0 && !pv_waited) {
-                bool okw = true;
-                if (lane == 0) okw = wait(kBarPvDone, (b - 1) & 1);
-                if (!__shfl_sync(0xffffffffu, okw, 0)) failed = true;
-                __syncwarp();
-            }
 #pragma unroll
             for (int i = 0; i < NG; ++i) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int h = 8 * i + 2 * tq + e;
-                    ptx::st_shared_u16(p_addr(h, r0), pb[i][e]);
-                    ptx::st_shared_u16(p_addr(h, r1), pb[i][2 + e]);
+                    ptx::st_shared_u16(p_addr(s, h, r0), pb[i][e]);
+                    ptx::st_shared_u16(p_addr(s, h, r1), pb[i][2 + e]);
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -413,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = aborted;
         if (nb > 0 && !aborted) {
             bool okw = true;
-            if (lane == 0) okw = wait(kBarPvDone, (nb - 1) & 1);
+            if (lane == 0) okw = wait(kBarPvDone + ((nb - 1) & 1), ((nb - 1) >> 1) & 1);
             okw = __shfl_sync(0xffffffffu, okw, 0);
             __syncwarp();
             if (okw) ptx::tc_fence_after();
