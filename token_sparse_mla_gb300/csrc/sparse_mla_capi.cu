@@ -234,7 +234,8 @@ Plan make_plan(int32_t T, int32_t h, int32_t topk, int32_t splits, int num_sms, 
         pl.splits = splits > 0 ? splits : auto_splits(T, nblk, num_sms);
         pl.ctas = static_cast<int64_t>(T) * pl.splits;
     }
-    pl.threads = small_heads(h) ? (fp8 ? smla::SmRoles<1>::kThreads : smla::SmRoles<0>::kThreads) : smla::kThreads;
+    pl.threads = small_heads(h) ? (fp8 ? smla::SmRoles<1>::kThreads : smla::SmRoles<0>::kThreads)
+                               : (fp8 ? smla::TcRoles<1>::kThreads : smla::TcRoles<0>::kThreads);
     pl.smem = h == 8    ? (fp8 ? smla::SmallLayout<8, 1>::kBytes : smla::SmallLayout<8, 0>::kBytes)
               : h == 16 ? (fp8 ? smla::SmallLayout<16, 1>::kBytes : smla::SmallLayout<16, 0>::kBytes)
               : h == 32 ? smla::Layout<32>::kBytes

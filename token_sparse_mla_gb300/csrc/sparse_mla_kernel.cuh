@@ -13,16 +13,18 @@
 // into the 128-byte-swizzled K-major operand layout; invalid entries are
 // zero-filled without a memory read.
 //
-// Roles (384 threads):
+// Roles (384 threads for bf16 rows, 448 for fp8 rows):
 //   warp 0      S^T issuer (one thread) and TMEM owner.  Swap-AB form, so the head
 //               count only has to fill the MMA's N dimension (no padding to 64):
 //                 S^T[64 rows, HP]        = K_blk[64 x 576] . Q^T          (M=64)
-//   warps 1-6   producers: cp.async gather of 64 rows per stage, 2 stages.
-//   warp 7      PV issuer (one thread):
+//   warps 1-NP  producers: gather of 64 rows per stage, 2 stages.  NP = 6 for bf16 rows
+//               (cp.async copies); NP = 8 for fp8 rows, whose producers dequantise in
+//               registers and hold a row's loads per lane (8 rows a warp instead of 11).
+//   warp NP+1   PV issuer (one thread):
 //                 O^T[512 dims, HP]      += V_blk^T[512 x 64] . P^T        (4 x M=128)
 //               V^T is read from the SAME shared-memory tile as K, as an MN-major
 //               operand.
-//   warps 8-11  softmax warpgroup: reads S^T from TMEM (16x256b loads: two KV rows and
+//   last 4      softmax warpgroup (warp w reads TMEM lane quadrant w % 4): reads S^T from TMEM (16x256b loads: two KV rows and
 //               a quarter of the heads per thread, all 32 lanes busy), masks invalid
 //               entries, keeps a running max per head in log2 units and only rescales
 //               O when that max grows by more than 2^8, keeps fp32 partial softmax sums
@@ -44,10 +46,13 @@ constexpr int kRows = 64;                           // KV rows per pipeline stag
 constexpr int kPanelBytes = kRows * 128;            // one panel of a 64-row stage
 constexpr int kStageBytes = kPanels * kPanelBytes;  // 73728 bytes = 64 rows x 1152
 constexpr int kStages = 2;
-constexpr int kTcProducers = 6;                         // producer warps 1 .. 6
-constexpr int kTcPvWarp = 1 + kTcProducers;             // the PV issuer's warp
-constexpr int kThreads = 32 * (kTcPvWarp + 1 + 4);      // 384
-constexpr int kSoftmaxThread0 = 32 * (kTcPvWarp + 1);
+template <int KVF>
+struct TcRoles {
+    static constexpr int kProducers = KVF == 1 ? 8 : 6;    // producer warps 1 .. kProducers
+    static constexpr int kPvWarp = 1 + kProducers;          // the PV issuer's warp
+    static constexpr int kThreads = 32 * (kPvWarp + 1 + 4); // 384 (bf16) / 448 (fp8)
+    static constexpr int kSoftmaxThread0 = 32 * (kPvWarp + 1);
+};
 
 template <int HP>
 struct Layout {
@@ -90,9 +95,12 @@ enum : int {
 // ([512 e4m3 | 4 fp32 scales, one per 128 latent values | 64 bf16 rope]), dequantised by the
 // producers into the same bf16 operand tile.
 template <int HP, int KVF>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcRoles<KVF>::kThreads, 1)
     sparse_mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const FwdParams p) {
     using L = Layout<HP>;
+    constexpr int kTcProducers = TcRoles<KVF>::kProducers;
+    constexpr int kTcPvWarp = TcRoles<KVF>::kPvWarp;
+    constexpr int kSoftmaxThread0 = TcRoles<KVF>::kSoftmaxThread0;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = ptx::smem_u32(smem);
     if (sbase & 1023u) {  // uniform across the grid: every CTA leaves before any barrier
