@@ -7,11 +7,12 @@
 // per-call o_accum split-KV buffer this avoids).
 //
 // The pass is bound by the KV row gather (PR #55738 report, 功能与动机: the
-// per-token top-k MQA kernel is HBM-bound by its KV gather).  Rows are fetched
-// with 16-byte cp.async from six producer warps, one warp per row at a time
-// (each warp instruction moves 512 contiguous bytes of a row), written straight
-// into the 128-byte-swizzled K-major operand layout; invalid entries are
-// zero-filled without a memory read.
+// per-token top-k MQA kernel is HBM-bound by its KV gather).  bf16 rows are fetched
+// with 16-byte cp.async by the producer warps, one warp per row at a time (each
+// warp instruction moves 512 contiguous bytes of a row), written straight into
+// the 128-byte-swizzled K-major operand layout; invalid entries are zero-filled
+// without a memory read.  fp8 rows are loaded into registers, dequantised and
+// stored into the same layout.
 //
 // Roles (384 threads for bf16 rows, 448 for fp8 rows):
 //   warp 0      S^T issuer (one thread) and TMEM owner.  Swap-AB form, so the head
