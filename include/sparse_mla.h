@@ -39,7 +39,10 @@
  *     (device, stream), allocated at the first call on that stream that needs it
  *     (or a larger one), cleared once, and reused.  Calls on one stream are
  *     ordered and share it; a stream capture needs one uncaptured call of the
- *     same size on that stream first (otherwise SMLA_ERR_INVALID_ARG).
+ *     same size on that stream first (otherwise SMLA_ERR_INVALID_ARG).  A
+ *     stream's scratch stays allocated until the process exits (it is keyed by
+ *     the stream handle, so a program that creates many short-lived streams
+ *     for such calls keeps one buffer for each).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).
  *   - A non-OK return means nothing was launched.  Device-side failures (a
