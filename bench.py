@@ -316,7 +316,8 @@ def per_config_runs(args, dev, stream, peaks: dict, main_entry: dict) -> dict:
         e = {"workload": name, "T": T, "h": H, "h_real": h_real, "padded_to_64": H != h_real,
              "kv_format": kv_format, "ms": ms, "query_tokens_per_s": T / (ms * 1e-3),
              "windows": 10, "steps_per_window": k * n, "gathered_bytes": gb,
-             "kernel": kernel_name(H), **roofline_fields(H, gb, row_bytes, ms, peaks)}
+             "kernel": kernel_name(H), **roofline_fields(H, gb, row_bytes, ms, peaks),
+             "traffic": ncu_traffic(name, H, H != h_real)}
         res[key] = e
         del qd, kvd, idd, out, lse, g, g1
         torch.cuda.synchronize(dev)

@@ -62,3 +62,15 @@ def test_kernel_source_hash_covers_every_kernel_source(tmp_path, monkeypatch):
     h0 = bench.kernel_source_hash()
     (src / "a.cuh").write_text("x ")
     assert bench.kernel_source_hash() != h0
+
+
+def test_per_config_traffic_keys(monkeypatch):
+    """The per-configuration entries look up traffic as (workload, heads launched, padded): the
+    native sweep at 16 and 64 heads, the prefill chunk and the native fp8 batch have launch lists;
+    padded arms have none of their own."""
+    d = json.loads((ROOT / "profiles" / "ncu_traffic.json").read_text())
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: d["kernel_source_hash"])
+    for name, h, h_real in (("sweep", 16, 16), ("sweep", 64, 64), ("prefill", 64, 64), ("fp8_mixed", 8, 8)):
+        assert bench.ncu_traffic(name, h, h != h_real) is not None, (name, h)
+    for name, h, h_real in (("sweep", 64, 8), ("fp8_mixed", 64, 8)):
+        assert bench.ncu_traffic(name, h, h != h_real) is None, (name, h)
